@@ -1,0 +1,163 @@
+"""Seeded synthetic inputs for the KDA prefill forward.
+
+This module holds shapes, distributions and seeds only: none of the method's
+arithmetic.  The CUDA path and the oracle both consume exactly the tensors made
+here (bf16 values are drawn in fp32 and rounded to nearest-even once).
+
+Workloads (K = V = 128, lower_bound = -5, scale = 1/sqrt(128)):
+  tiny      B=1, T=64, H=1, zero bf16 initial state, bf16 final state
+  batched   B=2, T=1024, H=96, bf16 initial state ~ N(0, 0.1^2), bf16 final state
+  packed3   cu_seqlens [0, 300, 1000, 2024], H=96, fp32 initial/final state
+  long      B=1, T=32768, H=32, no initial state, bf16 final state
+  packed64  64 sequences, lengths ~ U{64..8192} (seed 4), H=64, fp32 initial/final
+plus smaller variants of the same mix that the oracle evaluates in seconds.
+
+Distributions: q, k, v, g ~ N(0, 1); beta ~ U(0, 1); A_log ~ U(0, 1) [H];
+dt_bias ~ U(0, 1) [H, 128]; initial state ~ N(0, 0.1^2).  Draw order: lengths
+(packed64 and the ragged variants, always on a CPU generator), q, k, v, g, beta,
+A_log, dt_bias, initial state.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Optional
+
+import torch
+
+HEAD_DIM = 128
+
+
+@dataclass
+class Workload:
+    name: str
+    seed: int
+    H: int
+    B: int = 1
+    T: int = 0                       # tokens per batch element (batched) or total (packed)
+    seq_lens: Optional[list] = None  # packed mode when set
+    init_dtype: Optional[torch.dtype] = torch.bfloat16   # None = no initial state
+    init_zero: bool = False
+    final_dtype: torch.dtype = torch.bfloat16
+    lower_bound: float = -5.0
+    K: int = HEAD_DIM
+    V: int = HEAD_DIM
+
+    @property
+    def packed(self) -> bool:
+        return self.seq_lens is not None
+
+    @property
+    def num_seqs(self) -> int:
+        return len(self.seq_lens) if self.packed else self.B
+
+    @property
+    def total_tokens(self) -> int:
+        return self.B * self.T
+
+    @property
+    def units(self) -> int:
+        return self.num_seqs * self.H
+
+
+def _lengths(seed: int, n: int, lo: int, hi: int) -> list:
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
+
+
+def _packed(name, seed, H, lens, **kw) -> Workload:
+    return Workload(name=name, seed=seed, H=H, B=1, T=int(sum(lens)), seq_lens=list(lens), **kw)
+
+
+def workload(name: str) -> Workload:
+    """The named workload (see the module docstring)."""
+    f32, bf16 = torch.float32, torch.bfloat16
+    if name == "tiny":
+        return Workload("tiny", 0, H=1, B=1, T=64, init_dtype=bf16, init_zero=True, final_dtype=bf16)
+    if name == "batched":
+        return Workload("batched", 1, H=96, B=2, T=1024, init_dtype=bf16, final_dtype=bf16)
+    if name == "packed3":
+        return _packed("packed3", 2, 96, [300, 700, 1024], init_dtype=f32, final_dtype=f32)
+    if name == "long":
+        return Workload("long", 3, H=32, B=1, T=32768, init_dtype=None, final_dtype=bf16)
+    if name == "packed64":
+        return _packed("packed64", 4, 64, _lengths(4, 64, 64, 8192), init_dtype=f32, final_dtype=f32)
+    # Smaller cases with the same mix, several chunks and ragged tails.
+    if name == "batched_small":
+        return Workload("batched_small", 101, H=3, B=2, T=200, init_dtype=bf16, final_dtype=bf16)
+    if name == "packed3_small":
+        return _packed("packed3_small", 102, 2, [30, 70, 103], init_dtype=f32, final_dtype=f32)
+    if name == "long_small":
+        return Workload("long_small", 103, H=2, B=1, T=1000, init_dtype=None, final_dtype=bf16)
+    if name == "packed_mixed_small":
+        lens = _lengths(104, 9, 1, 300)
+        lens.insert(4, 0)  # one empty sequence
+        return _packed("packed_mixed_small", 104, 2, lens, init_dtype=f32, final_dtype=f32)
+    raise KeyError(name)
+
+
+FULL_WORKLOADS = ("tiny", "batched", "packed3", "long", "packed64")
+SMALL_WORKLOADS = ("tiny", "batched_small", "packed3_small", "long_small", "packed_mixed_small")
+
+
+@dataclass
+class Inputs:
+    w: Workload
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    g: torch.Tensor
+    beta: torch.Tensor
+    A_log: torch.Tensor
+    dt_bias: torch.Tensor
+    initial_state: Optional[torch.Tensor]
+    cu_seqlens: Optional[torch.Tensor]
+    scale: float
+    lower_bound: float
+    extra: dict = field(default_factory=dict)
+
+    def to(self, device) -> "Inputs":
+        mv = lambda t: None if t is None else t.to(device)
+        return Inputs(self.w, mv(self.q), mv(self.k), mv(self.v), mv(self.g), mv(self.beta),
+                      mv(self.A_log), mv(self.dt_bias), mv(self.initial_state), mv(self.cu_seqlens),
+                      self.scale, self.lower_bound, dict(self.extra))
+
+
+def _randn_bf16(shape, gen, device, chunk_elems=1 << 28):
+    """N(0,1) drawn in fp32 and rounded to bf16, in slabs to bound temporaries."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(-1)
+    for s in range(0, flat.numel(), chunk_elems):
+        e = min(flat.numel(), s + chunk_elems)
+        flat[s:e] = torch.randn(e - s, generator=gen, device=device, dtype=torch.float32)
+    return out
+
+
+def make_inputs(w, device="cpu") -> Inputs:
+    """Draw the workload's tensors on ``device`` from a generator seeded by ``w.seed``."""
+    if isinstance(w, str):
+        w = workload(w)
+    device = torch.device(device)
+    gen = torch.Generator(device=device).manual_seed(w.seed)
+    B, T, H, K, V = w.B, w.T, w.H, w.K, w.V
+    q = _randn_bf16((B, T, H, K), gen, device)
+    k = _randn_bf16((B, T, H, K), gen, device)
+    v = _randn_bf16((B, T, H, V), gen, device)
+    g = _randn_bf16((B, T, H, K), gen, device)
+    beta = torch.rand((B, T, H), generator=gen, device=device, dtype=torch.float32).to(torch.bfloat16)
+    A_log = torch.rand((H,), generator=gen, device=device, dtype=torch.float32)
+    dt_bias = torch.rand((H, K), generator=gen, device=device, dtype=torch.float32)
+    init = None
+    if w.init_dtype is not None:
+        shape = (w.num_seqs, H, V, K)
+        if w.init_zero:
+            init = torch.zeros(shape, dtype=w.init_dtype, device=device)
+        else:
+            init = (0.1 * torch.randn(shape, generator=gen, device=device,
+                                      dtype=torch.float32)).to(w.init_dtype)
+    cu = None
+    if w.packed:
+        cu = torch.tensor([0] + list(torch.cumsum(torch.tensor(w.seq_lens, dtype=torch.int64), 0)),
+                          dtype=torch.int64, device=device)
+    return Inputs(w, q, k, v, g, beta, A_log, dt_bias, init, cu,
+                  scale=1.0 / math.sqrt(K), lower_bound=w.lower_bound)
