@@ -1,0 +1,162 @@
+"""Thin ctypes binding of the KDA C ABI (``include/kda.h``).
+
+Argument marshalling only: every step of the forward runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+CPU fallback: if ``libkda.so`` is missing or the tensors are not on a CUDA device,
+the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_ALIAS, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(6)
+KDA_BF16, KDA_F32, KDA_I64 = 0, 1, 2
+KDA_DEVERR_CU_SEQLENS, KDA_DEVERR_TIMEOUT, KDA_DEVERR_INTERNAL = 0x1, 0x2, 0x4
+HEAD_DIM = 128
+
+# Every function include/kda.h declares.
+EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
+            "kda_read_device_status")
+
+_DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
+
+
+class KdaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4)]
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(msg)
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Load libkda.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise ImportError(f"KDA CUDA library not found at {p}; build it with "
+                              "gated_delta_rule_36_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        T = ctypes.POINTER(KdaTensor)
+        lib.kda_workspace_size.restype = ctypes.c_size_t
+        lib.kda_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int]
+        lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_fwd.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
+                                ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_last_error.restype = ctypes.c_char_p
+        lib.kda_last_error.argtypes = []
+        lib.kda_read_device_status.restype = ctypes.c_int
+        lib.kda_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                               ctypes.POINTER(ctypes.c_uint32)]
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _desc(t: Optional[torch.Tensor], name: str):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (the KDA path has no CPU fallback)")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.dim() > 4:
+        raise ValueError(f"{name}: at most 4 dims")
+    if t.dtype not in _DTYPE:
+        raise ValueError(f"{name}: unsupported dtype {t.dtype}")
+    d = KdaTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or 16)
+    d.dtype = _DTYPE[t.dtype]
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = int(s)
+    return d
+
+
+def _ref(d):
+    return None if d is None else ctypes.byref(d)
+
+
+def _check(lib, st: int):
+    if st != KDA_OK:
+        detail = lib.kda_last_error().decode()
+        raise KDAError(st, f"{lib.kda_status_string(st).decode()}: {detail}")
+
+
+def kda_workspace_size(T_total: int, H: int, N: int) -> int:
+    return int(load().kda_workspace_size(int(T_total), int(H), int(N)))
+
+
+def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+            final_state=None, cu_seqlens=None, workspace=None, stream=None):
+    """Run the forward through the C ABI.  Tensors as in ``include/kda.h``.
+
+    ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted;
+    ``stream`` defaults to torch's current stream of q's device.  Returns the
+    workspace (its first word is the device status).
+    """
+    lib = load()
+    descs = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (out, "out"),
+                                      (A_log, "A_log"), (dt_bias, "dt_bias"), (initial_state, "initial_state"),
+                                      (final_state, "final_state"), (cu_seqlens, "cu_seqlens"))]
+    dq, dk, dv, dg, db, do, da, dd, di, df, dc = descs
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    nseq = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else B
+    if workspace is None:
+        workspace = torch.empty(kda_workspace_size(B * T, H, nseq), dtype=torch.uint8, device=q.device)
+    if not (workspace.is_cuda and workspace.dtype == torch.uint8):
+        raise ValueError("workspace: must be a uint8 CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = lib.kda_fwd(_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)),
+                     _ref(do), _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di),
+                     _ref(df), _ref(dc), ctypes.c_void_p(workspace.data_ptr()),
+                     ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(sh))
+    _check(lib, st)
+    return workspace
+
+
+def kda_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    lib = load()
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    bits = ctypes.c_uint32(0)
+    _check(lib, lib.kda_read_device_status(ctypes.c_void_p(workspace.data_ptr()), ctypes.c_void_p(sh),
+                                           ctypes.byref(bits)))
+    return int(bits.value)
+
+
+def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+        final_state=None, cu_seqlens=None):
+    """FlashKDA-style convenience call: allocates the workspace, writes ``out`` and
+    ``final_state`` in place and returns ``out``."""
+    kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=initial_state,
+            final_state=final_state, cu_seqlens=cu_seqlens)
+    return out

@@ -1,0 +1,24 @@
+// Internal launch entry points of the KDA kernels (host side, not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "kda_device.cuh"
+
+namespace kda {
+
+// Sequences are sorted longest-first only up to this count; beyond it the
+// identity order is used (the sort is a quadratic rank count).
+constexpr int kMaxSortedSeqs = 8192;
+
+// Packed mode: validate cu_seqlens on the device (sets KDA_DEVERR_CU_SEQLENS) and
+// write the longest-first sequence order to `order`.
+cudaError_t launch_schedule(const int64_t* cu_seqlens, int nseq, int64_t T_total, int32_t* order,
+                            uint32_t* status, cudaStream_t stream);
+
+// Register-resident mma.sync forward (one CTA per unit).
+cudaError_t launch_fwd_mma(const FwdParams& p, cudaStream_t stream);
+size_t fwd_mma_smem_bytes();
+
+}  // namespace kda

@@ -1,0 +1,134 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention prefill forward.
+ *
+ * One call runs the whole chunked recurrent prefill of a batch on one GPU:
+ * per (sequence, head) unit and per token it applies the in-kernel gate
+ * (per-key-channel log-decay in [lower_bound, 0] from g, A_log, dt_bias),
+ * L2-normalises q and k, decays the V x K state per key channel, applies the
+ * beta-weighted delta-rule correction S += beta (v - S k) k^T and emits
+ * out = scale * S q.  Inside, tokens are processed in 32-token chunks through the
+ * centered intra-chunk matrices (Mqk, the inverse of the unit lower-triangular
+ * system) and state/output GEMMs.
+ *
+ * Sources (web pages that describe the method; the library shares no code with them):
+ *  - "FlashInfer PR #4262: Core Optimization Summary": section 1 (the fused
+ *    per-chunk pipeline), section 2 (fixed-anchor exponent centering), section 3
+ *    (chunk decomposition), sections 10 and 12 (exact in-place state alias and the
+ *    supported contract: bf16 q/k/v/g/beta, head dim 128, fp32 A_log/dt_bias,
+ *    finite negative lower_bound).
+ *  - "How FlashKDA Manages Recurrent State Across Sequences and Batch Modes":
+ *    the fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound,
+ *    initial_state, final_state, cu_seqlens) call, batched vs packed modes and the
+ *    workspace sized from (T_total, H, N).
+ *  - "How FlashKDA Stores On-Chip Recurrent State in BF16": bf16 or fp32 state I/O.
+ *
+ * Ownership: the caller owns every buffer, including the workspace.  The library
+ * never allocates, frees or synchronises a stream inside kda_fwd; all work is
+ * enqueued on `stream` in order.  All data pointers are DEVICE pointers.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL means the legacy default stream. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,   /* dtype, shape, contiguity, alignment or value check failed  */
+    KDA_ERR_UNSUPPORTED = 2,   /* valid request outside the built kernel's contract            */
+    KDA_ERR_ALIAS = 3,         /* initial/final state overlap other than an exact alias         */
+    KDA_ERR_WORKSPACE = 4,     /* workspace missing, too small or misaligned                    */
+    KDA_ERR_CUDA = 5           /* a CUDA runtime/driver call or kernel launch failed            */
+} kda_status;
+
+typedef enum { KDA_BF16 = 0, KDA_F32 = 1, KDA_I64 = 2 } kda_dtype;
+
+/* A dense, contiguous (row-major) device tensor.  data == NULL marks an absent
+ * optional tensor; the descriptor pointer itself may also be NULL for those. */
+typedef struct {
+    void* data;
+    int32_t dtype;     /* kda_dtype */
+    int32_t ndim;
+    int64_t shape[4];
+} kda_tensor;
+
+/* Head dimension handled by the kernel: K = V = 128. */
+#define KDA_HEAD_DIM 128
+/* Most negative lower_bound the chunk-32 centered operands support:
+ * 16 |lower_bound| log2(e) <= 126 keeps 2^(G - C) and 2^(C - G) normal in bf16
+ * (FlashInfer PR #4262 notes, sections 2 and 14). */
+#define KDA_MIN_LOWER_BOUND (-5.4585f)
+
+/* Device-side status bits, in the first 32-bit word of the workspace. */
+#define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] > T */
+#define KDA_DEVERR_TIMEOUT    0x2u  /* a bounded on-chip wait expired; outputs are invalid  */
+#define KDA_DEVERR_INTERNAL   0x4u  /* an internal consistency check failed                 */
+
+/*
+ * Bytes of workspace kda_fwd needs for T_total = B*T tokens, H heads and
+ * N sequences (N = B in batched mode, the number of cu_seqlens intervals in
+ * packed mode).  Mirrors get_workspace_size(T_total, H, N) of the FlashKDA API
+ * page.  The workspace holds the device status word and the longest-first
+ * sequence order; its contents need no initialisation.  Returns 0 for negative
+ * arguments.
+ */
+size_t kda_workspace_size(int64_t T_total, int H, int N);
+
+/*
+ * Run the KDA chunked prefill forward.
+ *
+ *   q, k, g, out   bf16 [B, T, H, 128]         (out is written; rows of tokens that
+ *   v              bf16 [B, T, H, 128]          belong to no sequence are NOT written)
+ *   beta           bf16 [B, T, H]               used as given (no sigmoid)
+ *   scale          finite float, applied to the normalised q
+ *   A_log          fp32 [H];   dt_bias  fp32 [H, 128]
+ *   lower_bound    finite, in [KDA_MIN_LOWER_BOUND, 0]
+ *   initial_state  NULL/absent (= zero state) or bf16/fp32 [Nseq, H, 128 (V), 128 (K)]
+ *   final_state    NULL/absent (not stored) or bf16/fp32 [Nseq, H, 128, 128]; may be the
+ *                  exact same allocation (same pointer, dtype and shape) as initial_state
+ *                  for an in-place update; any other overlap is KDA_ERR_ALIAS
+ *   cu_seqlens     NULL/absent = batched mode (Nseq = B, one chain per batch row);
+ *                  else int64 [N+1] with B == 1 (packed mode, Nseq = N): sequence n is
+ *                  tokens [cu_seqlens[n], cu_seqlens[n+1]) and starts from
+ *                  initial_state[n] (or zero); no state crosses a boundary
+ *   workspace      >= kda_workspace_size(B*T, H, Nseq) bytes, 256-byte aligned
+ *   stream         stream the work is enqueued on
+ *
+ * All tensors must be contiguous with 16-byte aligned data (beta: 2-byte).
+ * Host-detectable problems return a status before anything is enqueued.  Problems
+ * only the device can see (cu_seqlens contents, an expired bounded wait) set
+ * KDA_DEVERR_* bits in the workspace; read them with kda_read_device_status.
+ * A call whose cu_seqlens fail the device check writes neither out nor final_state.
+ */
+kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                   const kda_tensor* g, const kda_tensor* beta, float scale,
+                   const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                   float lower_bound, const kda_tensor* initial_state,
+                   const kda_tensor* final_state, const kda_tensor* cu_seqlens,
+                   void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/* Static description of a status code. */
+const char* kda_status_string(kda_status s);
+
+/* Human-readable detail of the last non-OK status returned on this host thread. */
+const char* kda_last_error(void);
+
+/*
+ * Wait for `stream`, then copy the device status word of the last kda_fwd that
+ * used `workspace` into *bits (0 = no device-side error).  Synchronises the
+ * stream: meant for tests and debugging, not for the hot path.
+ */
+kda_status kda_read_device_status(const void* workspace, kda_stream_t stream, uint32_t* bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

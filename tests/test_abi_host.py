@@ -1,0 +1,124 @@
+"""Host-only checks of the C ABI (no GPU, no compute calls).
+
+The library must build for sm_103a, load, and export every function
+``include/kda.h`` declares.  Invalid requests must be rejected with the right
+status before anything is enqueued, so these calls use fake device addresses.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_36_gb300 import binding as kb
+from gated_delta_rule_36_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kb.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert set(declared_functions()) == set(kb.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_workspace_size(lib):
+    assert kb.kda_workspace_size(0, 1, 0) >= 256 + 4
+    assert kb.kda_workspace_size(2048, 96, 3) >= 256 + 3 * 4
+    assert kb.kda_workspace_size(270000, 64, 64) % 256 == 0
+    assert lib.kda_workspace_size(-1, 1, 1) == 0
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.kda_status_string(s)
+
+
+BASE = 0x7F0000000000  # fake, 256-byte aligned device addresses: never dereferenced
+
+
+def T(dtype, shape, addr):
+    d = kb.KdaTensor()
+    d.data = addr
+    d.dtype = dtype
+    d.ndim = len(shape)
+    for i, s in enumerate(shape):
+        d.shape[i] = s
+    return d
+
+
+def call(lib, **over):
+    B, Tn, H = over.pop("BTH", (1, 64, 2))
+    a = dict(
+        q=T(kb.KDA_BF16, (B, Tn, H, 128), BASE + 0x0000000),
+        k=T(kb.KDA_BF16, (B, Tn, H, 128), BASE + 0x1000000),
+        v=T(kb.KDA_BF16, (B, Tn, H, 128), BASE + 0x2000000),
+        g=T(kb.KDA_BF16, (B, Tn, H, 128), BASE + 0x3000000),
+        beta=T(kb.KDA_BF16, (B, Tn, H), BASE + 0x4000000),
+        out=T(kb.KDA_BF16, (B, Tn, H, 128), BASE + 0x5000000),
+        A_log=T(kb.KDA_F32, (H,), BASE + 0x6000000),
+        dt_bias=T(kb.KDA_F32, (H, 128), BASE + 0x7000000),
+        init=None, final=None, cu=None, scale=0.088, lb=-5.0,
+        ws=BASE + 0x9000000, ws_bytes=1 << 20)
+    a.update(over)
+    r = lambda d: None if d is None else ctypes.byref(d)
+    return lib.kda_fwd(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]), ctypes.c_float(a["scale"]),
+                       r(a["out"]), r(a["A_log"]), r(a["dt_bias"]), ctypes.c_float(a["lb"]), r(a["init"]),
+                       r(a["final"]), r(a["cu"]), ctypes.c_void_p(a["ws"]), ctypes.c_size_t(a["ws_bytes"]),
+                       ctypes.c_void_p(0))
+
+
+def test_rejections(lib):
+    st = lambda d, H=2: T(d, (1, H, 128, 128), BASE + 0x8000000)
+    cases = [
+        (dict(q=T(kb.KDA_F32, (1, 64, 2, 128), BASE)), kb.KDA_ERR_INVALID_ARG),
+        (dict(q=T(kb.KDA_BF16, (1, 64, 2, 64), BASE)), kb.KDA_ERR_UNSUPPORTED),
+        (dict(q=None), kb.KDA_ERR_INVALID_ARG),
+        (dict(k=T(kb.KDA_BF16, (1, 63, 2, 128), BASE + 0x1000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(beta=T(kb.KDA_BF16, (1, 64, 3), BASE + 0x4000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(A_log=T(kb.KDA_BF16, (2,), BASE + 0x6000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(dt_bias=T(kb.KDA_F32, (2, 64), BASE + 0x7000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(lb=0.5), kb.KDA_ERR_INVALID_ARG),
+        (dict(lb=float("nan")), kb.KDA_ERR_INVALID_ARG),
+        (dict(lb=-6.0), kb.KDA_ERR_UNSUPPORTED),
+        (dict(scale=float("inf")), kb.KDA_ERR_INVALID_ARG),
+        (dict(q=T(kb.KDA_BF16, (1, 64, 2, 128), BASE + 8)), kb.KDA_ERR_INVALID_ARG),
+        (dict(init=T(kb.KDA_F32, (1, 2, 128, 64), BASE + 0x8000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(final=T(kb.KDA_I64, (1, 2, 128, 128), BASE + 0x8000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(init=st(kb.KDA_F32), final=T(kb.KDA_F32, (1, 2, 128, 128), BASE + 0x8000000 + 4096)),
+         kb.KDA_ERR_ALIAS),
+        (dict(init=st(kb.KDA_F32), final=st(kb.KDA_BF16)), kb.KDA_ERR_ALIAS),
+        (dict(BTH=(2, 32, 2), cu=T(kb.KDA_I64, (3,), BASE + 0xA000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(cu=T(kb.KDA_F32, (3,), BASE + 0xA000000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(cu=T(kb.KDA_I64, (3,), BASE + 0xA000000), init=st(kb.KDA_F32)), kb.KDA_ERR_INVALID_ARG),
+        (dict(ws=BASE + 0x9000000 + 16), kb.KDA_ERR_WORKSPACE),
+        (dict(ws=0), kb.KDA_ERR_WORKSPACE),
+        (dict(ws_bytes=16), kb.KDA_ERR_WORKSPACE),
+    ]
+    for over, expect in cases:
+        got = call(lib, **over)
+        assert got == expect, (over, got, lib.kda_last_error())
+        assert lib.kda_last_error(), over
+
+
+def test_binding_refuses_host_tensors():
+    import torch
+    x = torch.zeros(1, 4, 1, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kb.kda_fwd(x, x, x, x, torch.zeros(1, 4, 1, dtype=torch.bfloat16), 1.0, x.clone(),
+                   torch.zeros(1), torch.zeros(1, 128), -5.0, workspace=torch.zeros(512, dtype=torch.uint8))
