@@ -3,8 +3,8 @@
 Public API (thin ctypes binding of ``include/kda.h``):
   kda_fwd, kda_workspace_size, kda_read_device_status, fwd
 """
-from .binding import (KDAError, fwd, kda_fwd, kda_read_device_status,  # noqa: F401
+from .binding import (KDAError, fwd, kda_fwd, kda_fwd_no_alloc, kda_read_device_status,  # noqa: F401
                       kda_workspace_size, load, library_path)
 
-__all__ = ["KDAError", "fwd", "kda_fwd", "kda_read_device_status", "kda_workspace_size", "load",
+__all__ = ["KDAError", "fwd", "kda_fwd", "kda_fwd_no_alloc", "kda_read_device_status", "kda_workspace_size", "load",
            "library_path"]

@@ -23,7 +23,7 @@ HEAD_DIM = 128
 
 # Every function include/kda.h declares.
 EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
-            "kda_read_device_status")
+            "kda_read_device_status", "kda_fwd_no_alloc")
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
 
@@ -71,6 +71,9 @@ def load(path: Optional[str] = None):
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_uint32)]
+        lib.kda_fwd_no_alloc.restype = ctypes.c_int
+        lib.kda_fwd_no_alloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
+                                         ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
         if path is None:
             _lib = lib
         return lib
@@ -142,15 +145,42 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     return workspace
 
 
-def kda_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+def kda_read_device_status(workspace, stream=None) -> int:
+    """Status bits of the last call that used ``workspace`` (a uint8 CUDA tensor, or
+    the device address kda_fwd_no_alloc returns).  Synchronises the stream."""
     lib = load()
+    if isinstance(workspace, torch.Tensor):
+        addr, device = workspace.data_ptr(), workspace.device
+    else:
+        addr, device = int(workspace), torch.device("cuda", torch.cuda.current_device())
     if stream is None:
-        stream = torch.cuda.current_stream(workspace.device)
+        stream = torch.cuda.current_stream(device)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
     bits = ctypes.c_uint32(0)
-    _check(lib, lib.kda_read_device_status(ctypes.c_void_p(workspace.data_ptr()), ctypes.c_void_p(sh),
-                                           ctypes.byref(bits)))
+    _check(lib, lib.kda_read_device_status(ctypes.c_void_p(addr), ctypes.c_void_p(sh), ctypes.byref(bits)))
     return int(bits.value)
+
+
+def kda_fwd_no_alloc(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+                     final_state=None, cu_seqlens=None, stream=None) -> int:
+    """kda_fwd for callers that cannot allocate device memory: the library uses its
+    own fixed device array (KDA_NO_ALLOC_MAX_SEQS sequences at most) as the workspace
+    and nothing is allocated.  Calls that overlap on the GPU share that array and
+    race.  Returns the array's device address (for kda_read_device_status)."""
+    lib = load()
+    descs = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (out, "out"),
+                                      (A_log, "A_log"), (dt_bias, "dt_bias"), (initial_state, "initial_state"),
+                                      (final_state, "final_state"), (cu_seqlens, "cu_seqlens"))]
+    dq, dk, dv, dg, db, do, da, dd, di, df, dc = descs
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    used = ctypes.c_void_p(0)
+    st = lib.kda_fwd_no_alloc(_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)),
+                              _ref(do), _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di),
+                              _ref(df), _ref(dc), ctypes.c_void_p(sh), ctypes.byref(used))
+    _check(lib, st)
+    return int(used.value or 0)
 
 
 def fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,

@@ -64,6 +64,11 @@ kda_status check_state(const char* name, const kda_tensor* t, int64_t nseq, int6
 
 }  // namespace
 
+namespace kda {
+// Record a message for kda_last_error() from another translation unit of the library.
+void set_last_error(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace kda
+
 extern "C" {
 
 size_t kda_workspace_size(int64_t T_total, int H, int N) {

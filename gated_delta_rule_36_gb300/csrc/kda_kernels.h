@@ -22,3 +22,8 @@ cudaError_t launch_fwd_mma(const FwdParams& p, cudaStream_t stream);
 size_t fwd_mma_smem_bytes();
 
 }  // namespace kda
+
+namespace kda {
+// Set the text kda_last_error() returns on this host thread.
+void set_last_error(const char* msg);
+}  // namespace kda

@@ -127,6 +127,39 @@ const char* kda_last_error(void);
  */
 kda_status kda_read_device_status(const void* workspace, kda_stream_t stream, uint32_t* bits);
 
+/* Largest number of sequences (N in packed mode, B in batched mode) that
+ * kda_fwd_no_alloc accepts: its built-in workspace is 256 + 4 * this many bytes. */
+#define KDA_NO_ALLOC_MAX_SEQS 16384
+
+/*
+ * The same forward as kda_fwd, for callers that cannot allocate device memory and
+ * so cannot pass a workspace: for example a plugin inside a host framework that owns
+ * the whole device memory pool and gives its plugins no allocator, or a serving loop
+ * that must never allocate at run time.  The pages describe no counterpart of this
+ * call; it is an addition of this library.
+ *
+ * Arguments, results and errors are those of kda_fwd, minus the workspace.  The
+ * workspace is instead a fixed array in the library's own device memory
+ * (256 + 4 * KDA_NO_ALLOC_MAX_SEQS bytes), which every GPU that loads the library
+ * holds until the process exits.  Nothing in this call allocates or frees memory.
+ *  - More than KDA_NO_ALLOC_MAX_SEQS sequences: KDA_ERR_UNSUPPORTED, nothing enqueued.
+ *  - The first call on a device looks up the array's device address on that device
+ *    (the stream's device, made current for the lookup); make that first call before
+ *    any stream capture.
+ *  - Every call on a device shares the one array, and the array keeps what the last
+ *    call left in it (kda_fwd clears the status word at the start of each call).
+ *    Calls whose work overlaps on the GPU (for example on two streams at once) race
+ *    on it: order them on one stream or with events.
+ *  - If workspace_used is not NULL it receives the array's device address, so the
+ *    status word can be read with kda_read_device_status.
+ */
+kda_status kda_fwd_no_alloc(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                            const kda_tensor* g, const kda_tensor* beta, float scale,
+                            const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                            float lower_bound, const kda_tensor* initial_state,
+                            const kda_tensor* final_state, const kda_tensor* cu_seqlens,
+                            kda_stream_t stream, const void** workspace_used);
+
 #ifdef __cplusplus
 }
 #endif
