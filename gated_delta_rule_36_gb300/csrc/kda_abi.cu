@@ -4,6 +4,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "kda.h"
@@ -191,7 +192,13 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     p.scale = scale;
     p.lower_bound = lower_bound;
 
-    e = kda::launch_fwd_mma(p, s);
+    // KDA_FWD_KERNEL=mma selects the register-state ablation kernel; the default is
+    // the tcgen05 kernel with the state resident in TMEM.
+    static const bool use_mma = [] {
+        const char* v = getenv("KDA_FWD_KERNEL");
+        return v != nullptr && strcmp(v, "mma") == 0;
+    }();
+    e = use_mma ? kda::launch_fwd_mma(p, s) : kda::launch_fwd_tc(p, s);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }

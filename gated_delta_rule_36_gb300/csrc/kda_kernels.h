@@ -17,9 +17,14 @@ constexpr int kMaxSortedSeqs = 8192;
 cudaError_t launch_schedule(const int64_t* cu_seqlens, int nseq, int64_t T_total, int32_t* order,
                             uint32_t* status, cudaStream_t stream);
 
-// Register-resident mma.sync forward (one CTA per unit).
+// Register-resident mma.sync forward (one CTA per unit): the ablation variant that
+// keeps the state in mma.sync accumulator registers.
 cudaError_t launch_fwd_mma(const FwdParams& p, cudaStream_t stream);
 size_t fwd_mma_smem_bytes();
+
+// tcgen05 forward (one CTA per unit, two per SM, state resident in TMEM).
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream);
+size_t fwd_tc_smem_bytes();
 
 }  // namespace kda
 
