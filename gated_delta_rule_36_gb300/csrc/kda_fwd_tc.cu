@@ -5,26 +5,29 @@
 // section 6); the recurrent GEMMs run as tcgen05.mma with fp32 TMEM accumulators,
 // and the small intra-chunk products as warp-level mma.sync (section 7).
 //
-// Warp roles (320 threads):
-//   warps 0-3  TMEM group: thread v owns state row v (TMEM lane v).  Decays S,
-//              turns P into R = (V^T - P) diag(beta), converts U to bf16, drains the
-//              chunk output O, refreshes the bf16 copy of S, loads/stores the state.
-//   warp 4     MMA issuer (one thread) and TMEM allocator.
-//   warp 5     TMA producer: q, k, v, g boxes of 32 tokens per chunk, plus beta.
-//   warps 6-9  prep group: gate, prefix, q/k norms, centered operands (section 2),
-//              K_c K_i^T and Q_c K_i^T with mma.sync, the 32x32 inverse (section 3).
-// A two-slot SMEM ring carries prepared chunks from the prep group to the recurrent
-// consumer, which takes chunks strictly in order (section 4); mbarriers give
-// backpressure both ways, and every wait is bounded (timeout -> status bit).
+// Per chunk (section 3 notation; R' = V^T - P, W_beta = diag(beta) INV^T [K_r | Mqk^T]):
+//   GEMM1  [O_0 | P] = S_bf16 [Q_d | K_d]^T           M128 N64  K128  (A = bf16 S from TMEM)
+//          S = S diag(a)                              CUDA cores, during GEMM1
+//          R' = V^T - P                               CUDA cores -> bf16 -> TMEM
+//   GEMM3  [S | O] += R' W_beta                       M128 N160 K32   (A = R' from TMEM)
+// Since U = R INV^T = R' diag(beta) INV^T, the section-3 update U [K_r | Mqk^T] equals
+// R' W_beta; W_beta depends on the chunk only, so the prep warps build it (mma.sync)
+// ahead of the recurrence and the serial chain holds two tensor-core round trips.
 //
-// TMEM columns (256 per CTA): [0,128) fp32 S; [128,160) O; [160,192) P, then U;
-// [192,256) bf16 copy of S (A operand of GEMM1, two values per column).
-// Per chunk c (GEMM shapes M x N x K):
-//   GEMM1  [O_0 | P] = S_bf16 [Q_d | K_d]^T           128 x 64 x 128   (A from TMEM)
-//          S *= diag(a)                               (CUDA cores, TMEM ld/st)
-//          R = (V^T - P) diag(beta)                   (CUDA cores -> SMEM, bf16)
-//   GEMM2  U = R INV^T                                128 x 32 x 32
-//   GEMM3  [S | O] += U [K_r | Mqk^T]                 128 x 160 x 32   (section 8)
+// Warp roles (448 threads, 72 registers each):
+//   warps 0-3   TMEM group: thread v owns state row v (TMEM lane v): R', the chunk
+//               output O, the bf16 copy of S and the decay, initial/final state I/O.
+//   warps 4-11  prep group: gate, prefix, q/k norms, centered operands (section 2),
+//               K_c K_i^T and Q_c K_i^T with mma.sync, the 32x32 inverse, W_beta.
+//   warp 12     MMA issuer (one thread) and TMEM allocator.
+//   warp 13     TMA producer: q, k, v, g boxes of 32 tokens, plus beta.
+// A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
+// consumer (section 4); mbarriers give backpressure both ways and every wait is
+// bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
+//
+// TMEM columns (256 per CTA): [0,128) fp32 S; [128,160) O; [160,192) P;
+// [192,256) bf16 copy of S (two values per column), whose first 16 columns hold R'
+// between GEMM1 and GEMM3.
 #include <cuda.h>
 
 #include "kda_device.cuh"
@@ -34,37 +37,41 @@
 namespace kda {
 namespace {
 
-constexpr int TC_THREADS = 320;
-constexpr int W_MMA = 4, W_TMA = 5, W_PREP0 = 6;
+constexpr int TC_THREADS = 448;
+constexpr int W_PREP0 = 4, PREP_WARPS = 8, W_MMA = 12, W_TMA = 13;
+constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
 
-// Slot layout (bytes).  Raw q/k/g land where their derived operands are written.
-constexpr uint32_t SL_QDKD = 0;       // [Q_d | K_d] 64 x 128 K-major (raw q at 0, raw k at 8192)
+// Slot layout (bytes).  Raw q/k/g land where derived operands are later written.
+constexpr uint32_t SL_QDKD = 0;       // [Q_d | K_d]: 64 rows x 128, K-major, 128-B swizzle (raw q at 0, k at 8192)
 constexpr uint32_t SL_RAWQ = 0, SL_RAWK = 8192;
-constexpr uint32_t SL_KRMQ = 16384;   // [K_r^T (128 rows) | Mqk (32 rows)] x 32 K-major (raw g at 16384)
+constexpr uint32_t SL_W = 16384;      // W_beta^T: 160 rows (n) x 32 (token), K-major core layout (raw g below)
 constexpr uint32_t SL_RAWG = 16384;
-constexpr uint32_t SL_INV = 26624;    // INV 32 x 32 K-major (row j, column i)
-constexpr uint32_t SL_V = 28672;      // raw v [32][128]
-constexpr uint32_t SL_BETA = 36864;   // fp32 [32]
-constexpr uint32_t SL_A = 36992;      // fp32 [128]: 2^G_T
-constexpr uint32_t SLOT_BYTES = 37888;
+constexpr uint32_t SL_V = 26624;      // raw v [32][128]
+constexpr uint32_t SL_A = 34816;      // fp32 [128]: 2^G_T
+constexpr uint32_t SL_BETA = 35328;   // fp32 [32]
+constexpr uint32_t SLOT_BYTES = 35840;
 
-constexpr int PROW = 136;                              // padded bf16 row of the prep tiles
-constexpr uint32_t PTILE = 32 * PROW * 2;              // 8704 B
-constexpr uint32_t OFF_PREP = NSLOT * SLOT_BYTES;      // Q_c, K_c, K_i; later L, X (fp32) over Q_c
-constexpr uint32_t OFF_MISC = OFF_PREP + 3 * PTILE;    // tot[2][128], rq[32], rk[32]
-constexpr uint32_t OFF_RU = 103424;                    // R, then U: 128 x 32 K-major (8 KB)
-constexpr uint32_t OFF_BAR = OFF_RU + 8192;
-enum { B_FULLTMA = 0, B_FULL = 2, B_EMPTY = 4, B_G1 = 6, B_G2, B_G3, B_RREADY, B_UREADY, B_SREADY, B_DRAIN,
-       B_COUNT };
+// Prep scratch (per CTA).  32 x 128 bf16 tiles with 16-byte chunks XOR-swizzled by
+// (row % 8), so that both the row-wise stores and ldmatrix reads are conflict-free.
+constexpr uint32_t OFF_QC = NSLOT * SLOT_BYTES;   // Q_c, then L (fp32, column-major [32][36])
+constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then INV diag(beta) (bf16 [32][40], row i = column i)
+constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i
+constexpr uint32_t OFF_KR = OFF_KI + 8192;        // K_r (32 x 128, swizzled like Q_c)
+constexpr uint32_t OFF_MQK = OFF_KR + 8192;       // Mqk (bf16 [32][40])
+constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32]
+constexpr uint32_t OFF_BAR = OFF_MISC + 4352;
+enum { B_FULLTMA = 0, B_FULL = 2, B_EMPTY = 4, B_G1 = 6, B_G3, B_RREADY, B_SREADY, B_DRAIN, B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
-static_assert(OFF_MISC + 1280 <= OFF_RU, "prep scratch overlaps R/U");
+static_assert(SLOT_BYTES % 1024 == 0, "slots must keep the 128-B swizzle atoms 1 KB aligned");
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs must fit one SM");
+constexpr int LC = 36;   // fp32 row stride of L (column-major)
+constexpr int IB = 40;   // bf16 row stride of INV diag(beta)
 
-constexpr uint32_t TM_S = 0, TM_O = 128, TM_PU = 160, TM_SB = 192, TM_COLS = 256;
+constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 160, TM_SB = 192, TM_COLS = 256;
 
 struct TmaMaps {
     CUtensorMap q, k, v, g;
@@ -81,6 +88,13 @@ struct Unit {
 __device__ __forceinline__ uint32_t bar_addr(const Unit& u, int b) { return u.base + OFF_BAR + 8u * b; }
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) { return make_float2(bf16_lo(w), bf16_hi(w)); }
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 x) { return pack_bf16x2(x.x, x.y); }
+
+// byte offset of (row, col) in a 32 x 128 bf16 scratch tile (chunk ^= row % 8)
+__device__ __forceinline__ uint32_t sc128(int row, int col) {
+    return (uint32_t)(row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
+}
 
 // Bounded wait, with the verdict made uniform over the warp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
@@ -88,22 +102,22 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
     return __all_sync(0xffffffffu, ok);
 }
 
-// 32 consecutive state values of row `row_off` (element offset), as fp32 bits.
-__device__ __forceinline__ void load_state_piece(const FwdParams& p, size_t off, uint32_t (&r)[32]) {
+// 16 state values of row `off` (element offset) as fp32 bits (zeros without an initial state).
+__device__ __forceinline__ void load_state16(const FwdParams& p, size_t off, uint32_t (&r)[16]) {
     if (!p.init_state) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = 0u;
+        for (int j = 0; j < 16; ++j) r[j] = 0u;
     } else if (p.init_f32) {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const float*>(p.init_state) + off);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < 4; ++j) {
             const uint4 x = src[j];
             r[4 * j] = x.x; r[4 * j + 1] = x.y; r[4 * j + 2] = x.z; r[4 * j + 3] = x.w;
         }
     } else {
         const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.init_state) + off);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             const uint4 x = src[j];
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
@@ -115,21 +129,46 @@ __device__ __forceinline__ void load_state_piece(const FwdParams& p, size_t off,
     }
 }
 
-__device__ __forceinline__ void store_state_piece(const FwdParams& p, size_t off, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void store_state16(const FwdParams& p, size_t off, const uint32_t (&r)[16]) {
     if (!p.final_state) return;
     if (p.final_f32) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.final_state) + off);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        for (int j = 0; j < 4; ++j) dst[j] = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
     } else {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.final_state) + off);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 2; ++j) {
             dst[j] = make_uint4(pack_bf16x2(u2f(r[8 * j]), u2f(r[8 * j + 1])),
                                 pack_bf16x2(u2f(r[8 * j + 2]), u2f(r[8 * j + 3])),
                                 pack_bf16x2(u2f(r[8 * j + 4]), u2f(r[8 * j + 5])),
                                 pack_bf16x2(u2f(r[8 * j + 6]), u2f(r[8 * j + 7])));
         }
+    }
+}
+
+// One pass over S (8 pieces of 16 columns): write its bf16 copy (the next GEMM1 operand,
+// taken before the decay) and multiply S by diag(a) in place (the next GEMM3 adds to it).
+__device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* a_s) {
+#pragma unroll 1
+    for (int piece = 0; piece < 8; ++piece) {
+        uint32_t r[16];
+        tmem_ld16(lane_addr + TM_S + piece * 16, r);
+        tmem_wait_ld();
+        uint32_t b[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
+        tmem_st8(lane_addr + TM_SB + piece * 8, b);
+        const float4* a4 = reinterpret_cast<const float4*>(a_s + piece * 16);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float4 a = a4[j];
+            const float2 x0 = __fmul2_rn(make_float2(u2f(r[4 * j]), u2f(r[4 * j + 1])), make_float2(a.x, a.y));
+            const float2 x1 = __fmul2_rn(make_float2(u2f(r[4 * j + 2]), u2f(r[4 * j + 3])), make_float2(a.z, a.w));
+            r[4 * j] = f2u(x0.x); r[4 * j + 1] = f2u(x0.y);
+            r[4 * j + 2] = f2u(x1.x); r[4 * j + 3] = f2u(x1.y);
+        }
+        tmem_st16(lane_addr + TM_S + piece * 16, r);
     }
 }
 
@@ -142,98 +181,84 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
     const int v = pt;
     const size_t srow = (((size_t)u.n * p.H + u.h) * HD + v) * HD;
 
-    // initial state -> TMEM (fp32 and its bf16 copy); an empty sequence copies it through
+    // initial state -> TMEM; an empty sequence copies it straight through
 #pragma unroll 1
-    for (int piece = 0; piece < 4; ++piece) {
-        uint32_t r[32];
-        load_state_piece(p, srow + piece * 32, r);
-        if (u.nchunks == 0) {
-            store_state_piece(p, srow + piece * 32, r);
-            continue;
-        }
-        tmem_st32(lane_addr + TM_S + piece * 32, r);
-        uint32_t b[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
-        tmem_st16(lane_addr + TM_SB + piece * 16, b);
+    for (int piece = 0; piece < 8; ++piece) {
+        uint32_t r[16];
+        load_state16(p, srow + piece * 16, r);
+        if (u.nchunks == 0) store_state16(p, srow + piece * 16, r);
+        else tmem_st16(lane_addr + TM_S + piece * 16, r);
     }
     if (u.nchunks == 0) return;
+    tmem_wait_st();
+    if (!warp_wait(bar_addr(u, B_FULL), 0, p.status)) return;   // a of chunk 0
+    copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
     tmem_wait_st();
     tc_fence_before();
     named_bar_sync(2, 128);
     if (pt == 0) mbar_arrive(bar_addr(u, B_SREADY));
 
-    unsigned char* ru = u.gbase + OFF_RU;
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
-        const uint32_t kpar = (c >> 1) & 1, cpar = c & 1;
+        const uint32_t cpar = c & 1;
         const unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        if (!warp_wait(bar_addr(u, B_FULL + s), kpar, p.status)) return;
 
-        // S_d = S diag(a): off the critical path, overlapping GEMM1 (which reads the bf16 copy)
-        const float* a_s = reinterpret_cast<const float*>(gslot + SL_A);
-#pragma unroll 1
-        for (int piece = 0; piece < 4; ++piece) {
-            uint32_t r[32];
-            tmem_ld32(lane_addr + TM_S + piece * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = f2u(u2f(r[j]) * a_s[piece * 32 + j]);
-            tmem_st32(lane_addr + TM_S + piece * 32, r);
-        }
-        tmem_wait_st();
-
-        // R = (V^T - P) diag(beta) -> SMEM (bf16, K-major row v)
+        // R' = V^T - P -> bf16 -> TMEM (A operand of GEMM3)
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) return;
         tc_fence_after();
-        uint32_t pr[32];
-        tmem_ld32(lane_addr + TM_PU, pr);
-        tmem_wait_ld();
         {
             const uint16_t* vs = reinterpret_cast<const uint16_t*>(gslot + SL_V);
-            const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
             uint32_t rp[16];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float r0 = (bf16_bits_to_f32(vs[i * HD + v]) - u2f(pr[i])) * bs[i];
-                const float r1 = (bf16_bits_to_f32(vs[(i + 1) * HD + v]) - u2f(pr[i + 1])) * bs[i + 1];
-                rp[i >> 1] = pack_bf16x2(r0, r1);
-            }
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t pr[16];
+                tmem_ld16(lane_addr + TM_P + hh * 16, pr);
+                tmem_wait_ld();
 #pragma unroll
-            for (int kg = 0; kg < 4; ++kg)
-                *reinterpret_cast<uint4*>(ru + core_offset(v, 8 * kg, 32)) =
-                    make_uint4(rp[4 * kg], rp[4 * kg + 1], rp[4 * kg + 2], rp[4 * kg + 3]);
+                for (int i = 0; i < 16; i += 2) {
+                    const int t = hh * 16 + i;
+                    const float2 d = __ffma2_rn(make_float2(u2f(pr[i]), u2f(pr[i + 1])), make_float2(-1.f, -1.f),
+                                                make_float2(bf16_bits_to_f32(vs[t * HD + v]), bf16_bits_to_f32(vs[(t + 1) * HD + v])));
+                    rp[t >> 1] = f2_to_bf2(d);
+                }
+            }
+            tmem_st16(lane_addr + TM_SB, rp);
+            tmem_wait_st();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(2, 128);
         if (pt == 0) mbar_arrive(bar_addr(u, B_RREADY));
 
-        // U -> bf16 -> SMEM (GEMM2 has finished reading R)
-        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) return;
-        tc_fence_after();
-        tmem_ld32(lane_addr + TM_PU, pr);
-        tmem_wait_ld();
-        {
-            uint32_t up[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) up[i >> 1] = pack_bf16x2(u2f(pr[i]), u2f(pr[i + 1]));
-#pragma unroll
-            for (int kg = 0; kg < 4; ++kg)
-                *reinterpret_cast<uint4*>(ru + core_offset(v, 8 * kg, 32)) =
-                    make_uint4(up[4 * kg], up[4 * kg + 1], up[4 * kg + 2], up[4 * kg + 3]);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        named_bar_sync(2, 128);
-        if (pt == 0) mbar_arrive(bar_addr(u, B_UREADY));
-
-        // O -> out rows of this chunk; bf16 copy of S for the next chunk (or the final state)
+        // O of this chunk (kept as bf16 pairs), then the next chunk's S copy and decay
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) return;
         tc_fence_after();
-        tmem_ld32(lane_addr + TM_O, pr);
-        tmem_wait_ld();
+        uint32_t ob[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            uint32_t o[16];
+            tmem_ld16(lane_addr + TM_O + hh * 16, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int m = 0; m < 8; ++m) ob[hh * 8 + m] = pack_bf16x2(u2f(o[2 * m]), u2f(o[2 * m + 1]));
+        }
+        if (c + 1 < u.nchunks) {
+            const int s1 = (c + 1) & 1;
+            if (!warp_wait(bar_addr(u, B_FULL + s1), ((c + 1) >> 1) & 1, p.status)) return;
+            copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + s1 * SLOT_BYTES + SL_A));
+            tmem_wait_st();
+            tc_fence_before();
+            named_bar_sync(2, 128);
+            if (pt == 0) mbar_arrive(bar_addr(u, B_SREADY));
+        } else {
+#pragma unroll 1
+            for (int piece = 0; piece < 8; ++piece) {
+                uint32_t r[16];
+                tmem_ld16(lane_addr + TM_S + piece * 16, r);
+                tmem_wait_ld();
+                store_state16(p, srow + piece * 16, r);
+            }
+        }
         {
             const int64_t t0 = u.bos + (int64_t)c * CH;
             const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
@@ -241,31 +266,8 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
             const int64_t tstride = (int64_t)p.H * HD;
 #pragma unroll
             for (int i = 0; i < 32; ++i)
-                if (i < nvalid) orow[i * tstride] = __float2bfloat16_rn(u2f(pr[i]));
-        }
-        if (c + 1 < u.nchunks) {
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + TM_S + piece * 32, r);
-                tmem_wait_ld();
-                uint32_t b[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
-                tmem_st16(lane_addr + TM_SB + piece * 16, b);
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            if (pt == 0) mbar_arrive(bar_addr(u, B_SREADY));
-        } else {
-#pragma unroll 1
-            for (int piece = 0; piece < 4; ++piece) {
-                uint32_t r[32];
-                tmem_ld32(lane_addr + TM_S + piece * 32, r);
-                tmem_wait_ld();
-                store_state_piece(p, srow + piece * 32, r);
-            }
+                if (i < nvalid)
+                    *reinterpret_cast<uint16_t*>(orow + i * tstride) = (uint16_t)((i & 1) ? (ob[i >> 1] >> 16) : (ob[i >> 1] & 0xffffu));
         }
     }
 }
@@ -275,9 +277,7 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
 // ------------------------------------------------------------------------------
 __device__ void mma_issuer(const FwdParams& p, const Unit& u) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
-    constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);
     constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 160);
-    const uint32_t ru = u.base + OFF_RU;
     bool issued = false;
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
@@ -290,22 +290,15 @@ __device__ void mma_issuer(const FwdParams& p, const Unit& u) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
             tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
-                      make_sdesc_kmajor_noswizzle(slot + SL_QDKD + kk * 256, 128, 2048), idesc1, kk > 0);
+                      make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
         tc_commit(bar_addr(u, B_G1));
         issued = true;
         if (!mbar_wait_bounded(bar_addr(u, B_RREADY), cpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
-            tc_mma_ss(u.tmem + TM_PU, make_sdesc_kmajor_noswizzle(ru + kk * 256, 128, 512),
-                      make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512), idesc2, kk > 0);
-        tc_commit(bar_addr(u, B_G2));
-        if (!mbar_wait_bounded(bar_addr(u, B_UREADY), cpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-            tc_mma_ss(u.tmem + TM_S, make_sdesc_kmajor_noswizzle(ru + kk * 256, 128, 512),
-                      make_sdesc_kmajor_noswizzle(slot + SL_KRMQ + kk * 256, 128, 512), idesc3, 1u);
+            tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8,
+                      make_sdesc_kmajor_noswizzle(slot + SL_W + kk * 256, 128, 512), idesc3, 1u);
         tc_commit(bar_addr(u, B_G3));
         tc_commit(bar_addr(u, B_EMPTY + s));
     }
@@ -355,26 +348,32 @@ __device__ void tma_producer(const FwdParams& p, const TmaMaps& maps, const Unit
 }
 
 // ------------------------------------------------------------------------------
-// Prep group (128 threads): everything of a chunk that does not need the state.
+// Prep group (256 threads): everything of a chunk that does not need the state.
+// Elementwise phases: thread = (channel quad: channels 4 lane .. 4 lane + 3,
+// token quad: tokens 4 pw .. 4 pw + 3), pw = warp index within the group.
 // ------------------------------------------------------------------------------
 __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     const int lane = pt & 31, pw = pt >> 5, gq = lane >> 2, tq = lane & 3;
-    const int pp = pt & 63, half = pt >> 6, ch0 = 2 * pp;
+    const int c0 = 4 * lane;
     const float eA = expf(p.A_log[u.h]);
-    const float gm = -eA * LOG2E;
-    const float gb0 = gm * p.dt_bias[u.h * HD + ch0];
-    const float gb1 = gm * p.dt_bias[u.h * HD + ch0 + 1];
-    const float bcoef = p.lower_bound * LOG2E;   // b
-    const float Cst = 16.f * bcoef;              // fixed anchor C = 16 b
+    const float gm = -eA * LOG2E;                       // sigmoid(x) = 1 / (1 + 2^(gm (g + dt)))
+    const float4 dt = *reinterpret_cast<const float4*>(p.dt_bias + u.h * HD + c0);
+    const float2 gmv = make_float2(gm, gm);
+    const float2 gb01 = make_float2(gm * dt.x, gm * dt.y), gb23 = make_float2(gm * dt.z, gm * dt.w);
+    const float bcoef = p.lower_bound * LOG2E;          // b
+    const float Cst = 16.f * bcoef;                     // fixed anchor C = 16 b
     const float twoC = ex2_approx(Cst);
+    const float2 bcv = make_float2(bcoef, bcoef);
 
-    __nv_bfloat16* Qc = reinterpret_cast<__nv_bfloat16*>(u.gbase + OFF_PREP);
-    __nv_bfloat16* Kc = Qc + 32 * PROW;
-    __nv_bfloat16* Ki = Kc + 32 * PROW;
-    float* Lf = reinterpret_cast<float*>(u.gbase + OFF_PREP);   // over Q_c once it is consumed
-    float* Xf = Lf + 32 * 33;
-    float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);
-    float* rq = tot + 256;
+    unsigned char* qcs = u.gbase + OFF_QC;
+    unsigned char* kcs = u.gbase + OFF_KC;
+    unsigned char* kis = u.gbase + OFF_KI;
+    unsigned char* krs = u.gbase + OFF_KR;
+    unsigned char* mqs = u.gbase + OFF_MQK;
+    float* Lc = reinterpret_cast<float*>(u.gbase + OFF_QC);               // after Q_c is consumed
+    unsigned char* invb = u.gbase + OFF_KC;                               // after K_c is consumed
+    float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
+    float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
 
 #pragma unroll 1
@@ -385,199 +384,281 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status)) return;
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
-        const unsigned char* rawq = gslot + SL_RAWQ;
-        const unsigned char* rawk = gslot + SL_RAWK;
-        const unsigned char* rawg = gslot + SL_RAWG;
+        const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
 
-        // ---- A: gate, local prefix over 16 tokens x 2 channels; q/k row norms
-        uint32_t qw[16], kw[16];
-        float G0[16], G1[16];
+        // ---- A: q/k row norms (warp butterfly), gate and local prefix over 4 tokens x 4 channels
+        uint2 qv[4], kv[4];
+        float2 G01[4], G23[4];
         {
-            float acc0 = 0.f, acc1 = 0.f;
+            float part[8];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = 16 * half + j;
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * pw + r;
                 const bool valid = i < nvalid;
-                const uint32_t gw = lds32(rawg + i * 256 + ch0 * 2);
-                qw[j] = valid ? lds32(rawq + i * 256 + ch0 * 2) : 0u;
-                kw[j] = valid ? lds32(rawk + i * 256 + ch0 * 2) : 0u;
-                float l0 = bcoef * rcp_approx(1.f + ex2_approx(fmaf(gm, bf16_lo(gw), gb0)));
-                float l1 = bcoef * rcp_approx(1.f + ex2_approx(fmaf(gm, bf16_hi(gw), gb1)));
-                if (!valid) l0 = l1 = 0.f;
-                acc0 += l0;
-                acc1 += l1;
-                G0[j] = acc0;
-                G1[j] = acc1;
+                qv[r] = valid ? *reinterpret_cast<const uint2*>(gslot + SL_RAWQ + i * 256 + c0 * 2) : make_uint2(0, 0);
+                kv[r] = valid ? *reinterpret_cast<const uint2*>(gslot + SL_RAWK + i * 256 + c0 * 2) : make_uint2(0, 0);
+                const float2 q0 = bf2_to_f2(qv[r].x), q1 = bf2_to_f2(qv[r].y);
+                const float2 k0 = bf2_to_f2(kv[r].x), k1 = bf2_to_f2(kv[r].y);
+                const float2 sq = __ffma2_rn(q0, q0, __fmul2_rn(q1, q1));
+                const float2 sk = __ffma2_rn(k0, k0, __fmul2_rn(k1, k1));
+                part[r] = sq.x + sq.y;
+                part[4 + r] = sk.x + sk.y;
             }
-            tot[half * HD + ch0] = acc0;
-            tot[half * HD + ch0 + 1] = acc1;
-        }
-        {
-            const int r = pt >> 1, part = pt & 1;
-            const unsigned char* rowp = (r < 32 ? rawq + r * 256 : rawk + (r - 32) * 256) + part * 128;
-            float ss = 0.f;
+            // reduce-scatter the 8 partial row sums over the 32 lanes
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int ee = (e + pt) & 7;   // rotate so a quarter-warp hits distinct banks
-                const uint4 w4 = *reinterpret_cast<const uint4*>(rowp + ee * 16);
-                const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
+            for (int m = 0; m < 4; ++m) {
+                const bool hi = lane & 16;
+                const float send = hi ? part[m] : part[4 + m];
+                const float keep = hi ? part[4 + m] : part[m];
+                part[m] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+            }
 #pragma unroll
-                for (int m = 0; m < 4; ++m) {
-                    const float lo = bf16_lo(ws[m]), hi = bf16_hi(ws[m]);
-                    ss = fmaf(lo, lo, ss);
-                    ss = fmaf(hi, hi, ss);
-                }
+            for (int m = 0; m < 2; ++m) {
+                const bool hi = lane & 8;
+                const float send = hi ? part[m] : part[2 + m];
+                const float keep = hi ? part[2 + m] : part[m];
+                part[m] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
             }
-            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-            if (part == 0) {
-                const int tok = r & 31;
-                const float rn = tok < nvalid ? rsqrtf(ss + NORM_EPS) : 0.f;
-                if (r < 32) rq[tok] = rn; else rk[tok] = rn;
+            {
+                const bool hi = lane & 4;
+                const float send = hi ? part[0] : part[1];
+                const float keep = hi ? part[1] : part[0];
+                part[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
             }
+            part[0] += __shfl_xor_sync(0xffffffffu, part[0], 2);
+            part[0] += __shfl_xor_sync(0xffffffffu, part[0], 1);
+            if ((lane & 3) == 0) {
+                const int idx = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
+                const int tok = 4 * pw + (idx & 3);
+                const float rn = tok < nvalid ? rsqrtf(part[0] + NORM_EPS) : 0.f;
+                if (idx < 4) rq[tok] = rn; else rk[tok] = rn;
+            }
+
+            float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * pw + r;
+                const uint2 gw = *reinterpret_cast<const uint2*>(gslot + SL_RAWG + i * 256 + c0 * 2);
+                const float2 x01 = __ffma2_rn(gmv, bf2_to_f2(gw.x), gb01);
+                const float2 x23 = __ffma2_rn(gmv, bf2_to_f2(gw.y), gb23);
+                float2 l01 = __fmul2_rn(bcv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)),
+                                                         rcp_approx(1.f + ex2_approx(x01.y))));
+                float2 l23 = __fmul2_rn(bcv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)),
+                                                         rcp_approx(1.f + ex2_approx(x23.y))));
+                if (i >= nvalid) l01 = l23 = make_float2(0.f, 0.f);
+                acc01 = __fadd2_rn(acc01, l01);
+                acc23 = __fadd2_rn(acc23, l23);
+                G01[r] = acc01;
+                G23[r] = acc23;
+            }
+            *reinterpret_cast<float4*>(tot + pw * HD + c0) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
         }
-        named_bar_sync(1, 128);   // raw q/k/g are no longer read after this point
+        named_bar_sync(1, PREP_THREADS);   // raw q/k/g are no longer read after this point
 
         // ---- B: prefix combine, centered operands
         {
-            float off0 = 0.f, off1 = 0.f, tot0 = 0.f, tot1 = 0.f;
+            float2 rho01, rho23;
+            {
+                float2 off01 = make_float2(0.f, 0.f), off23 = make_float2(0.f, 0.f);
+                float2 T01 = make_float2(0.f, 0.f), T23 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const float a0 = tot[hh * HD + ch0], a1 = tot[hh * HD + ch0 + 1];
-                if (hh < half) { off0 += a0; off1 += a1; }
-                tot0 += a0;
-                tot1 += a1;
-            }
-            const float rho0 = ex2_approx(tot0 - Cst), rho1 = ex2_approx(tot1 - Cst);
-            if (half == 0) {
-                float* a_s = reinterpret_cast<float*>(gslot + SL_A);
-                a_s[ch0] = ex2_approx(tot0);
-                a_s[ch0 + 1] = ex2_approx(tot1);
-            }
-            uint32_t kr0[8], kr1[8];
-            float pend0 = 0.f, pend1 = 0.f;
+                for (int qq = 0; qq < PREP_WARPS; ++qq) {
+                    const float4 t4 = *reinterpret_cast<const float4*>(tot + qq * HD + c0);
+                    const float2 a01 = make_float2(t4.x, t4.y), a23 = make_float2(t4.z, t4.w);
+                    if (qq < pw) { off01 = __fadd2_rn(off01, a01); off23 = __fadd2_rn(off23, a23); }
+                    T01 = __fadd2_rn(T01, a01);
+                    T23 = __fadd2_rn(T23, a23);
+                }
+                rho01 = make_float2(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst));
+                rho23 = make_float2(ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
+                if (pw == 0)
+                    *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
+                        make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
+                const float2 mC = make_float2(-Cst, -Cst);
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const int i = 16 * half + j;
-                const float Ga = G0[j] + off0, Gb = G1[j] + off1;
-                const float ep0 = ex2_approx(Ga - Cst), ep1 = ex2_approx(Gb - Cst);
-                const float em0 = ex2_approx(Cst - Ga), em1 = ex2_approx(Cst - Gb);
-                const float qs = rq[i] * p.scale, ks = rk[i];
-                const float q0 = bf16_lo(qw[j]) * qs, q1 = bf16_hi(qw[j]) * qs;
-                const float k0 = bf16_lo(kw[j]) * ks, k1 = bf16_hi(kw[j]) * ks;
-                const float qc0 = q0 * ep0, qc1 = q1 * ep1;
-                const float kc0 = k0 * ep0, kc1 = k1 * ep1;
-                const float ki0 = k0 * em0, ki1 = k1 * em1;
-                const int o = i * PROW + ch0;
-                *reinterpret_cast<uint32_t*>(&Qc[o]) = pack_bf16x2(qc0, qc1);
-                *reinterpret_cast<uint32_t*>(&Kc[o]) = pack_bf16x2(kc0, kc1);
-                *reinterpret_cast<uint32_t*>(&Ki[o]) = pack_bf16x2(ki0, ki1);
-                *reinterpret_cast<uint32_t*>(gslot + SL_QDKD + core_offset(i, ch0, HD)) =
-                    pack_bf16x2(qc0 * twoC, qc1 * twoC);                       // Q_d
-                *reinterpret_cast<uint32_t*>(gslot + SL_QDKD + core_offset(32 + i, ch0, HD)) =
-                    pack_bf16x2(kc0 * twoC, kc1 * twoC);                       // K_d
-                const float r0 = ki0 * rho0, r1 = ki1 * rho1;                  // K_r
-                if (j & 1) {
-                    kr0[j >> 1] = pack_bf16x2(pend0, r0);
-                    kr1[j >> 1] = pack_bf16x2(pend1, r1);
-                } else {
-                    pend0 = r0;
-                    pend1 = r1;
+                for (int r = 0; r < 4; ++r) {   // G - C
+                    G01[r] = __fadd2_rn(__fadd2_rn(G01[r], off01), mC);
+                    G23[r] = __fadd2_rn(__fadd2_rn(G23[r], off23), mC);
                 }
             }
+            const float2 twoCv = make_float2(twoC, twoC);
 #pragma unroll
-            for (int g8 = 0; g8 < 2; ++g8) {   // K_r^T rows ch0, ch0+1; tokens 16 half + 8 g8 .. +7
-                const int kk = 16 * half + 8 * g8;
-                *reinterpret_cast<uint4*>(gslot + SL_KRMQ + core_offset(ch0, kk, 32)) =
-                    make_uint4(kr0[4 * g8], kr0[4 * g8 + 1], kr0[4 * g8 + 2], kr0[4 * g8 + 3]);
-                *reinterpret_cast<uint4*>(gslot + SL_KRMQ + core_offset(ch0 + 1, kk, 32)) =
-                    make_uint4(kr1[4 * g8], kr1[4 * g8 + 1], kr1[4 * g8 + 2], kr1[4 * g8 + 3]);
+            for (int r = 0; r < 4; ++r) {
+                const int i = 4 * pw + r;
+                const uint32_t o = sc128(i, c0);
+                const float qs = rq[i] * p.scale, ks = rk[i];
+                const float2 k01 = __fmul2_rn(bf2_to_f2(kv[r].x), make_float2(ks, ks));
+                const float2 k23 = __fmul2_rn(bf2_to_f2(kv[r].y), make_float2(ks, ks));
+                {   // 2^(G - C): Q_c, K_c and the recurrent-domain Q_d, K_d
+                    const float2 ep01 = make_float2(ex2_approx(G01[r].x), ex2_approx(G01[r].y));
+                    const float2 ep23 = make_float2(ex2_approx(G23[r].x), ex2_approx(G23[r].y));
+                    const float2 qc01 = __fmul2_rn(__fmul2_rn(bf2_to_f2(qv[r].x), make_float2(qs, qs)), ep01);
+                    const float2 qc23 = __fmul2_rn(__fmul2_rn(bf2_to_f2(qv[r].y), make_float2(qs, qs)), ep23);
+                    *reinterpret_cast<uint2*>(qcs + o) = make_uint2(f2_to_bf2(qc01), f2_to_bf2(qc23));
+                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + sw128_offset(i, c0, 64)) =
+                        make_uint2(f2_to_bf2(__fmul2_rn(qc01, twoCv)), f2_to_bf2(__fmul2_rn(qc23, twoCv)));   // Q_d
+                    const float2 kc01 = __fmul2_rn(k01, ep01), kc23 = __fmul2_rn(k23, ep23);
+                    *reinterpret_cast<uint2*>(kcs + o) = make_uint2(f2_to_bf2(kc01), f2_to_bf2(kc23));
+                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + sw128_offset(32 + i, c0, 64)) =
+                        make_uint2(f2_to_bf2(__fmul2_rn(kc01, twoCv)), f2_to_bf2(__fmul2_rn(kc23, twoCv)));   // K_d
+                }
+                {   // 2^(C - G): K_i and K_r = K_i 2^(G_T - C)
+                    const float2 em01 = make_float2(ex2_approx(-G01[r].x), ex2_approx(-G01[r].y));
+                    const float2 em23 = make_float2(ex2_approx(-G23[r].x), ex2_approx(-G23[r].y));
+                    const float2 ki01 = __fmul2_rn(k01, em01), ki23 = __fmul2_rn(k23, em23);
+                    *reinterpret_cast<uint2*>(kis + o) = make_uint2(f2_to_bf2(ki01), f2_to_bf2(ki23));
+                    *reinterpret_cast<uint2*>(krs + o) =
+                        make_uint2(f2_to_bf2(__fmul2_rn(ki01, rho01)), f2_to_bf2(__fmul2_rn(ki23, rho23)));   // K_r
+                }
             }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, PREP_THREADS);
 
-        // ---- C: K_c K_i^T (warps 0-1) and Q_c K_i^T (warps 2-3), 16 rows x 32 columns each
+        // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp
         {
-            const int mat = pw >> 1, mt = pw & 1;
-            const __nv_bfloat16* Ab = mat ? Qc : Kc;
-            float acc[4][4];
+            const int mat = pw >> 2, mt = (pw >> 1) & 1, nb = pw & 1;
+            const unsigned char* Ab = mat ? qcs : kcs;
+            float acc[2][4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+            for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-                uint32_t a[4];
-                ldmatrix_x4(a, Ab + (mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * PROW + kk * 16 + (lane >> 4) * 8);
-#pragma unroll
-                for (int nb = 0; nb < 2; ++nb) {
-                    uint32_t b[4];
-                    ldmatrix_x4(b, Ki + (nb * 16 + (lane & 7) + (lane >> 4) * 8) * PROW + kk * 16 + ((lane >> 3) & 1) * 8);
-                    mma_bf16_16816(acc[2 * nb], a, b[0], b[1]);
-                    mma_bf16_16816(acc[2 * nb + 1], a, b[2], b[3]);
-                }
+                uint32_t a[4], b[4];
+                ldmatrix_x4(a, Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kk * 16 + (lane >> 4) * 8));
+                ldmatrix_x4(b, kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, kk * 16 + ((lane >> 3) & 1) * 8));
+                mma_bf16_16816(acc[0], a, b[0], b[1]);
+                mma_bf16_16816(acc[1], a, b[2], b[3]);
             }
-            named_bar_sync(1, 128);   // Q_c / K_c / K_i fully read: L and X may overwrite them
-            const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
+            named_bar_sync(1, PREP_THREADS);   // Q_c / K_c / K_i fully read: L and INV diag(beta) may overwrite them
 #pragma unroll
-            for (int t = 0; t < 4; ++t) {
+            for (int t = 0; t < 2; ++t) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int i = mt * 16 + gq + hf * 8;
-                    const int j = t * 8 + 2 * tq;
+                    const int j = nb * 16 + t * 8 + 2 * tq;
                     const float v0 = acc[t][2 * hf], v1 = acc[t][2 * hf + 1];
                     // select, never multiply: the masked upper triangle may hold inf/NaN
                     if (mat == 0) {
-                        Lf[i * 33 + j] = (j < i) ? bs[i] * v0 : 0.f;
-                        Lf[i * 33 + j + 1] = (j + 1 < i) ? bs[i] * v1 : 0.f;
+                        Lc[j * LC + i] = (j < i) ? bs[i] * v0 : 0.f;
+                        Lc[(j + 1) * LC + i] = (j + 1 < i) ? bs[i] * v1 : 0.f;
                     } else {
-                        *reinterpret_cast<uint32_t*>(gslot + SL_KRMQ + core_offset(128 + i, j, 32)) =
+                        *reinterpret_cast<uint32_t*>(mqs + i * (IB * 2) + j * 2) =
                             pack_bf16x2((j <= i) ? v0 : 0.f, (j + 1 <= i) ? v1 : 0.f);   // Mqk
                     }
                 }
             }
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, PREP_THREADS);
 
-        // ---- D: INV = (I + L)^-1: diagonal 16x16 blocks by forward substitution
-        if (pw == 0) {
-            const int o = (lane >> 4) * 16, col = lane & 15;
-            float x[16];
+        // ---- D: INV = X = (I + L)^-1, blocked: 8x8 diagonal blocks by forward substitution,
+        //      then X21 = -X22 L21 X11 at the 8- and 16-row levels (fp32, all prep threads).
+        //      X is row-major [32][33] over the consumed K_i tile; its upper triangle is zero.
+        {
+            float* X = reinterpret_cast<float*>(kis);
+            float* T1 = X + 32 * 33;          // two 8x8 products (8-row level)
+            float* T2 = T1 + 128;             // one 16x16 product (16-row level)
+            if (pw == 0) {
+                const int bb = lane >> 3, cc = lane & 7, o = 8 * bb;
+                float x[8];
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) x[rr] = (rr == col) ? 1.f : 0.f;
+                for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-            for (int kk = 0; kk < 16; ++kk) {
-                const float xk = x[kk];
+                for (int k = 0; k < 7; ++k) {
+                    const float xk = x[k];
 #pragma unroll
-                for (int rr = kk + 1; rr < 16; ++rr) x[rr] = fmaf(-Lf[(o + rr) * 33 + o + kk], xk, x[rr]);
+                    for (int r = k + 1; r < 8; ++r) x[r] = fmaf(-Lc[(o + k) * LC + o + r], xk, x[r]);
+                }
+#pragma unroll
+                for (int r = 0; r < 8; ++r) X[(o + r) * 33 + o + cc] = x[r];
+            } else {
+                // zero the strictly upper 8x8 blocks (the off-diagonal lower ones are written below)
+                for (int e = pt - 32; e < 6 * 64; e += PREP_THREADS - 32) {
+                    const int blk = e >> 6, rr = (e >> 3) & 7, cc = e & 7;
+                    const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                    const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                    X[(8 * br + rr) * 33 + 8 * bc + cc] = 0.f;
+                }
+            }
+            named_bar_sync(1, PREP_THREADS);
+            if (pt < 128) {   // T1_p = L[b+1][b] X[b][b] for diagonal pairs b = 0, 2
+                const int pr = pt >> 6, rr = (pt >> 3) & 7, cc = pt & 7, o = 16 * pr;
+                float acc = 0.f;
+#pragma unroll
+                for (int n = 0; n < 8; ++n) acc = fmaf(Lc[(o + n) * LC + o + 8 + rr], X[(o + n) * 33 + o + cc], acc);
+                T1[pt] = acc;
+            }
+            named_bar_sync(1, PREP_THREADS);
+            if (pt < 128) {   // X[b+1][b] = -X[b+1][b+1] T1_p
+                const int pr = pt >> 6, rr = (pt >> 3) & 7, cc = pt & 7, o = 16 * pr;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 8; ++m) acc = fmaf(X[(o + 8 + rr) * 33 + o + 8 + m], T1[pr * 64 + m * 8 + cc], acc);
+                X[(o + 8 + rr) * 33 + o + cc] = -acc;
+            }
+            named_bar_sync(1, PREP_THREADS);
+            {   // T2 = L21 X11 (16x16 blocks)
+                const int rr = pt >> 4, cc = pt & 15;
+                float acc = 0.f;
+#pragma unroll
+                for (int n = 0; n < 16; ++n) acc = fmaf(Lc[n * LC + 16 + rr], X[n * 33 + cc], acc);
+                T2[pt] = acc;
+            }
+            named_bar_sync(1, PREP_THREADS);
+            {   // X21 = -X22 T2
+                const int rr = pt >> 4, cc = pt & 15;
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < 16; ++m) acc = fmaf(X[(16 + rr) * 33 + 16 + m], T2[m * 16 + cc], acc);
+                X[(16 + rr) * 33 + cc] = -acc;
+            }
+            named_bar_sync(1, PREP_THREADS);
+            {   // row i of the stored tile = beta_i * column i of X (= B of the W product)
+                const int i = pt >> 3, j0 = 4 * (pt & 7);
+                const float b = bs[i];
+                const float x0 = X[j0 * 33 + i], x1 = X[(j0 + 1) * 33 + i];
+                const float x2 = X[(j0 + 2) * 33 + i], x3 = X[(j0 + 3) * 33 + i];
+                *reinterpret_cast<uint2*>(invb + i * (IB * 2) + j0 * 2) =
+                    make_uint2(pack_bf16x2(b * x0, b * x1), pack_bf16x2(b * x2, b * x3));
+            }
+        }
+        named_bar_sync(1, PREP_THREADS);
+
+        // ---- E: W_beta^T = [K_r^T ; Mqk] INV diag(beta): 160 x 32 x 32 with mma.sync
+        //      (rows 0-127: K_r^T, A fragments by transposed ldmatrix from K_r; rows 128-159: Mqk)
+#pragma unroll 1
+        for (int mt = pw; mt < 10; mt += PREP_WARPS) {
+            float acc[4][4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                uint32_t a[4];
+                if (mt < 8)
+                    ldmatrix_x4_trans(a, krs + sc128(ks * 16 + (lane & 7) + ((lane >> 4) & 1) * 8, mt * 16 + ((lane >> 3) & 1) * 8));
+                else
+                    ldmatrix_x4(a, mqs + ((mt - 8) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * (IB * 2) +
+                                       (ks * 16 + (lane >> 4) * 8) * 2);
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+                    uint32_t b[4];
+                    ldmatrix_x4(b, invb + (nb * 16 + (lane & 7) + (lane >> 4) * 8) * (IB * 2) +
+                                       (ks * 16 + ((lane >> 3) & 1) * 8) * 2);
+                    mma_bf16_16816(acc[2 * nb], a, b[0], b[1]);
+                    mma_bf16_16816(acc[2 * nb + 1], a, b[2], b[3]);
+                }
             }
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) Xf[(o + rr) * 33 + o + col] = x[rr];
-        }
-        named_bar_sync(1, 128);
+            for (int t = 0; t < 4; ++t)
 #pragma unroll
-        for (int it = 0; it < 2; ++it) {   // T1 = L21 A^-1 (upper-right block of X as scratch)
-            const int e = it * 128 + pt, rr = e >> 4, cc = e & 15;
-            float acc = 0.f;
-            for (int m = cc; m < 16; ++m) acc = fmaf(Lf[(16 + rr) * 33 + m], Xf[m * 33 + cc], acc);
-            Xf[rr * 33 + 16 + cc] = acc;
-        }
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {   // X21 = -D^-1 T1
-            const int e = it * 128 + pt, rr = e >> 4, cc = e & 15;
-            float acc = 0.f;
-            for (int m = 0; m <= rr; ++m) acc = fmaf(Xf[(16 + rr) * 33 + 16 + m], Xf[m * 33 + 16 + cc], acc);
-            Xf[(16 + rr) * 33 + cc] = -acc;
-        }
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {   // INV rows j, column pairs i (upper triangle = 0)
-            const int e = it * 128 + pt, j = e >> 4, i2 = (e & 15) * 2;
-            const float v0 = (i2 <= j) ? Xf[j * 33 + i2] : 0.f;
-            const float v1 = (i2 + 1 <= j) ? Xf[j * 33 + i2 + 1] : 0.f;
-            *reinterpret_cast<uint32_t*>(gslot + SL_INV + core_offset(j, i2, 32)) = pack_bf16x2(v0, v1);
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int n = mt * 16 + gq + hf * 8, i = t * 8 + 2 * tq;
+                    *reinterpret_cast<uint32_t*>(gslot + SL_W + core_offset(n, i, 32)) =
+                        pack_bf16x2(acc[t][2 * hf], acc[t][2 * hf + 1]);
+                }
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_FULL + s));
     }
 }
@@ -624,12 +705,12 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
 
     if (warp < 4) {
         tmem_group(p, u, tid);
+    } else if (warp < W_PREP0 + PREP_WARPS) {
+        prep_group(p, u, tid - W_PREP0 * 32);
     } else if (warp == W_MMA) {
         if (lane == 0) mma_issuer(p, u);
     } else if (warp == W_TMA) {
         tma_producer(p, maps, u, lane);
-    } else {
-        prep_group(p, u, tid - W_PREP0 * 32);
     }
 
     tc_fence_before();

@@ -38,6 +38,23 @@ constexpr KDA_HD uint64_t make_sdesc_kmajor_noswizzle(uint32_t smem_addr, uint32
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte swizzle
+// layout: rows of 128 B (64 bf16 of K) whose 16-byte chunks are permuted by
+// chunk ^ (row % 8), 8-row atoms of 1 KB stacked `sbo` bytes apart (1024 when the
+// atoms are dense).  The leading offset is unused for this layout (encoded as 1).
+// Layout field (bits 61-63) = 2.  The atom base must be 1 KB aligned.
+constexpr KDA_HD uint64_t make_sdesc_kmajor_sw128(uint32_t smem_addr, uint32_t sbo = 1024) {
+    return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
+           (1ull << 46) | (2ull << 61);
+}
+
+// Byte offset of element (r, k) of a K-major bf16 tile with 64 <= kt columns in the
+// 128-byte swizzle layout above: column blocks of 64 elements, each a dense stack of
+// `rows` 128-byte rows.
+constexpr KDA_HD uint32_t sw128_offset(int r, int k, int rows) {
+    return (uint32_t)((k >> 6) * rows * 128 + r * 128 + ((((k >> 3) & 7) ^ (r & 7)) << 4) + ((k & 7) << 1));
+}
+
 // Byte offset of element (r, k) of a K-major bf16 tile with `kt` columns in the
 // no-swizzle core-matrix layout used by make_sdesc_kmajor_noswizzle(lbo = 128,
 // sbo = kt / 8 * 128).
@@ -61,13 +78,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                  : "memory");
 }
+// Test the phase with `parity`; while it is pending the thread may be suspended for up
+// to the hint (ns), so waiting warps leave the issue slots to the working ones.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(1000000u)
         : "memory");
     return ok != 0;
 }
@@ -177,6 +196,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
