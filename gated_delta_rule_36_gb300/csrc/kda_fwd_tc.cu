@@ -55,14 +55,15 @@ constexpr uint32_t SLOT_BYTES = 35840;
 
 // Prep scratch (per CTA).  32 x 128 bf16 tiles with 16-byte chunks XOR-swizzled by
 // (row % 8), so that both the row-wise stores and ldmatrix reads are conflict-free.
-constexpr uint32_t OFF_QC = NSLOT * SLOT_BYTES;   // Q_c, then L (fp32, column-major [32][36])
-constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then INV diag(beta) (bf16 [32][40], row i = column i)
-constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i
-constexpr uint32_t OFF_KR = OFF_KI + 8192;        // K_r (32 x 128, swizzled like Q_c)
-constexpr uint32_t OFF_MQK = OFF_KR + 8192;       // Mqk (bf16 [32][40])
-constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32]
-constexpr uint32_t OFF_BAR = OFF_MISC + 4352;
-enum { B_FULLTMA = 0, B_FULL = 2, B_EMPTY = 4, B_G1 = 6, B_G3, B_RREADY, B_SREADY, B_DRAIN, B_COUNT };
+constexpr uint32_t OFF_OSTG = NSLOT * SLOT_BYTES; // chunk output staging: bf16 [32 tokens][128]
+constexpr uint32_t OFF_QC = OFF_OSTG + 8192;      // Q_c, then L (fp32, column-major [32][36]) and T2
+constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then X = INV (fp32 [32][33]) and INV diag(beta)
+constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i (kept until the W product)
+constexpr uint32_t OFF_MQK = OFF_KI + 8192;       // Mqk (bf16 [32][40])
+constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32], rho[128]
+constexpr uint32_t OFF_BAR = OFF_MISC + 4864;
+enum { B_FULLTMA = 0, B_FULL = 2, B_EMPTY = 4, B_G1 = 6, B_G3, B_RREADY, B_SREADY, B_DRAIN, B_OSTAGED, B_OFREE,
+       B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
@@ -74,7 +75,7 @@ constexpr int IB = 40;   // bf16 row stride of INV diag(beta)
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 160, TM_SB = 192, TM_COLS = 256;
 
 struct TmaMaps {
-    CUtensorMap q, k, v, g;
+    CUtensorMap q, k, v, g, out;
 };
 
 struct Unit {
@@ -96,9 +97,11 @@ __device__ __forceinline__ uint32_t sc128(int row, int col) {
     return (uint32_t)(row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
 
-// Bounded wait, with the verdict made uniform over the warp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t* status) {
-    const bool ok = mbar_wait_bounded(bar, parity, status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+// Bounded wait, with the verdict made uniform over the warp.  `max_sleep_ns` > 0 backs
+// off between polls (long waits off the critical path).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t* status,
+                                          uint32_t max_sleep_ns = 0) {
+    const bool ok = mbar_wait_bounded(bar, parity, status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, max_sleep_ns);
     return __all_sync(0xffffffffu, ok);
 }
 
@@ -230,21 +233,33 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
         named_bar_sync(2, 128);
         if (pt == 0) mbar_arrive(bar_addr(u, B_RREADY));
 
-        // O of this chunk (kept as bf16 pairs), then the next chunk's S copy and decay
+        // O of this chunk -> staging tile [token][v] (written out by the MMA thread),
+        // then the next chunk's S copy and decay
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) return;
         tc_fence_after();
-        uint32_t ob[16];
+        if (c > 0 && !warp_wait(bar_addr(u, B_OFREE), (c - 1) & 1, p.status)) return;
+        {
+            unsigned char* ost = u.gbase + OFF_OSTG + 2 * v;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            uint32_t o[16];
-            tmem_ld16(lane_addr + TM_O + hh * 16, o);
-            tmem_wait_ld();
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t o[16];
+                tmem_ld16(lane_addr + TM_O + hh * 16, o);
+                tmem_wait_ld();
 #pragma unroll
-            for (int m = 0; m < 8; ++m) ob[hh * 8 + m] = pack_bf16x2(u2f(o[2 * m]), u2f(o[2 * m + 1]));
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t pr = pack_bf16x2(u2f(o[2 * m]), u2f(o[2 * m + 1]));
+                    const int i = hh * 16 + 2 * m;
+                    *reinterpret_cast<uint16_t*>(ost + i * 256) = (uint16_t)(pr & 0xffffu);
+                    *reinterpret_cast<uint16_t*>(ost + (i + 1) * 256) = (uint16_t)(pr >> 16);
+                }
+            }
         }
+        fence_proxy_async_smem();
+        named_bar_sync(2, 128);
+        if (pt == 0) mbar_arrive(bar_addr(u, B_OSTAGED));
         if (c + 1 < u.nchunks) {
             const int s1 = (c + 1) & 1;
-            if (!warp_wait(bar_addr(u, B_FULL + s1), ((c + 1) >> 1) & 1, p.status)) return;
+            if (!warp_wait(bar_addr(u, B_FULL + s1), ((c + 1) >> 1) & 1, p.status, 256)) return;
             copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + s1 * SLOT_BYTES + SL_A));
             tmem_wait_st();
             tc_fence_before();
@@ -259,23 +274,13 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
                 store_state16(p, srow + piece * 16, r);
             }
         }
-        {
-            const int64_t t0 = u.bos + (int64_t)c * CH;
-            const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
-            __nv_bfloat16* orow = p.out + (t0 * p.H + u.h) * HD + v;
-            const int64_t tstride = (int64_t)p.H * HD;
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-                if (i < nvalid)
-                    *reinterpret_cast<uint16_t*>(orow + i * tstride) = (uint16_t)((i & 1) ? (ob[i >> 1] >> 16) : (ob[i >> 1] & 0xffffu));
-        }
     }
 }
 
 // ------------------------------------------------------------------------------
 // MMA issuer (one thread).
 // ------------------------------------------------------------------------------
-__device__ void mma_issuer(const FwdParams& p, const Unit& u) {
+__device__ void mma_issuer(const FwdParams& p, const TmaMaps& maps, const Unit& u) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 160);
     bool issued = false;
@@ -301,7 +306,24 @@ __device__ void mma_issuer(const FwdParams& p, const Unit& u) {
                       make_sdesc_kmajor_noswizzle(slot + SL_W + kk * 256, 128, 512), idesc3, 1u);
         tc_commit(bar_addr(u, B_G3));
         tc_commit(bar_addr(u, B_EMPTY + s));
+        // write the staged chunk output: one tensor store for a full chunk, row copies for a tail
+        if (!mbar_wait_bounded(bar_addr(u, B_OSTAGED), cpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
+        {
+            const int64_t t0 = u.bos + (int64_t)c * CH;
+            const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
+            const uint32_t ost = u.base + OFF_OSTG;
+            if (nvalid == CH) {
+                tma_store_3d(&maps.out, ost, 0, u.h, (int)t0);
+            } else {
+                for (int i = 0; i < nvalid; ++i)
+                    bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
+            }
+            bulk_commit();
+            bulk_wait_read_all();
+            mbar_arrive(bar_addr(u, B_OFREE));
+        }
     }
+    bulk_wait_all();   // the output must be in global memory before the kernel ends
     if (issued) {  // nothing of ours may still run on the tensor core when TMEM is freed
         tc_commit(bar_addr(u, B_DRAIN));
         mbar_wait_bounded(bar_addr(u, B_DRAIN), 0, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
@@ -317,7 +339,7 @@ __device__ void tma_producer(const FwdParams& p, const TmaMaps& maps, const Unit
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
         const int k = c >> 1;
-        if (c >= NSLOT && !warp_wait(bar_addr(u, B_EMPTY + s), (k - 1) & 1, p.status)) break;
+        if (c >= NSLOT && !warp_wait(bar_addr(u, B_EMPTY + s), (k - 1) & 1, p.status, 512)) break;
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
@@ -368,84 +390,68 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     unsigned char* qcs = u.gbase + OFF_QC;
     unsigned char* kcs = u.gbase + OFF_KC;
     unsigned char* kis = u.gbase + OFF_KI;
-    unsigned char* krs = u.gbase + OFF_KR;
     unsigned char* mqs = u.gbase + OFF_MQK;
     float* Lc = reinterpret_cast<float*>(u.gbase + OFF_QC);               // after Q_c is consumed
-    unsigned char* invb = u.gbase + OFF_KC;                               // after K_c is consumed
+    float* T2 = Lc + 32 * LC;                                             // 16 x 16
+    float* X = reinterpret_cast<float*>(u.gbase + OFF_KC);                // after K_c is consumed
+    unsigned char* invb = u.gbase + OFF_KC + 32 * 33 * 4;
     float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
+    float* rho = rk + 32;                                                 // 2^(G_T - C) per channel
 
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
         const uint32_t kpar = (c >> 1) & 1;
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status)) return;
+        if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) return;
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
         const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
 
-        // ---- A: q/k row norms (warp butterfly), gate and local prefix over 4 tokens x 4 channels
+        // ---- A: q/k row norms (row pass: 4 threads per row), gate and local prefix over
+        //      4 tokens x 4 channels
         uint2 qv[4], kv[4];
         float2 G01[4], G23[4];
         {
-            float part[8];
+            const int row = pt >> 2, part = pt & 3;   // rows 0-31 q, 32-63 k; 32 elements per thread
+            const unsigned char* rp = gslot + (row < 32 ? SL_RAWQ + row * 256 : SL_RAWK + (row - 32) * 256);
+            float2 ss = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                const int i = 4 * pw + r;
-                const bool valid = i < nvalid;
-                qv[r] = valid ? *reinterpret_cast<const uint2*>(gslot + SL_RAWQ + i * 256 + c0 * 2) : make_uint2(0, 0);
-                kv[r] = valid ? *reinterpret_cast<const uint2*>(gslot + SL_RAWK + i * 256 + c0 * 2) : make_uint2(0, 0);
-                const float2 q0 = bf2_to_f2(qv[r].x), q1 = bf2_to_f2(qv[r].y);
-                const float2 k0 = bf2_to_f2(kv[r].x), k1 = bf2_to_f2(kv[r].y);
-                const float2 sq = __ffma2_rn(q0, q0, __fmul2_rn(q1, q1));
-                const float2 sk = __ffma2_rn(k0, k0, __fmul2_rn(k1, k1));
-                part[r] = sq.x + sq.y;
-                part[4 + r] = sk.x + sk.y;
+            for (int e = 0; e < 4; ++e) {
+                const uint4 w4 = *reinterpret_cast<const uint4*>(rp + ((4 * e + part + 4 * (row & 1)) & 15) * 16);
+                const float2 x0 = bf2_to_f2(w4.x), x1 = bf2_to_f2(w4.y), x2 = bf2_to_f2(w4.z), x3 = bf2_to_f2(w4.w);
+                ss = __ffma2_rn(x0, x0, ss);
+                ss = __ffma2_rn(x1, x1, ss);
+                ss = __ffma2_rn(x2, x2, ss);
+                ss = __ffma2_rn(x3, x3, ss);
             }
-            // reduce-scatter the 8 partial row sums over the 32 lanes
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const bool hi = lane & 16;
-                const float send = hi ? part[m] : part[4 + m];
-                const float keep = hi ? part[4 + m] : part[m];
-                part[m] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-            }
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const bool hi = lane & 8;
-                const float send = hi ? part[m] : part[2 + m];
-                const float keep = hi ? part[2 + m] : part[m];
-                part[m] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
-            }
-            {
-                const bool hi = lane & 4;
-                const float send = hi ? part[0] : part[1];
-                const float keep = hi ? part[1] : part[0];
-                part[0] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
-            }
-            part[0] += __shfl_xor_sync(0xffffffffu, part[0], 2);
-            part[0] += __shfl_xor_sync(0xffffffffu, part[0], 1);
-            if ((lane & 3) == 0) {
-                const int idx = ((lane >> 4) & 1) * 4 + ((lane >> 3) & 1) * 2 + ((lane >> 2) & 1);
-                const int tok = 4 * pw + (idx & 3);
-                const float rn = tok < nvalid ? rsqrtf(part[0] + NORM_EPS) : 0.f;
-                if (idx < 4) rq[tok] = rn; else rk[tok] = rn;
+            float sum = ss.x + ss.y;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (part == 0) {
+                const int tok = row & 31;
+                const float rn = tok < nvalid ? rsqrtf(sum + NORM_EPS) : 0.f;
+                if (row < 32) rq[tok] = rn; else rk[tok] = rn;
             }
 
             float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int i = 4 * pw + r;
-                const uint2 gw = *reinterpret_cast<const uint2*>(gslot + SL_RAWG + i * 256 + c0 * 2);
+                const uint32_t off = i * 256 + c0 * 2;
+                qv[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWQ + off);
+                kv[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWK + off);
+                const uint2 gw = *reinterpret_cast<const uint2*>(gslot + SL_RAWG + off);
                 const float2 x01 = __ffma2_rn(gmv, bf2_to_f2(gw.x), gb01);
                 const float2 x23 = __ffma2_rn(gmv, bf2_to_f2(gw.y), gb23);
-                float2 l01 = __fmul2_rn(bcv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)),
-                                                         rcp_approx(1.f + ex2_approx(x01.y))));
-                float2 l23 = __fmul2_rn(bcv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)),
-                                                         rcp_approx(1.f + ex2_approx(x23.y))));
-                if (i >= nvalid) l01 = l23 = make_float2(0.f, 0.f);
+                const float bl = i < nvalid ? bcoef : 0.f;   // tokens past the end: lambda = 0
+                const float2 blv = make_float2(bl, bl);
+                const float2 l01 = __fmul2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)),
+                                                              rcp_approx(1.f + ex2_approx(x01.y))));
+                const float2 l23 = __fmul2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)),
+                                                              rcp_approx(1.f + ex2_approx(x23.y))));
                 acc01 = __fadd2_rn(acc01, l01);
                 acc23 = __fadd2_rn(acc23, l23);
                 G01[r] = acc01;
@@ -457,7 +463,6 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 
         // ---- B: prefix combine, centered operands
         {
-            float2 rho01, rho23;
             {
                 float2 off01 = make_float2(0.f, 0.f), off23 = make_float2(0.f, 0.f);
                 float2 T01 = make_float2(0.f, 0.f), T23 = make_float2(0.f, 0.f);
@@ -469,11 +474,12 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     T01 = __fadd2_rn(T01, a01);
                     T23 = __fadd2_rn(T23, a23);
                 }
-                rho01 = make_float2(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst));
-                rho23 = make_float2(ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
-                if (pw == 0)
+                if (pw == 0) {
                     *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
                         make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
+                    *reinterpret_cast<float4*>(rho + c0) = make_float4(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst),
+                                                                       ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
+                }
                 const float2 mC = make_float2(-Cst, -Cst);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {   // G - C
@@ -507,8 +513,6 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     const float2 em23 = make_float2(ex2_approx(-G23[r].x), ex2_approx(-G23[r].y));
                     const float2 ki01 = __fmul2_rn(k01, em01), ki23 = __fmul2_rn(k23, em23);
                     *reinterpret_cast<uint2*>(kis + o) = make_uint2(f2_to_bf2(ki01), f2_to_bf2(ki23));
-                    *reinterpret_cast<uint2*>(krs + o) =
-                        make_uint2(f2_to_bf2(__fmul2_rn(ki01, rho01)), f2_to_bf2(__fmul2_rn(ki23, rho23)));   // K_r
                 }
             }
         }
@@ -551,111 +555,139 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         }
         named_bar_sync(1, PREP_THREADS);
 
-        // ---- D: INV = X = (I + L)^-1, blocked: 8x8 diagonal blocks by forward substitution,
-        //      then X21 = -X22 L21 X11 at the 8- and 16-row levels (fp32, all prep threads).
-        //      X is row-major [32][33] over the consumed K_i tile; its upper triangle is zero.
-        {
-            float* X = reinterpret_cast<float*>(kis);
-            float* T1 = X + 32 * 33;          // two 8x8 products (8-row level)
-            float* T2 = T1 + 128;             // one 16x16 product (16-row level)
-            if (pw == 0) {
-                const int bb = lane >> 3, cc = lane & 7, o = 8 * bb;
-                float x[8];
+        // ---- D: INV = X = (I + L)^-1 in fp32: the two diagonal 16x16 blocks by forward
+        //      substitution (warp 0, lane = column), then X21 = -X22 L21 X11 (all prep threads).
+        //      INV diag(beta) is stored transposed (row i = beta_i * column i of X) as the
+        //      B operand of the W product; X is row-major [32][33] (its diagonal blocks hold
+        //      zeros above the diagonal; the upper-right block is never read).
+        if (pw == 0) {
+            const int o = (lane >> 4) * 16, cc = lane & 15;
+            float x[16];
 #pragma unroll
-                for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-                for (int k = 0; k < 7; ++k) {
-                    const float xk = x[k];
+            for (int k = 0; k < 15; ++k) {
+                const float xk = x[k];
+                const float* col = Lc + (o + k) * LC + o;
 #pragma unroll
-                    for (int r = k + 1; r < 8; ++r) x[r] = fmaf(-Lc[(o + k) * LC + o + r], xk, x[r]);
-                }
+                for (int r4 = (k + 1) >> 2; r4 < 4; ++r4) {
+                    const float4 l4 = *reinterpret_cast<const float4*>(col + 4 * r4);
+                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                for (int r = 0; r < 8; ++r) X[(o + r) * 33 + o + cc] = x[r];
-            } else {
-                // zero the strictly upper 8x8 blocks (the off-diagonal lower ones are written below)
-                for (int e = pt - 32; e < 6 * 64; e += PREP_THREADS - 32) {
-                    const int blk = e >> 6, rr = (e >> 3) & 7, cc = e & 7;
-                    const int br = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-                    const int bc = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-                    X[(8 * br + rr) * 33 + 8 * bc + cc] = 0.f;
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * r4 + e > k) x[4 * r4 + e] = fmaf(-lv[e], xk, x[4 * r4 + e]);
                 }
             }
-            named_bar_sync(1, PREP_THREADS);
-            if (pt < 128) {   // T1_p = L[b+1][b] X[b][b] for diagonal pairs b = 0, 2
-                const int pr = pt >> 6, rr = (pt >> 3) & 7, cc = pt & 7, o = 16 * pr;
-                float acc = 0.f;
 #pragma unroll
-                for (int n = 0; n < 8; ++n) acc = fmaf(Lc[(o + n) * LC + o + 8 + rr], X[(o + n) * 33 + o + cc], acc);
-                T1[pt] = acc;
-            }
-            named_bar_sync(1, PREP_THREADS);
-            if (pt < 128) {   // X[b+1][b] = -X[b+1][b+1] T1_p
-                const int pr = pt >> 6, rr = (pt >> 3) & 7, cc = pt & 7, o = 16 * pr;
-                float acc = 0.f;
+            for (int r = 0; r < 16; ++r) X[(o + r) * 33 + o + cc] = x[r];
+            const float bj = bs[o + cc];
+            uint32_t w[8];
 #pragma unroll
-                for (int m = 0; m < 8; ++m) acc = fmaf(X[(o + 8 + rr) * 33 + o + 8 + m], T1[pr * 64 + m * 8 + cc], acc);
-                X[(o + 8 + rr) * 33 + o + cc] = -acc;
-            }
-            named_bar_sync(1, PREP_THREADS);
-            {   // T2 = L21 X11 (16x16 blocks)
-                const int rr = pt >> 4, cc = pt & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int n = 0; n < 16; ++n) acc = fmaf(Lc[n * LC + 16 + rr], X[n * 33 + cc], acc);
-                T2[pt] = acc;
-            }
-            named_bar_sync(1, PREP_THREADS);
-            {   // X21 = -X22 T2
-                const int rr = pt >> 4, cc = pt & 15;
-                float acc = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) acc = fmaf(X[(16 + rr) * 33 + 16 + m], T2[m * 16 + cc], acc);
-                X[(16 + rr) * 33 + cc] = -acc;
-            }
-            named_bar_sync(1, PREP_THREADS);
-            {   // row i of the stored tile = beta_i * column i of X (= B of the W product)
-                const int i = pt >> 3, j0 = 4 * (pt & 7);
-                const float b = bs[i];
-                const float x0 = X[j0 * 33 + i], x1 = X[(j0 + 1) * 33 + i];
-                const float x2 = X[(j0 + 2) * 33 + i], x3 = X[(j0 + 3) * 33 + i];
-                *reinterpret_cast<uint2*>(invb + i * (IB * 2) + j0 * 2) =
-                    make_uint2(pack_bf16x2(b * x0, b * x1), pack_bf16x2(b * x2, b * x3));
+            for (int r = 0; r < 8; ++r) w[r] = pack_bf16x2(bj * x[2 * r], bj * x[2 * r + 1]);
+            unsigned char* row = invb + (o + cc) * (IB * 2);
+            *reinterpret_cast<uint4*>(row + o * 2) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(row + o * 2 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+            if (o == 16) {   // row i >= 16, columns j < 16: X[j][i] lies above the diagonal
+                *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(row + 16) = make_uint4(0, 0, 0, 0);
             }
         }
         named_bar_sync(1, PREP_THREADS);
-
-        // ---- E: W_beta^T = [K_r^T ; Mqk] INV diag(beta): 160 x 32 x 32 with mma.sync
-        //      (rows 0-127: K_r^T, A fragments by transposed ldmatrix from K_r; rows 128-159: Mqk)
-#pragma unroll 1
-        for (int mt = pw; mt < 10; mt += PREP_WARPS) {
-            float acc[4][4];
+        if (pw == 0) {
+            // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8;
+            // X21 goes straight into the transposed tile: row cc, column 16 + rr
+            float t[2][4];
 #pragma unroll
-            for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+            for (int nt = 0; nt < 2; ++nt) t[nt][0] = t[nt][1] = t[nt][2] = t[nt][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
-                uint32_t a[4];
-                if (mt < 8)
-                    ldmatrix_x4_trans(a, krs + sc128(ks * 16 + (lane & 7) + ((lane >> 4) & 1) * 8, mt * 16 + ((lane >> 3) & 1) * 8));
-                else
-                    ldmatrix_x4(a, mqs + ((mt - 8) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * (IB * 2) +
-                                       (ks * 16 + (lane >> 4) * 8) * 2);
+                const int k0 = ks * 8 + tq;
+                // A = L21 [16 rr][16 n]: L21[rr][n] = L[16 + rr][n] = Lc[n * LC + 16 + rr]
+                const uint32_t a[4] = {f2tf32(Lc[k0 * LC + 16 + gq]), f2tf32(Lc[k0 * LC + 24 + gq]),
+                                       f2tf32(Lc[(k0 + 4) * LC + 16 + gq]), f2tf32(Lc[(k0 + 4) * LC + 24 + gq])};
 #pragma unroll
-                for (int nb = 0; nb < 2; ++nb) {
-                    uint32_t b[4];
-                    ldmatrix_x4(b, invb + (nb * 16 + (lane & 7) + (lane >> 4) * 8) * (IB * 2) +
-                                       (ks * 16 + ((lane >> 3) & 1) * 8) * 2);
-                    mma_bf16_16816(acc[2 * nb], a, b[0], b[1]);
-                    mma_bf16_16816(acc[2 * nb + 1], a, b[2], b[3]);
+                for (int nt = 0; nt < 2; ++nt) {   // B = X11 [16 n][16 cc]
+                    const uint32_t b0 = f2tf32(X[k0 * 33 + nt * 8 + gq]), b1 = f2tf32(X[(k0 + 4) * 33 + nt * 8 + gq]);
+                    mma_tf32_1688(t[nt], a, b0, b1);
+                }
+            }
+            // T2 to shared memory (the second product reads it as its B operand)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) T2[(gq + (e >> 1) * 8) * 16 + nt * 8 + 2 * tq + (e & 1)] = t[nt][e];
+            __syncwarp();
+            float x21[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) x21[nt][0] = x21[nt][1] = x21[nt][2] = x21[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int k0 = ks * 8 + tq;
+                // A = X22 [16 rr][16 m] = X[16 + rr][16 + m]
+                const uint32_t a[4] = {f2tf32(X[(16 + gq) * 33 + 16 + k0]), f2tf32(X[(24 + gq) * 33 + 16 + k0]),
+                                       f2tf32(X[(16 + gq) * 33 + 20 + k0]), f2tf32(X[(24 + gq) * 33 + 20 + k0])};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {   // B = T2 [16 m][16 cc]
+                    const uint32_t b0 = f2tf32(T2[k0 * 16 + nt * 8 + gq]), b1 = f2tf32(T2[(k0 + 4) * 16 + nt * 8 + gq]);
+                    mma_tf32_1688(x21[nt], a, b0, b1);
                 }
             }
 #pragma unroll
-            for (int t = 0; t < 4; ++t)
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                    const int n = mt * 16 + gq + hf * 8, i = t * 8 + 2 * tq;
-                    *reinterpret_cast<uint32_t*>(gslot + SL_W + core_offset(n, i, 32)) =
-                        pack_bf16x2(acc[t][2 * hf], acc[t][2 * hf + 1]);
+                for (int e = 0; e < 4; ++e) {
+                    const int rr = gq + (e >> 1) * 8, cc = nt * 8 + 2 * tq + (e & 1);
+                    reinterpret_cast<__nv_bfloat16*>(invb + cc * (IB * 2))[16 + rr] =
+                        __float2bfloat16_rn(-x21[nt][e] * bs[cc]);
                 }
+        }
+        named_bar_sync(1, PREP_THREADS);
+
+        // ---- E: W_beta^T = [K_r^T ; Mqk] INV diag(beta), 160 x 32 x 32 with mma.sync.
+        //      Rows d < 128 use K_r = K_i diag(rho): A fragments by transposed ldmatrix from
+        //      K_i, rows scaled by rho_d in the epilogue.  Warp pw: rows 16 pw .. 16 pw + 15
+        //      of the K_r part (all 32 columns) and one 16 x 8 tile of the Mqk part.
+        {
+            const int mts[2] = {pw, 8 + (pw >> 2)};
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int mt = mts[q];
+                const int nt0 = q == 0 ? 0 : (pw & 3), ntn = q == 0 ? 4 : 1;
+                float acc[4][4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4];
+                    if (q == 0)
+                        ldmatrix_x4_trans(a, kis + sc128(ks * 16 + (lane & 7) + ((lane >> 4) & 1) * 8, mt * 16 + ((lane >> 3) & 1) * 8));
+                    else
+                        ldmatrix_x4(a, mqs + ((mt - 8) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * (IB * 2) +
+                                           (ks * 16 + (lane >> 4) * 8) * 2);
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        if (t >= ntn) break;
+                        const int nt = nt0 + t;
+                        // B fragment of columns 8 nt .. 8 nt + 7: rows of the transposed INV diag(beta)
+                        const unsigned char* bp = invb + (nt * 8 + (lane & 7)) * (IB * 2) + (ks * 16 + ((lane >> 3) & 1) * 8) * 2;
+                        uint32_t b0, b1;
+                        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+                                     : "=r"(b0), "=r"(b1) : "r"(smem_u32(bp)));
+                        mma_bf16_16816(acc[t], a, b0, b1);
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    if (t >= ntn) break;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int n = mt * 16 + gq + hf * 8, i = (nt0 + t) * 8 + 2 * tq;
+                        const float sc = q == 0 ? rho[n] : 1.f;
+                        *reinterpret_cast<uint32_t*>(gslot + SL_W + core_offset(n, i, 32)) =
+                            pack_bf16x2(acc[t][2 * hf] * sc, acc[t][2 * hf + 1] * sc);
+                    }
+                }
+            }
         }
         fence_proxy_async_smem();
         named_bar_sync(1, PREP_THREADS);
@@ -693,6 +725,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
         tma_prefetch_desc(&maps.g);
+        tma_prefetch_desc(&maps.out);
     }
     if (warp == W_MMA) {
         tmem_alloc(u.base + OFF_TMEMADDR, TM_COLS);
@@ -708,7 +741,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
     } else if (warp < W_PREP0 + PREP_WARPS) {
         prep_group(p, u, tid - W_PREP0 * 32);
     } else if (warp == W_MMA) {
-        if (lane == 0) mma_issuer(p, u);
+        if (lane == 0) mma_issuer(p, maps, u);
     } else if (warp == W_TMA) {
         tma_producer(p, maps, u, lane);
     }
@@ -760,7 +793,8 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     TmaMaps maps;
     if (!encode_tokens_map(&maps.q, p.q, p.T_total, p.H) || !encode_tokens_map(&maps.k, p.k, p.T_total, p.H) ||
-        !encode_tokens_map(&maps.v, p.v, p.T_total, p.H) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H))
+        !encode_tokens_map(&maps.v, p.v, p.T_total, p.H) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
+        !encode_tokens_map(&maps.out, p.out, p.T_total, p.H))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SMEM_BYTES);

@@ -93,14 +93,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with `parity` to complete, for at most `limit` SM clock
 // cycles.  Returns false (and sets `status_bit` in *status) when the limit expires.
+// With max_sleep_ns > 0 the thread backs off between polls (exponentially, up to
+// that many ns), for waits that are long and off the critical path.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t* status,
-                                                  uint32_t status_bit, long long limit) {
+                                                  uint32_t status_bit, long long limit,
+                                                  uint32_t max_sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    uint32_t ns = 16;
     while (!mbar_try_wait(bar, parity)) {
         if (clock64() - t0 > limit) {
             atomicOr(status, status_bit);
             return false;
+        }
+        if (max_sleep_ns) {
+            __nanosleep(ns);
+            ns = ns * 2 < max_sleep_ns ? ns * 2 : max_sleep_ns;
         }
     }
     return true;
@@ -114,6 +122,25 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int 
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
+// Shared -> global tensor store of one box (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(tmap),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+// Shared -> global linear bulk copy (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;\n" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// Wait until every committed bulk store of this thread is complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory"); }
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
 }

@@ -9,6 +9,7 @@ NaN sentinel.
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 import torch
@@ -94,6 +95,8 @@ def assert_close(name, got, ref, dtype):
     got = got.detach().float().cpu().numpy() if isinstance(got, torch.Tensor) else got
     assert np.all(np.isfinite(got)), f"{name}: non-finite values"
     max_abs, rel = errors(got, ref)
+    if os.environ.get("KDA_TEST_VERBOSE"):
+        print(f"[err] {name}: max_abs={max_abs:.3e} rel_fro={rel:.3e} ({'fp32' if dtype == torch.float32 else 'bf16'})")
     if dtype == torch.float32:
         assert rel <= F32_REL_FRO, f"{name}: rel Frobenius {rel:.3e} > {F32_REL_FRO}"
     else:
