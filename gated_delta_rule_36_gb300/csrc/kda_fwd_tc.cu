@@ -14,16 +14,17 @@
 // R' W_beta; W_beta depends on the chunk only, so the prep warps build it (mma.sync)
 // ahead of the recurrence and the serial chain holds two tensor-core round trips.
 //
-// Warp roles (448 threads, 72 registers each):
-//   warps 0-3   TMEM group: thread v owns state row v (TMEM lane v): R', the chunk
-//               output O, the bf16 copy of S and the decay, initial/final state I/O.
+// Warp roles (384 threads, up to 80 registers each):
+//   warps 0-3   chain group: thread v owns state row v (TMEM lane v): initial/final
+//               state I/O, the bf16 copy of S, the decay, R' and the chunk output O.
+//               Its thread 0 also issues the tensor-core MMAs, the TMA loads of each
+//               chunk's q, k, v, g boxes and the TMA store of each output tile; its
+//               warp 0 loads beta and owns the TMEM allocation.
 //   warps 4-11  prep group: gate, prefix, q/k norms, centered operands (section 2),
 //               K_c K_i^T and Q_c K_i^T with mma.sync, the 32x32 inverse, W_beta.
-//   warp 12     MMA issuer (one thread) and TMEM allocator.
-//   warp 13     TMA producer: q, k, v, g boxes of 32 tokens, plus beta.
 // A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
-// consumer (section 4); mbarriers give backpressure both ways and every wait is
-// bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
+// consumer (section 4): the chain refills a slot as soon as GEMM3 has read it, and
+// every mbarrier wait is bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
 //
 // TMEM columns (256 per CTA): [0,128) fp32 S; [128,160) O; [160,192) P;
 // [192,256) bf16 copy of S (two values per column), whose first 16 columns hold R'
@@ -37,8 +38,8 @@
 namespace kda {
 namespace {
 
-constexpr int TC_THREADS = 448;
-constexpr int W_PREP0 = 4, PREP_WARPS = 8, W_MMA = 12, W_TMA = 13;
+constexpr int TC_THREADS = 384;
+constexpr int W_PREP0 = 4, PREP_WARPS = 8;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
@@ -56,14 +57,14 @@ constexpr uint32_t SLOT_BYTES = 35840;
 // Prep scratch (per CTA).  32 x 128 bf16 tiles with 16-byte chunks XOR-swizzled by
 // (row % 8), so that both the row-wise stores and ldmatrix reads are conflict-free.
 constexpr uint32_t OFF_OSTG = NSLOT * SLOT_BYTES; // chunk output staging: bf16 [32 tokens][128]
-constexpr uint32_t OFF_QC = OFF_OSTG + 8192;      // Q_c, then L (fp32, column-major [32][36]) and T2
+constexpr uint32_t OFF_QC = OFF_OSTG + 8192;      // Q_c, then T2 (fp32 [16][16])
 constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then X = INV (fp32 [32][33]) and INV diag(beta)
 constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i (kept until the W product)
 constexpr uint32_t OFF_MQK = OFF_KI + 8192;       // Mqk (bf16 [32][40])
-constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32], rho[128]
-constexpr uint32_t OFF_BAR = OFF_MISC + 4864;
-enum { B_FULLTMA = 0, B_FULL = 2, B_EMPTY = 4, B_G1 = 6, B_G3, B_RREADY, B_SREADY, B_DRAIN, B_OSTAGED, B_OFREE,
-       B_COUNT };
+constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32], then L; rho[128]
+constexpr uint32_t MISC_L_BYTES = 32 * 36 * 4;    // L (fp32, column-major [32][36]) over tot, rq, rk
+constexpr uint32_t OFF_BAR = OFF_MISC + MISC_L_BYTES + 512;
+enum { B_FULLTMA = 0, B_FULL = 2, B_G1 = 4, B_G3, B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
@@ -150,9 +151,8 @@ __device__ __forceinline__ void store_state16(const FwdParams& p, size_t off, co
     }
 }
 
-// One pass over S (8 pieces of 16 columns): write its bf16 copy (the next GEMM1 operand,
-// taken before the decay) and multiply S by diag(a) in place (the next GEMM3 adds to it).
-__device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* a_s) {
+// The bf16 copy of S (the next GEMM1 operand), 8 pieces of 16 columns.
+__device__ __forceinline__ void copy_state_bf16(uint32_t lane_addr) {
 #pragma unroll 1
     for (int piece = 0; piece < 8; ++piece) {
         uint32_t r[16];
@@ -162,6 +162,17 @@ __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* 
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
         tmem_st8(lane_addr + TM_SB + piece * 8, b);
+    }
+}
+
+// S = S diag(a) in place (GEMM3 of the chunk then adds to it); runs while GEMM1 reads
+// the bf16 copy.
+__device__ __forceinline__ void decay_state(uint32_t lane_addr, const float* a_s) {
+#pragma unroll 1
+    for (int piece = 0; piece < 8; ++piece) {
+        uint32_t r[16];
+        tmem_ld16(lane_addr + TM_S + piece * 16, r);
+        tmem_wait_ld();
         const float4* a4 = reinterpret_cast<const float4*>(a_s + piece * 16);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -176,10 +187,43 @@ __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* 
 }
 
 // ------------------------------------------------------------------------------
-// TMEM group: state row v = TMEM lane v.
+// Chain group: state row v = TMEM lane v; thread 0 issues the MMAs and the TMA copies.
 // ------------------------------------------------------------------------------
-__device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
-    const int w = pt >> 5;
+__device__ __forceinline__ int chunk_valid(const Unit& u, int c) {
+    const int64_t t0 = u.bos + (int64_t)c * CH;
+    return (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
+}
+
+// q, k, g, v boxes of chunk c into its slot (thread 0 of the chain group).
+__device__ __forceinline__ void load_chunk_boxes(const TmaMaps& maps, const Unit& u, int c) {
+    const int s = c & 1;
+    const int t0 = (int)(u.bos + (int64_t)c * CH);
+    const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLTMA + s);
+    mbar_arrive_expect_tx(full, 4u * CH * HD * 2u);
+    tma_load_3d(slot + SL_RAWQ, &maps.q, 0, u.h, t0, full);
+    tma_load_3d(slot + SL_RAWK, &maps.k, 0, u.h, t0, full);
+    tma_load_3d(slot + SL_RAWG, &maps.g, 0, u.h, t0, full);
+    tma_load_3d(slot + SL_V, &maps.v, 0, u.h, t0, full);
+}
+
+// beta of token `lane` of chunk c (0 past the end), by a plain load: its token stride
+// is 2H bytes, too narrow for a tensor box when H is small.
+__device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, int c, int lane) {
+    const int64_t t0 = u.bos + (int64_t)c * CH;
+    return lane < chunk_valid(u, c)
+               ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h])
+               : 0.f;
+}
+
+__device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b) {
+    reinterpret_cast<float*>(u.gbase + (c & 1) * SLOT_BYTES + SL_BETA)[lane] = b;
+    mbar_arrive(bar_addr(u, B_FULLTMA + (c & 1)));
+}
+
+__device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
+    constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
+    constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 160);
+    const int w = pt >> 5, lane = pt & 31;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     const int v = pt;
     const size_t srow = (((size_t)u.n * p.H + u.h) * HD + v) * HD;
@@ -193,22 +237,39 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
         else tmem_st16(lane_addr + TM_S + piece * 16, r);
     }
     if (u.nchunks == 0) return;
+    const int first = u.nchunks < NSLOT ? u.nchunks : NSLOT;
+    if (pt == 0)
+        for (int c = 0; c < first; ++c) load_chunk_boxes(maps, u, c);
+    if (w == 0)
+        for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta(p, u, c, lane));
+    int issued = first;
     tmem_wait_st();
-    if (!warp_wait(bar_addr(u, B_FULL), 0, p.status)) return;   // a of chunk 0
-    copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
+    copy_state_bf16(lane_addr);
     tmem_wait_st();
     tc_fence_before();
     named_bar_sync(2, 128);
-    if (pt == 0) mbar_arrive(bar_addr(u, B_SREADY));
 
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
         const uint32_t cpar = c & 1;
+        const uint32_t slot = u.base + s * SLOT_BYTES;
         const unsigned char* gslot = u.gbase + s * SLOT_BYTES;
 
+        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T, and the decay by a of this chunk meanwhile
+        if (!warp_wait(bar_addr(u, B_FULL + s), (c >> 1) & 1, p.status, 256)) break;
+        tc_fence_after();
+        if (pt == 0) {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
+                          make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
+            tc_commit(bar_addr(u, B_G1));
+        }
+        decay_state(lane_addr, reinterpret_cast<const float*>(gslot + SL_A));
+
         // R' = V^T - P -> bf16 -> TMEM (A operand of GEMM3)
-        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) return;
+        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
         {
             const uint16_t* vs = reinterpret_cast<const uint16_t*>(gslot + SL_V);
@@ -231,13 +292,31 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
         }
         tc_fence_before();
         named_bar_sync(2, 128);
-        if (pt == 0) mbar_arrive(bar_addr(u, B_RREADY));
 
-        // O of this chunk -> staging tile [token][v] (written out by the MMA thread),
-        // then the next chunk's S copy and decay
-        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) return;
+        // GEMM3 [S | O] += R' W_beta
+        if (pt == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)
+                tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8,
+                          make_sdesc_kmajor_noswizzle(slot + SL_W + kk * 256, 128, 512), idesc3, 1u);
+            tc_commit(bar_addr(u, B_G3));
+        }
+        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) break;
         tc_fence_after();
-        if (c > 0 && !warp_wait(bar_addr(u, B_OFREE), (c - 1) & 1, p.status)) return;
+
+        // the slot has been read for the last time: refill it with chunk c + 2 (beta
+        // stays in flight in a register until the end of the iteration)
+        const bool refill = c + NSLOT < u.nchunks;
+        float beta_next = 0.f;
+        if (refill) {
+            if (pt == 0) load_chunk_boxes(maps, u, c + NSLOT);
+            if (w == 0) beta_next = load_beta(p, u, c + NSLOT, lane);
+            issued = c + NSLOT + 1;
+        }
+
+        // O of this chunk -> staging tile [token][v] -> one tensor store (row copies
+        // for a tail chunk); O must leave TMEM before the next GEMM1 writes it
         {
             unsigned char* ost = u.gbase + OFF_OSTG + 2 * v;
 #pragma unroll
@@ -255,16 +334,29 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
             }
         }
         fence_proxy_async_smem();
+        tc_fence_before();
         named_bar_sync(2, 128);
-        if (pt == 0) mbar_arrive(bar_addr(u, B_OSTAGED));
+        if (pt == 0) {
+            const int64_t t0 = u.bos + (int64_t)c * CH;
+            const int nvalid = chunk_valid(u, c);
+            const uint32_t ost = u.base + OFF_OSTG;
+            if (nvalid == CH) {
+                tma_store_3d(&maps.out, ost, 0, u.h, (int)t0);
+            } else {
+                for (int i = 0; i < nvalid; ++i)
+                    bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
+            }
+            bulk_commit();
+        }
+
         if (c + 1 < u.nchunks) {
-            const int s1 = (c + 1) & 1;
-            if (!warp_wait(bar_addr(u, B_FULL + s1), ((c + 1) >> 1) & 1, p.status, 256)) return;
-            copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + s1 * SLOT_BYTES + SL_A));
+            // the bf16 copy of S for the next GEMM1
+            copy_state_bf16(lane_addr);
             tmem_wait_st();
             tc_fence_before();
+            if (refill && w == 0) put_beta(u, c + NSLOT, lane, beta_next);
+            if (pt == 0) bulk_wait_read_all();   // the staging tile is free again
             named_bar_sync(2, 128);
-            if (pt == 0) mbar_arrive(bar_addr(u, B_SREADY));
         } else {
 #pragma unroll 1
             for (int piece = 0; piece < 8; ++piece) {
@@ -275,98 +367,14 @@ __device__ void tmem_group(const FwdParams& p, const Unit& u, int pt) {
             }
         }
     }
-}
-
-// ------------------------------------------------------------------------------
-// MMA issuer (one thread).
-// ------------------------------------------------------------------------------
-__device__ void mma_issuer(const FwdParams& p, const TmaMaps& maps, const Unit& u) {
-    constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
-    constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 160);
-    bool issued = false;
-#pragma unroll 1
-    for (int c = 0; c < u.nchunks; ++c) {
-        const int s = c & 1;
-        const uint32_t kpar = (c >> 1) & 1, cpar = c & 1;
-        const uint32_t slot = u.base + s * SLOT_BYTES;
-        if (!mbar_wait_bounded(bar_addr(u, B_FULL + s), kpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
-        if (!mbar_wait_bounded(bar_addr(u, B_SREADY), cpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-            tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
-                      make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
-        tc_commit(bar_addr(u, B_G1));
-        issued = true;
-        if (!mbar_wait_bounded(bar_addr(u, B_RREADY), cpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk)
-            tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8,
-                      make_sdesc_kmajor_noswizzle(slot + SL_W + kk * 256, 128, 512), idesc3, 1u);
-        tc_commit(bar_addr(u, B_G3));
-        tc_commit(bar_addr(u, B_EMPTY + s));
-        // write the staged chunk output: one tensor store for a full chunk, row copies for a tail
-        if (!mbar_wait_bounded(bar_addr(u, B_OSTAGED), cpar, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT)) break;
-        {
-            const int64_t t0 = u.bos + (int64_t)c * CH;
-            const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
-            const uint32_t ost = u.base + OFF_OSTG;
-            if (nvalid == CH) {
-                tma_store_3d(&maps.out, ost, 0, u.h, (int)t0);
-            } else {
-                for (int i = 0; i < nvalid; ++i)
-                    bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
-            }
-            bulk_commit();
-            bulk_wait_read_all();
-            mbar_arrive(bar_addr(u, B_OFREE));
-        }
-    }
-    bulk_wait_all();   // the output must be in global memory before the kernel ends
-    if (issued) {  // nothing of ours may still run on the tensor core when TMEM is freed
-        tc_commit(bar_addr(u, B_DRAIN));
-        mbar_wait_bounded(bar_addr(u, B_DRAIN), 0, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
-    }
-}
-
-// ------------------------------------------------------------------------------
-// TMA producer (one warp).
-// ------------------------------------------------------------------------------
-__device__ void tma_producer(const FwdParams& p, const TmaMaps& maps, const Unit& u, int lane) {
-    int issued = 0;
-#pragma unroll 1
-    for (int c = 0; c < u.nchunks; ++c) {
-        const int s = c & 1;
-        const int k = c >> 1;
-        if (c >= NSLOT && !warp_wait(bar_addr(u, B_EMPTY + s), (k - 1) & 1, p.status, 512)) break;
-        const int64_t t0 = u.bos + (int64_t)c * CH;
-        const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
-        unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        float bval = 0.f;
-        if (lane < nvalid)
-            bval = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h]);
-        reinterpret_cast<float*>(gslot + SL_BETA)[lane] = bval;
-        const uint32_t full = bar_addr(u, B_FULLTMA + s);
-        mbar_arrive(full);
-        if (lane == 0) {
-            const uint32_t slot = u.base + s * SLOT_BYTES;
-            mbar_arrive_expect_tx(full, 4u * CH * HD * 2u);
-            tma_load_3d(slot + SL_RAWQ, &maps.q, 0, u.h, (int)t0, full);
-            tma_load_3d(slot + SL_RAWK, &maps.k, 0, u.h, (int)t0, full);
-            tma_load_3d(slot + SL_RAWG, &maps.g, 0, u.h, (int)t0, full);
-            tma_load_3d(slot + SL_V, &maps.v, 0, u.h, (int)t0, full);
-        }
-        __syncwarp();
-        issued = c + 1;
-    }
-    // copies still in flight must land before the CTA exits
-    if (lane == 0) {
+    if (pt == 0) {
+        bulk_wait_all();   // the output must be in global memory before the kernel ends
+        // boxes still in flight must land before the CTA exits (only after a timeout can
+        // one be unconsumed)
         for (int c = issued - NSLOT < 0 ? 0 : issued - NSLOT; c < issued; ++c)
             mbar_wait_bounded(bar_addr(u, B_FULLTMA + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
                               WAIT_LIMIT);
     }
-    __syncwarp();
 }
 
 // ------------------------------------------------------------------------------
@@ -391,21 +399,21 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     unsigned char* kcs = u.gbase + OFF_KC;
     unsigned char* kis = u.gbase + OFF_KI;
     unsigned char* mqs = u.gbase + OFF_MQK;
-    float* Lc = reinterpret_cast<float*>(u.gbase + OFF_QC);               // after Q_c is consumed
-    float* T2 = Lc + 32 * LC;                                             // 16 x 16
+    float* Lc = reinterpret_cast<float*>(u.gbase + OFF_MISC);             // after the prefix and norms are used
+    float* T2 = reinterpret_cast<float*>(u.gbase + OFF_QC);               // after Q_c is consumed, 16 x 16
     float* X = reinterpret_cast<float*>(u.gbase + OFF_KC);                // after K_c is consumed
     unsigned char* invb = u.gbase + OFF_KC + 32 * 33 * 4;
     float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
-    float* rho = rk + 32;                                                 // 2^(G_T - C) per channel
+    float* rho = reinterpret_cast<float*>(u.gbase + OFF_MISC + MISC_L_BYTES);   // 2^(G_T - C) per channel
 
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
         const uint32_t kpar = (c >> 1) & 1;
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) return;
+        if (c == 0 && !warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) return;
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
         const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
@@ -519,22 +527,34 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         fence_proxy_async_smem();
         named_bar_sync(1, PREP_THREADS);
 
-        // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp
+        // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp.
+        //      The upper-right block of both is masked to zero, so its warps skip the products.
         {
             const int mat = pw >> 2, mt = (pw >> 1) & 1, nb = pw & 1;
             const unsigned char* Ab = mat ? qcs : kcs;
-            float acc[2][4];
+            float acc[2][4], acc2[2][4];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+            for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                uint32_t a[4], b[4];
-                ldmatrix_x4(a, Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kk * 16 + (lane >> 4) * 8));
-                ldmatrix_x4(b, kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, kk * 16 + ((lane >> 3) & 1) * 8));
-                mma_bf16_16816(acc[0], a, b[0], b[1]);
-                mma_bf16_16816(acc[1], a, b[2], b[3]);
+                for (int e = 0; e < 4; ++e) acc[t][e] = acc2[t][e] = 0.f;
+            if (nb <= mt) {
+#pragma unroll
+                for (int kk = 0; kk < 8; kk += 2) {   // two independent chains per n-tile (even / odd k steps)
+                    uint32_t a[4], b[4], a2[4], b2[4];
+                    ldmatrix_x4(a, Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kk * 16 + (lane >> 4) * 8));
+                    ldmatrix_x4(b, kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, kk * 16 + ((lane >> 3) & 1) * 8));
+                    ldmatrix_x4(a2, Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kk * 16 + 16 + (lane >> 4) * 8));
+                    ldmatrix_x4(b2, kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, kk * 16 + 16 + ((lane >> 3) & 1) * 8));
+                    mma_bf16_16816(acc[0], a, b[0], b[1]);
+                    mma_bf16_16816(acc[1], a, b[2], b[3]);
+                    mma_bf16_16816(acc2[0], a2, b2[0], b2[1]);
+                    mma_bf16_16816(acc2[1], a2, b2[2], b2[3]);
+                }
+#pragma unroll
+                for (int t = 0; t < 2; ++t)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[t][e] += acc2[t][e];
             }
-            named_bar_sync(1, PREP_THREADS);   // Q_c / K_c / K_i fully read: L and INV diag(beta) may overwrite them
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
 #pragma unroll
@@ -544,8 +564,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     const float v0 = acc[t][2 * hf], v1 = acc[t][2 * hf + 1];
                     // select, never multiply: the masked upper triangle may hold inf/NaN
                     if (mat == 0) {
-                        Lc[j * LC + i] = (j < i) ? bs[i] * v0 : 0.f;
-                        Lc[(j + 1) * LC + i] = (j + 1 < i) ? bs[i] * v1 : 0.f;
+                        if (nb <= mt) {
+                            Lc[j * LC + i] = (j < i) ? bs[i] * v0 : 0.f;
+                            Lc[(j + 1) * LC + i] = (j + 1 < i) ? bs[i] * v1 : 0.f;
+                        }
                     } else {
                         *reinterpret_cast<uint32_t*>(mqs + i * (IB * 2) + j * 2) =
                             pack_bf16x2((j <= i) ? v0 : 0.f, (j + 1 <= i) ? v1 : 0.f);   // Mqk
@@ -556,7 +578,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         named_bar_sync(1, PREP_THREADS);
 
         // ---- D: INV = X = (I + L)^-1 in fp32: the two diagonal 16x16 blocks by forward
-        //      substitution (warp 0, lane = column), then X21 = -X22 L21 X11 (all prep threads).
+        //      substitution (lane = column), then X21 = -X22 L21 X11 with tf32 mma.sync, all in warp 0.
         //      INV diag(beta) is stored transposed (row i = beta_i * column i of X) as the
         //      B operand of the W product; X is row-major [32][33] (its diagonal blocks hold
         //      zeros above the diagonal; the upper-right block is never read).
@@ -591,9 +613,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
                 *reinterpret_cast<uint4*>(row + 16) = make_uint4(0, 0, 0, 0);
             }
-        }
-        named_bar_sync(1, PREP_THREADS);
-        if (pw == 0) {
+            __syncwarp();
             // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8;
             // X21 goes straight into the transposed tile: row cc, column 16 + rr
             float t[2][4];
@@ -690,6 +710,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             }
         }
         fence_proxy_async_smem();
+        // the next chunk's boxes (normally landed long ago) are checked before the barrier,
+        // where the wait overlaps the slower warps
+        if (c + 1 < u.nchunks && !warp_wait(bar_addr(u, B_FULLTMA + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 128))
+            return;
         named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_FULL + s));
     }
@@ -699,7 +723,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tid = threadIdx.x, warp = tid >> 5;
     Unit u;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -715,19 +739,18 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(bar_addr(u, B_FULLTMA + s), 33);
             mbar_init(bar_addr(u, B_FULL + s), 1);
-            mbar_init(bar_addr(u, B_EMPTY + s), 1);
         }
         for (int b = B_G1; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
         mbar_fence_init();
     }
-    if (warp == W_TMA && lane == 0) {
+    if (tid == 32) {
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.k);
         tma_prefetch_desc(&maps.v);
         tma_prefetch_desc(&maps.g);
         tma_prefetch_desc(&maps.out);
     }
-    if (warp == W_MMA) {
+    if (warp == 0) {
         tmem_alloc(u.base + OFF_TMEMADDR, TM_COLS);
         tmem_relinquish();
     }
@@ -736,19 +759,15 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
     tc_fence_after();
     u.tmem = *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR);
 
-    if (warp < 4) {
-        tmem_group(p, u, tid);
-    } else if (warp < W_PREP0 + PREP_WARPS) {
+    if (warp < W_PREP0) {
+        chain_group(p, maps, u, tid);
+    } else {
         prep_group(p, u, tid - W_PREP0 * 32);
-    } else if (warp == W_MMA) {
-        if (lane == 0) mma_issuer(p, maps, u);
-    } else if (warp == W_TMA) {
-        tma_producer(p, maps, u, lane);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == W_MMA) {
+    if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(u.tmem, TM_COLS);
     }
