@@ -419,61 +419,68 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
 
         // ---- A: q/k row norms (row pass: 4 threads per row), gate and local prefix over
-        //      4 tokens x 4 channels
+        //      4 tokens x 4 channels; the two are independent and written so that they overlap
         uint2 qv[4], kv[4];
         float2 G01[4], G23[4];
         {
             const int row = pt >> 2, part = pt & 3;   // rows 0-31 q, 32-63 k; 32 elements per thread
             const unsigned char* rp = gslot + (row < 32 ? SL_RAWQ + row * 256 : SL_RAWK + (row - 32) * 256);
-            float2 ss = make_float2(0.f, 0.f);
+            uint4 w4[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint4 w4 = *reinterpret_cast<const uint4*>(rp + ((4 * e + part + 4 * (row & 1)) & 15) * 16);
-                const float2 x0 = bf2_to_f2(w4.x), x1 = bf2_to_f2(w4.y), x2 = bf2_to_f2(w4.z), x3 = bf2_to_f2(w4.w);
-                ss = __ffma2_rn(x0, x0, ss);
-                ss = __ffma2_rn(x1, x1, ss);
-                ss = __ffma2_rn(x2, x2, ss);
-                ss = __ffma2_rn(x3, x3, ss);
-            }
-            float sum = ss.x + ss.y;
-            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            if (part == 0) {
-                const int tok = row & 31;
-                const float rn = tok < nvalid ? rsqrtf(sum + NORM_EPS) : 0.f;
-                if (row < 32) rq[tok] = rn; else rk[tok] = rn;
+            for (int e = 0; e < 4; ++e)
+                w4[e] = *reinterpret_cast<const uint4*>(rp + ((4 * e + part + 4 * (row & 1)) & 15) * 16);
+            uint2 gw[4];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const uint32_t off = (4 * pw + r) * 256 + c0 * 2;
+                qv[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWQ + off);
+                kv[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWK + off);
+                gw[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWG + off);
             }
 
             float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int i = 4 * pw + r;
-                const uint32_t off = i * 256 + c0 * 2;
-                qv[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWQ + off);
-                kv[r] = *reinterpret_cast<const uint2*>(gslot + SL_RAWK + off);
-                const uint2 gw = *reinterpret_cast<const uint2*>(gslot + SL_RAWG + off);
-                const float2 x01 = __ffma2_rn(gmv, bf2_to_f2(gw.x), gb01);
-                const float2 x23 = __ffma2_rn(gmv, bf2_to_f2(gw.y), gb23);
+                const float2 x01 = __ffma2_rn(gmv, bf2_to_f2(gw[r].x), gb01);
+                const float2 x23 = __ffma2_rn(gmv, bf2_to_f2(gw[r].y), gb23);
                 const float bl = i < nvalid ? bcoef : 0.f;   // tokens past the end: lambda = 0
                 const float2 blv = make_float2(bl, bl);
-                const float2 l01 = __fmul2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)),
-                                                              rcp_approx(1.f + ex2_approx(x01.y))));
-                const float2 l23 = __fmul2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)),
-                                                              rcp_approx(1.f + ex2_approx(x23.y))));
-                acc01 = __fadd2_rn(acc01, l01);
-                acc23 = __fadd2_rn(acc23, l23);
+                acc01 = __ffma2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)), rcp_approx(1.f + ex2_approx(x01.y))),
+                                   acc01);
+                acc23 = __ffma2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)), rcp_approx(1.f + ex2_approx(x23.y))),
+                                   acc23);
                 G01[r] = acc01;
                 G23[r] = acc23;
             }
             *reinterpret_cast<float4*>(tot + pw * HD + c0) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
+
+            float2 ss0 = make_float2(0.f, 0.f), ss1 = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 x0 = bf2_to_f2(w4[e].x), x1 = bf2_to_f2(w4[e].y), x2 = bf2_to_f2(w4[e].z), x3 = bf2_to_f2(w4[e].w);
+                ss0 = __ffma2_rn(x0, x0, ss0);
+                ss1 = __ffma2_rn(x1, x1, ss1);
+                ss0 = __ffma2_rn(x2, x2, ss0);
+                ss1 = __ffma2_rn(x3, x3, ss1);
+            }
+            const float2 ss = __fadd2_rn(ss0, ss1);
+            float sum = ss.x + ss.y;
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            const int tok = row & 31;
+            const float rn = tok < nvalid ? rsqrtf(sum + NORM_EPS) : 0.f;
+            if (part == 0) {
+                if (row < 32) rq[tok] = rn; else rk[tok] = rn;
+            }
         }
         named_bar_sync(1, PREP_THREADS);   // raw q/k/g are no longer read after this point
 
         // ---- B: prefix combine, centered operands
         {
+            float2 T01 = make_float2(0.f, 0.f), T23 = make_float2(0.f, 0.f);
             {
                 float2 off01 = make_float2(0.f, 0.f), off23 = make_float2(0.f, 0.f);
-                float2 T01 = make_float2(0.f, 0.f), T23 = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int qq = 0; qq < PREP_WARPS; ++qq) {
                     const float4 t4 = *reinterpret_cast<const float4*>(tot + qq * HD + c0);
@@ -482,17 +489,13 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     T01 = __fadd2_rn(T01, a01);
                     T23 = __fadd2_rn(T23, a23);
                 }
-                if (pw == 0) {
-                    *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
-                        make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
-                    *reinterpret_cast<float4*>(rho + c0) = make_float4(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst),
-                                                                       ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
-                }
                 const float2 mC = make_float2(-Cst, -Cst);
+                off01 = __fadd2_rn(off01, mC);
+                off23 = __fadd2_rn(off23, mC);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {   // G - C
-                    G01[r] = __fadd2_rn(__fadd2_rn(G01[r], off01), mC);
-                    G23[r] = __fadd2_rn(__fadd2_rn(G23[r], off23), mC);
+                    G01[r] = __fadd2_rn(G01[r], off01);
+                    G23[r] = __fadd2_rn(G23[r], off23);
                 }
             }
             const float2 twoCv = make_float2(twoC, twoC);
@@ -522,6 +525,12 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     const float2 ki01 = __fmul2_rn(k01, em01), ki23 = __fmul2_rn(k23, em23);
                     *reinterpret_cast<uint2*>(kis + o) = make_uint2(f2_to_bf2(ki01), f2_to_bf2(ki23));
                 }
+            }
+            if (pw == 0) {   // a = 2^G_T (chain decay) and rho = 2^(G_T - C) (the K_r scale of the W product)
+                *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
+                    make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
+                *reinterpret_cast<float4*>(rho + c0) = make_float4(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst),
+                                                                   ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
             }
         }
         fence_proxy_async_smem();
