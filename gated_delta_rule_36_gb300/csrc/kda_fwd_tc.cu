@@ -7,9 +7,10 @@
 //
 // Per chunk (section 3 notation; R' = V^T - P, W_beta = diag(beta) INV^T [K_r | Mqk^T]):
 //   GEMM1  [O_0 | P] = S_bf16 [Q_d | K_d]^T           M128 N64  K128  (A = bf16 S from TMEM)
+//          P -= V^T                                   M128 N32  K32   (A = V from SMEM, B = -I)
 //          S = S diag(a)                              CUDA cores, during GEMM1
-//          R' = V^T - P                               CUDA cores -> bf16 -> TMEM
-//   GEMM3  [S | O] += R' W_beta                       M128 N160 K32   (A = R' from TMEM)
+//          -R' = P - V^T                              TMEM -> bf16 -> TMEM
+//   GEMM3  [S | O] += (-R') (-W_beta)                 M128 N160 K32   (A from TMEM)
 // Since U = R INV^T = R' diag(beta) INV^T, the section-3 update U [K_r | Mqk^T] equals
 // R' W_beta; W_beta depends on the chunk only, so the prep warps build it (mma.sync)
 // ahead of the recurrence and the serial chain holds two tensor-core round trips.
@@ -40,6 +41,9 @@ namespace {
 
 constexpr int TC_THREADS = 384;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
+// Single-thread duties of the chain group, spread over its warps (one per SM sub-partition):
+// warp 1 issues the MMAs, warp 2 the TMA loads and beta, warp 3 the output stores.
+constexpr int T_MMA = 32, T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
@@ -49,7 +53,7 @@ constexpr uint32_t SL_QDKD = 0;       // [Q_d | K_d]: 64 rows x 128, K-major, 12
 constexpr uint32_t SL_RAWQ = 0, SL_RAWK = 8192;
 constexpr uint32_t SL_W = 16384;      // W_beta^T: 160 rows (n) x 32 (token), K-major core layout (raw g below)
 constexpr uint32_t SL_RAWG = 16384;
-constexpr uint32_t SL_V = 26624;      // raw v [32][128]
+constexpr uint32_t SL_V = 26624;      // raw v: two [32 tokens][64] 128-byte-swizzled blocks (MN-major A of P -= V^T)
 constexpr uint32_t SL_A = 34816;      // fp32 [128]: 2^G_T
 constexpr uint32_t SL_BETA = 35328;   // fp32 [32]
 constexpr uint32_t SLOT_BYTES = 35840;
@@ -63,7 +67,8 @@ constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i (kept until the W produ
 constexpr uint32_t OFF_MQK = OFF_KI + 8192;       // Mqk (bf16 [32][40])
 constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32], then L; rho[128]
 constexpr uint32_t MISC_L_BYTES = 32 * 36 * 4;    // L (fp32, column-major [32][36]) over tot, rq, rk
-constexpr uint32_t OFF_BAR = OFF_MISC + MISC_L_BYTES + 512;
+constexpr uint32_t OFF_NEGI = OFF_MISC + MISC_L_BYTES + 512;   // -I (bf16 32 x 32, K-major core layout)
+constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
 enum { B_FULLTMA = 0, B_FULL = 2, B_G1 = 4, B_G3, B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
@@ -76,7 +81,7 @@ constexpr int IB = 40;   // bf16 row stride of INV diag(beta)
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 160, TM_SB = 192, TM_COLS = 256;
 
 struct TmaMaps {
-    CUtensorMap q, k, v, g, out;
+    CUtensorMap q, k, v, g, out;   // v: boxes of 64 channels with the 128-byte swizzle
 };
 
 struct Unit {
@@ -204,6 +209,7 @@ __device__ __forceinline__ void load_chunk_boxes(const TmaMaps& maps, const Unit
     tma_load_3d(slot + SL_RAWK, &maps.k, 0, u.h, t0, full);
     tma_load_3d(slot + SL_RAWG, &maps.g, 0, u.h, t0, full);
     tma_load_3d(slot + SL_V, &maps.v, 0, u.h, t0, full);
+    tma_load_3d(slot + SL_V + 4096, &maps.v, 64, u.h, t0, full);
 }
 
 // beta of token `lane` of chunk c (0 past the end), by a plain load: its token stride
@@ -222,6 +228,7 @@ __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b
 
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
+    constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
     constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 160);
     const int w = pt >> 5, lane = pt & 31;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
@@ -238,11 +245,19 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     }
     if (u.nchunks == 0) return;
     const int first = u.nchunks < NSLOT ? u.nchunks : NSLOT;
-    if (pt == 0)
+    if (pt == T_TMA)
         for (int c = 0; c < first; ++c) load_chunk_boxes(maps, u, c);
-    if (w == 0)
+    if (w == W_BETA)
         for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta(p, u, c, lane));
     int issued = first;
+    {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
+        const int n = pt >> 2, kb = pt & 3;
+        const uint32_t m1 = ((n >> 3) == kb) ? ((n & 1) ? 0xBF800000u : 0x0000BF80u) : 0u;   // bf16 -1 at column n
+        const int wi = (n & 7) >> 1;
+        *reinterpret_cast<uint4*>(u.gbase + OFF_NEGI + core_offset(n, 8 * kb, 32)) =
+            make_uint4(wi == 0 ? m1 : 0u, wi == 1 ? m1 : 0u, wi == 2 ? m1 : 0u, wi == 3 ? m1 : 0u);
+        fence_proxy_async_smem();
+    }
     tmem_wait_st();
     copy_state_bf16(lane_addr);
     tmem_wait_st();
@@ -259,20 +274,23 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T, and the decay by a of this chunk meanwhile
         if (!warp_wait(bar_addr(u, B_FULL + s), (c >> 1) & 1, p.status, 256)) break;
         tc_fence_after();
-        if (pt == 0) {
+        if (pt == T_MMA) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
                           make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk)   // P -= V^T: tokens 16 kk .. 16 kk + 15
+                tc_mma_ss(u.tmem + TM_P, make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024),
+                          make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512), idescv, 1u);
             tc_commit(bar_addr(u, B_G1));
         }
         decay_state(lane_addr, reinterpret_cast<const float*>(gslot + SL_A));
 
-        // R' = V^T - P -> bf16 -> TMEM (A operand of GEMM3)
+        // -R' = P - V^T (from GEMM1) -> bf16 -> TMEM (A operand of GEMM3, whose B is -W_beta)
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
         {
-            const uint16_t* vs = reinterpret_cast<const uint16_t*>(gslot + SL_V);
             uint32_t rp[16];
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -280,12 +298,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 tmem_ld16(lane_addr + TM_P + hh * 16, pr);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 16; i += 2) {
-                    const int t = hh * 16 + i;
-                    const float2 d = __ffma2_rn(make_float2(u2f(pr[i]), u2f(pr[i + 1])), make_float2(-1.f, -1.f),
-                                                make_float2(bf16_bits_to_f32(vs[t * HD + v]), bf16_bits_to_f32(vs[(t + 1) * HD + v])));
-                    rp[t >> 1] = f2_to_bf2(d);
-                }
+                for (int i = 0; i < 8; ++i) rp[hh * 8 + i] = pack_bf16x2(u2f(pr[2 * i]), u2f(pr[2 * i + 1]));
             }
             tmem_st16(lane_addr + TM_SB, rp);
             tmem_wait_st();
@@ -294,7 +307,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         named_bar_sync(2, 128);
 
         // GEMM3 [S | O] += R' W_beta
-        if (pt == 0) {
+        if (pt == T_MMA) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
@@ -310,8 +323,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const bool refill = c + NSLOT < u.nchunks;
         float beta_next = 0.f;
         if (refill) {
-            if (pt == 0) load_chunk_boxes(maps, u, c + NSLOT);
-            if (w == 0) beta_next = load_beta(p, u, c + NSLOT, lane);
+            if (pt == T_TMA) load_chunk_boxes(maps, u, c + NSLOT);
+            if (w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
             issued = c + NSLOT + 1;
         }
 
@@ -336,7 +349,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(2, 128);
-        if (pt == 0) {
+        if (pt == T_STORE) {
             const int64_t t0 = u.bos + (int64_t)c * CH;
             const int nvalid = chunk_valid(u, c);
             const uint32_t ost = u.base + OFF_OSTG;
@@ -354,8 +367,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             copy_state_bf16(lane_addr);
             tmem_wait_st();
             tc_fence_before();
-            if (refill && w == 0) put_beta(u, c + NSLOT, lane, beta_next);
-            if (pt == 0) bulk_wait_read_all();   // the staging tile is free again
+            if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
+            if (pt == T_STORE) bulk_wait_read_all();   // the staging tile is free again
             named_bar_sync(2, 128);
         } else {
 #pragma unroll 1
@@ -367,8 +380,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             }
         }
     }
-    if (pt == 0) {
-        bulk_wait_all();   // the output must be in global memory before the kernel ends
+    if (pt == T_STORE) bulk_wait_all();   // the output must be in global memory before the kernel ends
+    if (pt == T_TMA) {
         // boxes still in flight must land before the CTA exits (only after a timeout can
         // one be unconsumed)
         for (int c = issued - NSLOT < 0 ? 0 : issued - NSLOT; c < issued; ++c)
@@ -526,7 +539,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     *reinterpret_cast<uint2*>(kis + o) = make_uint2(f2_to_bf2(ki01), f2_to_bf2(ki23));
                 }
             }
-            if (pw == 0) {   // a = 2^G_T (chain decay) and rho = 2^(G_T - C) (the K_r scale of the W product)
+            if (pw == 4) {   // a = 2^G_T (chain decay) and rho = 2^(G_T - C) (the K_r scale of the W product)
                 *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
                     make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
                 *reinterpret_cast<float4*>(rho + c0) = make_float4(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst),
@@ -537,9 +550,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         named_bar_sync(1, PREP_THREADS);
 
         // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp.
-        //      The upper-right block of both is masked to zero, so its warps skip the products.
+        //      The upper-right block of both is masked to zero, so its warps (0 and 4) skip the products.
         {
-            const int mat = pw >> 2, mt = (pw >> 1) & 1, nb = pw & 1;
+            // blocks (mt, nb) of warp pw: (0,1) [all zero], (0,0), (1,0), (1,1) for pw & 3 = 0..3
+            const int bi = pw & 3, mat = pw >> 2, mt = bi >> 1, nb = (bi & 1) ^ (1 - mt);
             const unsigned char* Ab = mat ? qcs : kcs;
             float acc[2][4], acc2[2][4];
 #pragma unroll
@@ -672,7 +686,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         }
         named_bar_sync(1, PREP_THREADS);
 
-        // ---- E: W_beta^T = [K_r^T ; Mqk] INV diag(beta), 160 x 32 x 32 with mma.sync.
+        // ---- E: -W_beta^T = -[K_r^T ; Mqk] INV diag(beta), 160 x 32 x 32 with mma.sync.
         //      Rows d < 128 use K_r = K_i diag(rho): A fragments by transposed ldmatrix from
         //      K_i, rows scaled by rho_d in the epilogue.  Warp pw: rows 16 pw .. 16 pw + 15
         //      of the K_r part (all 32 columns) and one 16 x 8 tile of the Mqk part.
@@ -697,6 +711,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     for (int t = 0; t < 4; ++t) {
                         if (t >= ntn) break;
                         const int nt = nt0 + t;
+                        if (ks == 0 && nt >= 2) continue;   // INV[k][n] = 0 for k < 16 <= n
+                        if (q == 1 && mt == 8 && ks == 1) continue;   // Mqk[i][k] = 0 for i < 16 <= k
                         // B fragment of columns 8 nt .. 8 nt + 7: rows of the transposed INV diag(beta)
                         const unsigned char* bp = invb + (nt * 8 + (lane & 7)) * (IB * 2) + (ks * 16 + ((lane >> 3) & 1) * 8) * 2;
                         uint32_t b0, b1;
@@ -711,7 +727,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         const int n = mt * 16 + gq + hf * 8, i = (nt0 + t) * 8 + 2 * tq;
-                        const float sc = q == 0 ? rho[n] : 1.f;
+                        const float sc = q == 0 ? -rho[n] : -1.f;   // -W_beta (the chain feeds -R')
                         *reinterpret_cast<uint32_t*>(gslot + SL_W + core_offset(n, i, 32)) =
                             pack_bf16x2(acc[t][2 * hf] * sc, acc[t][2 * hf + 1] * sc);
                     }
@@ -799,17 +815,18 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, h, t); boxes of 128 x 1 x 32.
-bool encode_tokens_map(CUtensorMap* m, const void* ptr, int64_t T_total, int H) {
+// [T_total, H, 128] bf16 viewed as a 3-D tensor (d, h, t); boxes of `box_d` x 1 x 32
+// (box_d = 64 with the 128-byte swizzle, 128 without).
+bool encode_tokens_map(CUtensorMap* m, const void* ptr, int64_t T_total, int H, bool sw128 = false) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)HD, (cuuint64_t)H, (cuuint64_t)(T_total > 0 ? T_total : 1)};
     const cuuint64_t strides[2] = {(cuuint64_t)HD * 2, (cuuint64_t)H * HD * 2};
-    const cuuint32_t box[3] = {(cuuint32_t)HD, 1, (cuuint32_t)CH};
+    const cuuint32_t box[3] = {(cuuint32_t)(sw128 ? 64 : HD), 1, (cuuint32_t)CH};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -821,7 +838,7 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
     if (units == 0) return cudaSuccess;
     TmaMaps maps;
     if (!encode_tokens_map(&maps.q, p.q, p.T_total, p.H) || !encode_tokens_map(&maps.k, p.k, p.T_total, p.H) ||
-        !encode_tokens_map(&maps.v, p.v, p.T_total, p.H) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
+        !encode_tokens_map(&maps.v, p.v, p.T_total, p.H, true) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
         !encode_tokens_map(&maps.out, p.out, p.T_total, p.H))
         return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

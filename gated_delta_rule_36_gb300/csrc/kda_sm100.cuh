@@ -21,8 +21,8 @@ namespace kda {
 //   bit 15 A major (0 = K-major)   bit 16 B major (0 = K-major, 1 = MN-major)
 //   [17,23) N >> 3   [24,29) M >> 4
 // ---------------------------------------------------------------------------
-constexpr KDA_HD uint32_t make_idesc_bf16_f32(int M, int N, bool b_mn_major = false) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+constexpr KDA_HD uint32_t make_idesc_bf16_f32(int M, int N, bool b_mn_major = false, bool a_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
@@ -46,6 +46,15 @@ constexpr KDA_HD uint64_t make_sdesc_kmajor_noswizzle(uint32_t smem_addr, uint32
 constexpr KDA_HD uint64_t make_sdesc_kmajor_sw128(uint32_t smem_addr, uint32_t sbo = 1024) {
     return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) |
            (1ull << 46) | (2ull << 61);
+}
+
+// Shared-memory matrix descriptor for an MN-major operand in the 128-byte swizzle layout:
+// atoms of 8 K-rows x 128 B (64 bf16 along M or N), 16-byte chunks permuted by
+// chunk ^ (row % 8); `lbo` = byte distance between atoms adjacent along M/N, `sbo` =
+// byte distance between 8-row groups along K.  Layout field = 2; atoms 1 KB aligned.
+constexpr KDA_HD uint64_t make_sdesc_mnmajor_sw128(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // Byte offset of element (r, k) of a K-major bf16 tile with 64 <= kt columns in the
