@@ -398,6 +398,11 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     const int lane = pt & 31, pw = pt >> 5, gq = lane >> 2, tq = lane & 3;
     const int c0 = 4 * lane;
+    // phase B store offsets of token 4 pw (channels c0 .. c0 + 3); token 4 pw + r differs by one XOR:
+    // its row adds r to bits 8-9 (scratch tiles, 256-byte rows) or 7-8 (swizzled slot, 128-byte rows),
+    // and its 16-byte chunk index is XORed with r
+    const uint32_t oB_sc = sc128(4 * pw, c0);
+    const uint32_t oB_sw = sw128_offset(4 * pw, c0, 64);
     const float eA = expf(p.A_log[u.h]);
     const float gm = -eA * LOG2E;                       // sigmoid(x) = 1 / (1 + 2^(gm (g + dt)))
     const float4 dt = *reinterpret_cast<const float4*>(p.dt_bias + u.h * HD + c0);
@@ -515,7 +520,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int i = 4 * pw + r;
-                const uint32_t o = sc128(i, c0);
+                const uint32_t o = oB_sc ^ (uint32_t)((r << 4) | (r << 8));        // sc128(i, c0)
+                const uint32_t od = oB_sw ^ (uint32_t)((r << 4) | (r << 7));       // sw128_offset(i, c0, 64)
                 const float qs = rq[i] * p.scale, ks = rk[i];
                 const float2 k01 = __fmul2_rn(bf2_to_f2(kv[r].x), make_float2(ks, ks));
                 const float2 k23 = __fmul2_rn(bf2_to_f2(kv[r].y), make_float2(ks, ks));
@@ -525,11 +531,11 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     const float2 qc01 = __fmul2_rn(__fmul2_rn(bf2_to_f2(qv[r].x), make_float2(qs, qs)), ep01);
                     const float2 qc23 = __fmul2_rn(__fmul2_rn(bf2_to_f2(qv[r].y), make_float2(qs, qs)), ep23);
                     *reinterpret_cast<uint2*>(qcs + o) = make_uint2(f2_to_bf2(qc01), f2_to_bf2(qc23));
-                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + sw128_offset(i, c0, 64)) =
+                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + od) =
                         make_uint2(f2_to_bf2(__fmul2_rn(qc01, twoCv)), f2_to_bf2(__fmul2_rn(qc23, twoCv)));   // Q_d
                     const float2 kc01 = __fmul2_rn(k01, ep01), kc23 = __fmul2_rn(k23, ep23);
                     *reinterpret_cast<uint2*>(kcs + o) = make_uint2(f2_to_bf2(kc01), f2_to_bf2(kc23));
-                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + sw128_offset(32 + i, c0, 64)) =
+                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + (od + 32 * 128)) =
                         make_uint2(f2_to_bf2(__fmul2_rn(kc01, twoCv)), f2_to_bf2(__fmul2_rn(kc23, twoCv)));   // K_d
                 }
                 {   // 2^(C - G): K_i and K_r = K_i 2^(G_T - C)
@@ -561,13 +567,17 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) acc[t][e] = acc2[t][e] = 0.f;
             if (nb <= mt) {
+                // 16-byte chunk 2 kk + h of row r sits at chunk (2 kk + h) ^ (r % 8) = (h ^ (r % 8)) ^ 2 kk:
+                // k step kk is one XOR of the k-step-0 address with kk << 5 (the tiles are 256-byte aligned)
+                const uint32_t a0 = smem_u32(Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, (lane >> 4) * 8));
+                const uint32_t b0 = smem_u32(kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, ((lane >> 3) & 1) * 8));
 #pragma unroll
                 for (int kk = 0; kk < 8; kk += 2) {   // two independent chains per n-tile (even / odd k steps)
                     uint32_t a[4], b[4], a2[4], b2[4];
-                    ldmatrix_x4(a, Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kk * 16 + (lane >> 4) * 8));
-                    ldmatrix_x4(b, kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, kk * 16 + ((lane >> 3) & 1) * 8));
-                    ldmatrix_x4(a2, Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, kk * 16 + 16 + (lane >> 4) * 8));
-                    ldmatrix_x4(b2, kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, kk * 16 + 16 + ((lane >> 3) & 1) * 8));
+                    ldmatrix_x4_s(a, a0 ^ (kk << 5));
+                    ldmatrix_x4_s(b, b0 ^ (kk << 5));
+                    ldmatrix_x4_s(a2, a0 ^ ((kk + 1) << 5));
+                    ldmatrix_x4_s(b2, b0 ^ ((kk + 1) << 5));
                     mma_bf16_16816(acc[0], a, b[0], b[1]);
                     mma_bf16_16816(acc[1], a, b[2], b[3]);
                     mma_bf16_16816(acc2[0], a2, b2[0], b2[1]);
@@ -699,14 +709,17 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 float acc[4][4];
 #pragma unroll
                 for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+                // A of k step ks: 16 rows (4096 bytes of K_i, or 16 Mqk rows) past k step 0
+                const uint32_t aE = q == 0 ? smem_u32(kis + sc128((lane & 7) + ((lane >> 4) & 1) * 8, mt * 16 + ((lane >> 3) & 1) * 8))
+                                           : smem_u32(mqs + ((mt - 8) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * (IB * 2) +
+                                                      (lane >> 4) * 16);
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     uint32_t a[4];
                     if (q == 0)
-                        ldmatrix_x4_trans(a, kis + sc128(ks * 16 + (lane & 7) + ((lane >> 4) & 1) * 8, mt * 16 + ((lane >> 3) & 1) * 8));
+                        ldmatrix_x4_trans_s(a, aE + ks * 4096);
                     else
-                        ldmatrix_x4(a, mqs + ((mt - 8) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * (IB * 2) +
-                                           (ks * 16 + (lane >> 4) * 8) * 2);
+                        ldmatrix_x4_s(a, aE + ks * 32);
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         if (t >= ntn) break;
