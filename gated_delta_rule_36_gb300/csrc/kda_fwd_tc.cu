@@ -5,15 +5,14 @@
 // section 6); the recurrent GEMMs run as tcgen05.mma with fp32 TMEM accumulators,
 // and the small intra-chunk products as warp-level mma.sync (section 7).
 //
-// Per chunk (section 3 notation; R' = V^T - P, W_beta = diag(beta) INV^T [K_r | Mqk^T]):
+// Per chunk (section 3 notation; R = V^T - P, B2 = diag(beta) INV^T):
 //   GEMM1  [O_0 | P] = S_bf16 [Q_d | K_d]^T           M128 N64  K128  (A = bf16 S from TMEM)
 //          P -= V^T                                   M128 N32  K32   (A = V from SMEM, B = -I)
 //          S = S diag(a)                              CUDA cores, during GEMM1
-//          -R' = P - V^T                              TMEM -> bf16 -> TMEM
-//   GEMM3  [S | O] += (-R') (-W_beta)                 M128 N160 K32   (A from TMEM)
-// Since U = R INV^T = R' diag(beta) INV^T, the section-3 update U [K_r | Mqk^T] equals
-// R' W_beta; W_beta depends on the chunk only, so the prep warps build it (mma.sync)
-// ahead of the recurrence and the serial chain holds two tensor-core round trips.
+//   GEMM2  U = (-R) (-B2)                             M128 N32  K32   (A = -R in bf16 from TMEM)
+//   GEMM3  S += U K_r,  O += U Mqk^T                  M128 N128 + N32, K32 (A = U in bf16 from TMEM)
+// The prep warps build Q_d, K_d, K_r, Mqk and -B2 for a chunk (mma.sync for the 32 x 32
+// products and the inverse) while the chain runs the previous one.
 //
 // Warp roles (384 threads, up to 80 registers each):
 //   warps 0-3   chain group: thread v owns state row v (TMEM lane v): initial/final
@@ -42,8 +41,9 @@ namespace {
 constexpr int TC_THREADS = 384;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
 // Single-thread duties of the chain group, spread over its warps (one per SM sub-partition):
-// warp 1 issues the MMAs, warp 2 the TMA loads and beta, warp 3 the output stores.
-constexpr int T_MMA = 32, T_TMA = 64, W_BETA = 2, T_STORE = 96;
+// warp 1 issues the MMAs, warp 2 loads beta, warp 3 stores each output tile and then
+// refills the slot it was staged in with TMA loads.
+constexpr int T_MMA = 32, W_BETA = 2, T_STORE = 96, T_TMA = T_STORE;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
@@ -51,33 +51,36 @@ constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wai
 // Slot layout (bytes).  Raw q/k/g land where derived operands are later written.
 constexpr uint32_t SL_QDKD = 0;       // [Q_d | K_d]: 64 rows x 128, K-major, 128-B swizzle (raw q at 0, k at 8192)
 constexpr uint32_t SL_RAWQ = 0, SL_RAWK = 8192;
-constexpr uint32_t SL_W = 16384;      // W_beta^T: 160 rows (n) x 32 (token), K-major core layout (raw g below)
+constexpr uint32_t SL_KR = 16384;     // K_r [32 tokens][128]: two 64-channel blocks, 128-B swizzle (MN-major B of GEMM3)
 constexpr uint32_t SL_RAWG = 16384;
-constexpr uint32_t SL_V = 26624;      // raw v: two [32 tokens][64] 128-byte-swizzled blocks (MN-major A of P -= V^T)
-constexpr uint32_t SL_A = 34816;      // fp32 [128]: 2^G_T
-constexpr uint32_t SL_BETA = 35328;   // fp32 [32]
-constexpr uint32_t SLOT_BYTES = 35840;
+constexpr uint32_t SL_V = 24576;      // raw v, two [32][64] 128-B swizzled blocks (MN-major A of P -= V^T);
+                                      // after GEMM1 the chunk output staging tile [32 tokens][128]
+constexpr uint32_t SL_MQT = 32768;    // Mqk [32 i][32 j], K-major core layout (B of O += U Mqk^T)
+constexpr uint32_t SL_INV = 34816;    // -B2 [32 i][32 j] = -beta_j INV[i][j], K-major core layout (B of GEMM2)
+constexpr uint32_t SL_A = 36864;      // fp32 [128]: 2^G_T
+constexpr uint32_t SL_BETA = 37376;   // fp32 [32]
+constexpr uint32_t SLOT_BYTES = 37888;
 
 // Prep scratch (per CTA).  32 x 128 bf16 tiles with 16-byte chunks XOR-swizzled by
 // (row % 8), so that both the row-wise stores and ldmatrix reads are conflict-free.
-constexpr uint32_t OFF_OSTG = NSLOT * SLOT_BYTES; // chunk output staging: bf16 [32 tokens][128]
-constexpr uint32_t OFF_QC = OFF_OSTG + 8192;      // Q_c, then T2 (fp32 [16][16])
-constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then X = INV (fp32 [32][33]) and INV diag(beta)
-constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i (kept until the W product)
-constexpr uint32_t OFF_MQK = OFF_KI + 8192;       // Mqk (bf16 [32][40])
-constexpr uint32_t OFF_MISC = OFF_MQK + 2560;     // tot[8][128], rq[32], rk[32], then L; rho[128]
+constexpr uint32_t OFF_QC = NSLOT * SLOT_BYTES;   // Q_c, then T2 (fp32 [16][16])
+constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then X = INV (fp32 [32][33])
+constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i
+constexpr uint32_t OFF_MISC = OFF_KI + 8192;      // tot[8][128], rq[32], rk[32], then L
 constexpr uint32_t MISC_L_BYTES = 32 * 36 * 4;    // L (fp32, column-major [32][36]) over tot, rq, rk
-constexpr uint32_t OFF_NEGI = OFF_MISC + MISC_L_BYTES + 512;   // -I (bf16 32 x 32, K-major core layout)
+constexpr uint32_t OFF_NEGI = OFF_MISC + MISC_L_BYTES;   // -I (bf16 32 x 32, K-major core layout)
 constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
-enum { B_FULLTMA = 0, B_FULL = 2, B_G1 = 4, B_G3, B_COUNT };
+enum { B_FULLTMA = 0, B_FULL = 2, B_G1 = 4, B_G2, B_G3, B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
 static_assert(SLOT_BYTES % 1024 == 0, "slots must keep the 128-B swizzle atoms 1 KB aligned");
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs must fit one SM");
+static_assert(OFF_QC % 256 == 0 && OFF_KC % 256 == 0 && OFF_KI % 256 == 0, "scratch tiles must be 256-B aligned");
 constexpr int LC = 36;   // fp32 row stride of L (column-major)
-constexpr int IB = 40;   // bf16 row stride of INV diag(beta)
 
+// TMEM columns: S (fp32), O, P then U (fp32), and the bf16 copy of S whose first 16
+// columns carry -R and then U between the GEMMs.
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 160, TM_SB = 192, TM_COLS = 256;
 
 struct TmaMaps {
@@ -156,6 +159,22 @@ __device__ __forceinline__ void store_state16(const FwdParams& p, size_t off, co
     }
 }
 
+// The 32 fp32 P columns of this lane (-R after GEMM1, U after GEMM2) -> bf16 -> the
+// first 16 columns of the bf16 copy of S (the A operand of the next GEMM).
+__device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr) {
+    uint32_t rp[16];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pr[16];
+        tmem_ld16(lane_addr + TM_P + hh * 16, pr);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) rp[hh * 8 + i] = pack_bf16x2(u2f(pr[2 * i]), u2f(pr[2 * i + 1]));
+    }
+    tmem_st16(lane_addr + TM_SB, rp);
+    tmem_wait_st();
+}
+
 // The bf16 copy of S (the next GEMM1 operand), 8 pieces of 16 columns.
 __device__ __forceinline__ void copy_state_bf16(uint32_t lane_addr) {
 #pragma unroll 1
@@ -229,7 +248,8 @@ __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
-    constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 160);
+    constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);                // GEMM2, and O += U Mqk^T
+    constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 128, true);         // S += U K_r, B MN-major
     const int w = pt >> 5, lane = pt & 31;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     const int v = pt;
@@ -287,51 +307,50 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
         decay_state(lane_addr, reinterpret_cast<const float*>(gslot + SL_A));
 
-        // -R' = P - V^T (from GEMM1) -> bf16 -> TMEM (A operand of GEMM3, whose B is -W_beta)
+        // -R = P - V^T (from GEMM1) -> bf16 -> TMEM: A operand of GEMM2
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
-        {
-            uint32_t rp[16];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                uint32_t pr[16];
-                tmem_ld16(lane_addr + TM_P + hh * 16, pr);
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) rp[hh * 8 + i] = pack_bf16x2(u2f(pr[2 * i]), u2f(pr[2 * i + 1]));
-            }
-            tmem_st16(lane_addr + TM_SB, rp);
-            tmem_wait_st();
-        }
+        p_cols_to_bf16(lane_addr);
         tc_fence_before();
         named_bar_sync(2, 128);
-
-        // GEMM3 [S | O] += R' W_beta
-        if (pt == T_MMA) {
+        if (pt == T_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
+                tc_mma_ts(u.tmem + TM_P, u.tmem + TM_SB + kk * 8,
+                          make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512), idesc2, kk > 0);
+            tc_commit(bar_addr(u, B_G2));
+        }
+
+        // U -> bf16 -> TMEM: A operand of GEMM3
+        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) break;
+        tc_fence_after();
+        p_cols_to_bf16(lane_addr);
+        tc_fence_before();
+        named_bar_sync(2, 128);
+        if (pt == T_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 2; ++kk) {
                 tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8,
-                          make_sdesc_kmajor_noswizzle(slot + SL_W + kk * 256, 128, 512), idesc3, 1u);
+                          make_sdesc_mnmajor_sw128(slot + SL_KR + kk * 2048, 4096, 1024), idesc3, 1u);
+                tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
+                          make_sdesc_kmajor_noswizzle(slot + SL_MQT + kk * 256, 128, 512), idesc2, 1u);
+            }
             tc_commit(bar_addr(u, B_G3));
         }
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) break;
         tc_fence_after();
 
-        // the slot has been read for the last time: refill it with chunk c + 2 (beta
-        // stays in flight in a register until the end of the iteration)
+        // O of this chunk -> staging tile [token][v] in the slot's V region (GEMM1 has read V)
+        // -> one tensor store (row copies for a tail chunk); then the slot has been read for
+        // the last time and is refilled with chunk c + 2 (beta stays in flight in a register
+        // until the end of the iteration)
         const bool refill = c + NSLOT < u.nchunks;
         float beta_next = 0.f;
-        if (refill) {
-            if (pt == T_TMA) load_chunk_boxes(maps, u, c + NSLOT);
-            if (w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
-            issued = c + NSLOT + 1;
-        }
-
-        // O of this chunk -> staging tile [token][v] -> one tensor store (row copies
-        // for a tail chunk); O must leave TMEM before the next GEMM1 writes it
+        if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
         {
-            unsigned char* ost = u.gbase + OFF_OSTG + 2 * v;
+            unsigned char* ost = u.gbase + s * SLOT_BYTES + SL_V + 2 * v;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t o[16];
@@ -352,7 +371,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (pt == T_STORE) {
             const int64_t t0 = u.bos + (int64_t)c * CH;
             const int nvalid = chunk_valid(u, c);
-            const uint32_t ost = u.base + OFF_OSTG;
+            const uint32_t ost = slot + SL_V;
             if (nvalid == CH) {
                 tma_store_3d(&maps.out, ost, 0, u.h, (int)t0);
             } else {
@@ -360,7 +379,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                     bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
             }
             bulk_commit();
+            if (refill) {
+                bulk_wait_read_all();   // the staging tile is read: the slot may be overwritten
+                load_chunk_boxes(maps, u, c + NSLOT);
+            }
         }
+        if (refill) issued = c + NSLOT + 1;
 
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1
@@ -368,7 +392,6 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             tmem_wait_st();
             tc_fence_before();
             if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
-            if (pt == T_STORE) bulk_wait_read_all();   // the staging tile is free again
             named_bar_sync(2, 128);
         } else {
 #pragma unroll 1
@@ -403,6 +426,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     // and its 16-byte chunk index is XORed with r
     const uint32_t oB_sc = sc128(4 * pw, c0);
     const uint32_t oB_sw = sw128_offset(4 * pw, c0, 64);
+    const uint32_t oB_kr = sw128_offset(4 * pw, c0, 32);
     const float eA = expf(p.A_log[u.h]);
     const float gm = -eA * LOG2E;                       // sigmoid(x) = 1 / (1 + 2^(gm (g + dt)))
     const float4 dt = *reinterpret_cast<const float4*>(p.dt_bias + u.h * HD + c0);
@@ -416,15 +440,12 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     unsigned char* qcs = u.gbase + OFF_QC;
     unsigned char* kcs = u.gbase + OFF_KC;
     unsigned char* kis = u.gbase + OFF_KI;
-    unsigned char* mqs = u.gbase + OFF_MQK;
     float* Lc = reinterpret_cast<float*>(u.gbase + OFF_MISC);             // after the prefix and norms are used
     float* T2 = reinterpret_cast<float*>(u.gbase + OFF_QC);               // after Q_c is consumed, 16 x 16
     float* X = reinterpret_cast<float*>(u.gbase + OFF_KC);                // after K_c is consumed
-    unsigned char* invb = u.gbase + OFF_KC + 32 * 33 * 4;
     float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
-    float* rho = reinterpret_cast<float*>(u.gbase + OFF_MISC + MISC_L_BYTES);   // 2^(G_T - C) per channel
 
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
@@ -517,6 +538,9 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 }
             }
             const float2 twoCv = make_float2(twoC, twoC);
+            // rho = 2^(G_T - C) of this thread's channels: K_r = K_i diag(rho) = k 2^(G_T - G)
+            const float2 rho01 = make_float2(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst));
+            const float2 rho23 = make_float2(ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int i = 4 * pw + r;
@@ -543,14 +567,13 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     const float2 em23 = make_float2(ex2_approx(-G23[r].x), ex2_approx(-G23[r].y));
                     const float2 ki01 = __fmul2_rn(k01, em01), ki23 = __fmul2_rn(k23, em23);
                     *reinterpret_cast<uint2*>(kis + o) = make_uint2(f2_to_bf2(ki01), f2_to_bf2(ki23));
+                    *reinterpret_cast<uint2*>(gslot + SL_KR + (oB_kr ^ (uint32_t)((r << 4) | (r << 7)))) =
+                        make_uint2(f2_to_bf2(__fmul2_rn(ki01, rho01)), f2_to_bf2(__fmul2_rn(ki23, rho23)));   // K_r
                 }
             }
-            if (pw == 4) {   // a = 2^G_T (chain decay) and rho = 2^(G_T - C) (the K_r scale of the W product)
+            if (pw == 4)   // a = 2^G_T: the chain's decay of S
                 *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
                     make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
-                *reinterpret_cast<float4*>(rho + c0) = make_float4(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst),
-                                                                   ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
-            }
         }
         fence_proxy_async_smem();
         named_bar_sync(1, PREP_THREADS);
@@ -602,7 +625,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                             Lc[(j + 1) * LC + i] = (j + 1 < i) ? bs[i] * v1 : 0.f;
                         }
                     } else {
-                        *reinterpret_cast<uint32_t*>(mqs + i * (IB * 2) + j * 2) =
+                        *reinterpret_cast<uint32_t*>(gslot + SL_MQT + core_offset(i, j, 32)) =
                             pack_bf16x2((j <= i) ? v0 : 0.f, (j + 1 <= i) ? v1 : 0.f);   // Mqk
                     }
                 }
@@ -612,9 +635,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 
         // ---- D: INV = X = (I + L)^-1 in fp32: the two diagonal 16x16 blocks by forward
         //      substitution (lane = column), then X21 = -X22 L21 X11 with tf32 mma.sync, all in warp 0.
-        //      INV diag(beta) is stored transposed (row i = beta_i * column i of X) as the
-        //      B operand of the W product; X is row-major [32][33] (its diagonal blocks hold
-        //      zeros above the diagonal; the upper-right block is never read).
+        //      -B2[i][j] = -beta_j X[i][j] goes to the slot in the K-major core layout (the B
+        //      operand of GEMM2); X is row-major [32][33] (its diagonal blocks hold zeros above
+        //      the diagonal; the upper-right block is never read).
+        unsigned char* b2s = gslot + SL_INV;
         if (pw == 0) {
             const int o = (lane >> 4) * 16, cc = lane & 15;
             float x[16];
@@ -635,20 +659,15 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) X[(o + r) * 33 + o + cc] = x[r];
-            const float bj = bs[o + cc];
-            uint32_t w[8];
+            const float mbj = -bs[o + cc];
 #pragma unroll
-            for (int r = 0; r < 8; ++r) w[r] = pack_bf16x2(bj * x[2 * r], bj * x[2 * r + 1]);
-            unsigned char* row = invb + (o + cc) * (IB * 2);
-            *reinterpret_cast<uint4*>(row + o * 2) = make_uint4(w[0], w[1], w[2], w[3]);
-            *reinterpret_cast<uint4*>(row + o * 2 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-            if (o == 16) {   // row i >= 16, columns j < 16: X[j][i] lies above the diagonal
-                *reinterpret_cast<uint4*>(row) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(row + 16) = make_uint4(0, 0, 0, 0);
-            }
+            for (int r = 0; r < 16; ++r)
+                *reinterpret_cast<__nv_bfloat16*>(b2s + core_offset(o + r, o + cc, 32)) = __float2bfloat16_rn(mbj * x[r]);
+            // rows i < 16, columns j >= 16 lie above the diagonal: zero
+            *reinterpret_cast<uint4*>(b2s + core_offset(lane >> 1, 16 + 8 * (lane & 1), 32)) = make_uint4(0, 0, 0, 0);
             __syncwarp();
             // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8;
-            // X21 goes straight into the transposed tile: row cc, column 16 + rr
+            // X21 goes straight into -B2: row 16 + rr, columns cc, cc + 1
             float t[2][4];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) t[nt][0] = t[nt][1] = t[nt][2] = t[nt][3] = 0.f;
@@ -688,64 +707,11 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int rr = gq + (e >> 1) * 8, cc = nt * 8 + 2 * tq + (e & 1);
-                    reinterpret_cast<__nv_bfloat16*>(invb + cc * (IB * 2))[16 + rr] =
-                        __float2bfloat16_rn(-x21[nt][e] * bs[cc]);
+                for (int hf = 0; hf < 2; ++hf) {   // -B2[16 + rr][cc] = -beta_cc X21[rr][cc] = beta_cc x21
+                    const int rr = gq + hf * 8, cc = nt * 8 + 2 * tq;
+                    *reinterpret_cast<uint32_t*>(b2s + core_offset(16 + rr, cc, 32)) =
+                        pack_bf16x2(x21[nt][2 * hf] * bs[cc], x21[nt][2 * hf + 1] * bs[cc + 1]);
                 }
-        }
-        named_bar_sync(1, PREP_THREADS);
-
-        // ---- E: -W_beta^T = -[K_r^T ; Mqk] INV diag(beta), 160 x 32 x 32 with mma.sync.
-        //      Rows d < 128 use K_r = K_i diag(rho): A fragments by transposed ldmatrix from
-        //      K_i, rows scaled by rho_d in the epilogue.  Warp pw: rows 16 pw .. 16 pw + 15
-        //      of the K_r part (all 32 columns) and one 16 x 8 tile of the Mqk part.
-        {
-            const int mts[2] = {pw, 8 + (pw >> 2)};
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int mt = mts[q];
-                const int nt0 = q == 0 ? 0 : (pw & 3), ntn = q == 0 ? 4 : 1;
-                float acc[4][4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-                // A of k step ks: 16 rows (4096 bytes of K_i, or 16 Mqk rows) past k step 0
-                const uint32_t aE = q == 0 ? smem_u32(kis + sc128((lane & 7) + ((lane >> 4) & 1) * 8, mt * 16 + ((lane >> 3) & 1) * 8))
-                                           : smem_u32(mqs + ((mt - 8) * 16 + (lane & 7) + ((lane >> 3) & 1) * 8) * (IB * 2) +
-                                                      (lane >> 4) * 16);
-#pragma unroll
-                for (int ks = 0; ks < 2; ++ks) {
-                    uint32_t a[4];
-                    if (q == 0)
-                        ldmatrix_x4_trans_s(a, aE + ks * 4096);
-                    else
-                        ldmatrix_x4_s(a, aE + ks * 32);
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        if (t >= ntn) break;
-                        const int nt = nt0 + t;
-                        if (ks == 0 && nt >= 2) continue;   // INV[k][n] = 0 for k < 16 <= n
-                        if (q == 1 && mt == 8 && ks == 1) continue;   // Mqk[i][k] = 0 for i < 16 <= k
-                        // B fragment of columns 8 nt .. 8 nt + 7: rows of the transposed INV diag(beta)
-                        const unsigned char* bp = invb + (nt * 8 + (lane & 7)) * (IB * 2) + (ks * 16 + ((lane >> 3) & 1) * 8) * 2;
-                        uint32_t b0, b1;
-                        asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
-                                     : "=r"(b0), "=r"(b1) : "r"(smem_u32(bp)));
-                        mma_bf16_16816(acc[t], a, b0, b1);
-                    }
-                }
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    if (t >= ntn) break;
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int n = mt * 16 + gq + hf * 8, i = (nt0 + t) * 8 + 2 * tq;
-                        const float sc = q == 0 ? -rho[n] : -1.f;   // -W_beta (the chain feeds -R')
-                        *reinterpret_cast<uint32_t*>(gslot + SL_W + core_offset(n, i, 32)) =
-                            pack_bf16x2(acc[t][2 * hf] * sc, acc[t][2 * hf + 1] * sc);
-                    }
-                }
-            }
         }
         fence_proxy_async_smem();
         // the next chunk's boxes (normally landed long ago) are checked before the barrier,
