@@ -41,9 +41,9 @@ namespace {
 constexpr int TC_THREADS = 384;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
 // Single-thread duties of the chain group, spread over its warps (one per SM sub-partition):
-// warp 1 issues the MMAs, warp 2 loads beta, warp 3 stores each output tile and then
-// refills the slot it was staged in with TMA loads.
-constexpr int T_MMA = 32, W_BETA = 2, T_STORE = 96, T_TMA = T_STORE;
+// warp 1 issues the MMAs, warp 2 refills q, k, g and beta, warp 3 stores each output tile
+// and then refills v, whose slot region held the tile.
+constexpr int T_MMA = 32, T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
@@ -70,7 +70,9 @@ constexpr uint32_t OFF_MISC = OFF_KI + 8192;      // tot[8][128], rq[32], rk[32]
 constexpr uint32_t MISC_L_BYTES = 32 * 36 * 4;    // L (fp32, column-major [32][36]) over tot, rq, rk
 constexpr uint32_t OFF_NEGI = OFF_MISC + MISC_L_BYTES;   // -I (bf16 32 x 32, K-major core layout)
 constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
-enum { B_FULLTMA = 0, B_FULL = 2, B_G1 = 4, B_G2, B_G3, B_COUNT };
+// Per slot: FULLTMA (q, k, g boxes and beta landed), FULLV (v box landed), AREADY (the prep
+// warps wrote a), FULL (the prep warps finished the chunk).  Chain: G1, G2, G3 (MMA commits).
+enum { B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 4, B_FULL = 6, B_G1 = 8, B_G2, B_G3, B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
@@ -175,8 +177,9 @@ __device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr) {
     tmem_wait_st();
 }
 
-// The bf16 copy of S (the next GEMM1 operand), 8 pieces of 16 columns.
-__device__ __forceinline__ void copy_state_bf16(uint32_t lane_addr) {
+// One pass over S: its bf16 copy (the next GEMM1 operand, taken before the decay), then
+// S = S diag(a) in place with the next chunk's a (its GEMM3 adds to the decayed S).
+__device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* a_s) {
 #pragma unroll 1
     for (int piece = 0; piece < 8; ++piece) {
         uint32_t r[16];
@@ -186,17 +189,6 @@ __device__ __forceinline__ void copy_state_bf16(uint32_t lane_addr) {
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
         tmem_st8(lane_addr + TM_SB + piece * 8, b);
-    }
-}
-
-// S = S diag(a) in place (GEMM3 of the chunk then adds to it); runs while GEMM1 reads
-// the bf16 copy.
-__device__ __forceinline__ void decay_state(uint32_t lane_addr, const float* a_s) {
-#pragma unroll 1
-    for (int piece = 0; piece < 8; ++piece) {
-        uint32_t r[16];
-        tmem_ld16(lane_addr + TM_S + piece * 16, r);
-        tmem_wait_ld();
         const float4* a4 = reinterpret_cast<const float4*>(a_s + piece * 16);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -218,17 +210,35 @@ __device__ __forceinline__ int chunk_valid(const Unit& u, int c) {
     return (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
 }
 
-// q, k, g, v boxes of chunk c into its slot (thread 0 of the chain group).
-__device__ __forceinline__ void load_chunk_boxes(const TmaMaps& maps, const Unit& u, int c) {
+// q, k, g boxes of chunk c into its slot (on FULLTMA, which beta completes).
+__device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int c) {
     const int s = c & 1;
     const int t0 = (int)(u.bos + (int64_t)c * CH);
     const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLTMA + s);
-    mbar_arrive_expect_tx(full, 4u * CH * HD * 2u);
+    mbar_arrive_expect_tx(full, 3u * CH * HD * 2u);
     tma_load_3d(slot + SL_RAWQ, &maps.q, 0, u.h, t0, full);
     tma_load_3d(slot + SL_RAWK, &maps.k, 0, u.h, t0, full);
     tma_load_3d(slot + SL_RAWG, &maps.g, 0, u.h, t0, full);
+}
+
+// the v box of chunk c (two 64-channel halves, 128-byte swizzle) on FULLV.
+__device__ __forceinline__ void load_v(const TmaMaps& maps, const Unit& u, int c) {
+    const int s = c & 1;
+    const int t0 = (int)(u.bos + (int64_t)c * CH);
+    const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLV + s);
+    mbar_arrive_expect_tx(full, CH * HD * 2u);
     tma_load_3d(slot + SL_V, &maps.v, 0, u.h, t0, full);
     tma_load_3d(slot + SL_V + 4096, &maps.v, 64, u.h, t0, full);
+}
+
+// Pull chunk c's q, k, g, v boxes into L2 ahead of the loads that refill its slot.
+__device__ __forceinline__ void prefetch_chunk(const TmaMaps& maps, const Unit& u, int c) {
+    const int t0 = (int)(u.bos + (int64_t)c * CH);
+    tma_prefetch_l2_3d(&maps.q, 0, u.h, t0);
+    tma_prefetch_l2_3d(&maps.k, 0, u.h, t0);
+    tma_prefetch_l2_3d(&maps.g, 0, u.h, t0);
+    tma_prefetch_l2_3d(&maps.v, 0, u.h, t0);
+    tma_prefetch_l2_3d(&maps.v, 64, u.h, t0);
 }
 
 // beta of token `lane` of chunk c (0 past the end), by a plain load: its token stride
@@ -266,10 +276,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     if (u.nchunks == 0) return;
     const int first = u.nchunks < NSLOT ? u.nchunks : NSLOT;
     if (pt == T_TMA)
-        for (int c = 0; c < first; ++c) load_chunk_boxes(maps, u, c);
+        for (int c = 0; c < first; ++c) load_qkg(maps, u, c);
+    if (pt == T_STORE)
+        for (int c = 0; c < first; ++c) load_v(maps, u, c);
     if (w == W_BETA)
         for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta(p, u, c, lane));
-    int issued = first;
+    int issued = first;   // chunks whose boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
         const int n = pt >> 2, kb = pt & 3;
         const uint32_t m1 = ((n >> 3) == kb) ? ((n & 1) ? 0xBF800000u : 0x0000BF80u) : 0u;   // bf16 -1 at column n
@@ -279,37 +291,49 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         fence_proxy_async_smem();
     }
     tmem_wait_st();
-    copy_state_bf16(lane_addr);
-    tmem_wait_st();
-    tc_fence_before();
-    named_bar_sync(2, 128);
+    bool ok = warp_wait(bar_addr(u, B_AREADY), 0, p.status, 256);   // a of chunk 0
+    if (ok) {
+        copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
+        tmem_wait_st();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+    }
 
 #pragma unroll 1
-    for (int c = 0; c < u.nchunks; ++c) {
+    for (int c = 0; ok && c < u.nchunks; ++c) {
         const int s = c & 1;
-        const uint32_t cpar = c & 1;
+        const uint32_t cpar = c & 1, kpar = (c >> 1) & 1;
         const uint32_t slot = u.base + s * SLOT_BYTES;
-        const unsigned char* gslot = u.gbase + s * SLOT_BYTES;
 
-        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T, and the decay by a of this chunk meanwhile
-        if (!warp_wait(bar_addr(u, B_FULL + s), (c >> 1) & 1, p.status, 256)) break;
-        tc_fence_after();
-        if (pt == T_MMA) {
+        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T and P -= V^T, once the prep warps finished
+        // the chunk and its v box landed
+        const bool refill = c + NSLOT < u.nchunks;
+        if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
+        // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
+        if (!warp_wait(bar_addr(u, B_FULL + s), kpar, p.status, 256)) break;
+        // the prep warps are done with the slot's beta: chunk c + 2's goes in after GEMM1
+        float beta_next = 0.f;
+        if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
+        if (w == 1) {
+            if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) break;
+            tc_fence_after();
+            if (pt == T_MMA) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
-                          make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
+                              make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)   // P -= V^T: tokens 16 kk .. 16 kk + 15
-                tc_mma_ss(u.tmem + TM_P, make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024),
-                          make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512), idescv, 1u);
-            tc_commit(bar_addr(u, B_G1));
+                for (int kk = 0; kk < 2; ++kk)   // P -= V^T: tokens 16 kk .. 16 kk + 15
+                    tc_mma_ss(u.tmem + TM_P, make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024),
+                              make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512), idescv, 1u);
+                tc_commit(bar_addr(u, B_G1));
+            }
         }
-        decay_state(lane_addr, reinterpret_cast<const float*>(gslot + SL_A));
 
-        // -R = P - V^T (from GEMM1) -> bf16 -> TMEM: A operand of GEMM2
+        // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
+        if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
         p_cols_to_bf16(lane_addr);
         tc_fence_before();
         named_bar_sync(2, 128);
@@ -342,13 +366,16 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) break;
         tc_fence_after();
 
-        // O of this chunk -> staging tile [token][v] in the slot's V region (GEMM1 has read V)
-        // -> one tensor store (row copies for a tail chunk); then the slot has been read for
-        // the last time and is refilled with chunk c + 2 (beta stays in flight in a register
-        // until the end of the iteration)
-        const bool refill = c + NSLOT < u.nchunks;
-        float beta_next = 0.f;
-        if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
+        // The slot's q, k, g regions have been read for the last time: refill them with
+        // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
+        if (refill) {
+            if (pt == T_TMA) load_qkg(maps, u, c + NSLOT);
+            issued = c + NSLOT + 1;
+        }
+
+        // O of this chunk -> staging tile [token][v] in the slot's v region (GEMM1 has read
+        // v) -> one tensor store (row copies for a tail chunk); once the store has read the
+        // tile, the region takes chunk c + 2's v
         {
             unsigned char* ost = u.gbase + s * SLOT_BYTES + SL_V + 2 * v;
 #pragma unroll
@@ -380,18 +407,17 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             }
             bulk_commit();
             if (refill) {
-                bulk_wait_read_all();   // the staging tile is read: the slot may be overwritten
-                load_chunk_boxes(maps, u, c + NSLOT);
+                bulk_wait_read_all();
+                load_v(maps, u, c + NSLOT);
             }
         }
-        if (refill) issued = c + NSLOT + 1;
 
         if (c + 1 < u.nchunks) {
-            // the bf16 copy of S for the next GEMM1
-            copy_state_bf16(lane_addr);
+            // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
+            if (!warp_wait(bar_addr(u, B_AREADY + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 256)) break;
+            copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
             tmem_wait_st();
             tc_fence_before();
-            if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
             named_bar_sync(2, 128);
         } else {
 #pragma unroll 1
@@ -404,12 +430,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
     }
     if (pt == T_STORE) bulk_wait_all();   // the output must be in global memory before the kernel ends
-    if (pt == T_TMA) {
+    if (pt == T_TMA || pt == T_STORE) {
         // boxes still in flight must land before the CTA exits (only after a timeout can
         // one be unconsumed)
+        const int b0 = pt == T_TMA ? B_FULLTMA : B_FULLV;
         for (int c = issued - NSLOT < 0 ? 0 : issued - NSLOT; c < issued; ++c)
-            mbar_wait_bounded(bar_addr(u, B_FULLTMA + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
-                              WAIT_LIMIT);
+            mbar_wait_bounded(bar_addr(u, b0 + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
 }
 
@@ -577,6 +603,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         }
         fence_proxy_async_smem();
         named_bar_sync(1, PREP_THREADS);
+        if (pt == 0) mbar_arrive(bar_addr(u, B_AREADY + s));   // the chain may decay S by a
 
         // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp.
         //      The upper-right block of both is masked to zero, so its warps (0 and 4) skip the products.
@@ -742,6 +769,8 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
     if (tid == 0) {
         for (int s = 0; s < NSLOT; ++s) {
             mbar_init(bar_addr(u, B_FULLTMA + s), 33);
+            mbar_init(bar_addr(u, B_FULLV + s), 1);
+            mbar_init(bar_addr(u, B_AREADY + s), 1);
             mbar_init(bar_addr(u, B_FULL + s), 1);
         }
         for (int b = B_G1; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
