@@ -686,13 +686,20 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) X[(o + r) * 33 + o + cc] = x[r];
-            const float mbj = -bs[o + cc];
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                *reinterpret_cast<__nv_bfloat16*>(b2s + core_offset(o + r, o + cc, 32)) = __float2bfloat16_rn(mbj * x[r]);
             // rows i < 16, columns j >= 16 lie above the diagonal: zero
             *reinterpret_cast<uint4*>(b2s + core_offset(lane >> 1, 16 + 8 * (lane & 1), 32)) = make_uint4(0, 0, 0, 0);
             __syncwarp();
+            {   // -B2 row o + cc of the diagonal block: read back from X, two 16-byte stores
+                const float* xr = X + (o + cc) * 33 + o;
+                const float4 b0 = *reinterpret_cast<const float4*>(bs + o), b1 = *reinterpret_cast<const float4*>(bs + o + 4);
+                const float4 b2 = *reinterpret_cast<const float4*>(bs + o + 8), b3 = *reinterpret_cast<const float4*>(bs + o + 12);
+                const float bv[16] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w, b2.x, b2.y, b2.z, b2.w, b3.x, b3.y, b3.z, b3.w};
+                uint32_t wv[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) wv[j] = pack_bf16x2(-bv[2 * j] * xr[2 * j], -bv[2 * j + 1] * xr[2 * j + 1]);
+                *reinterpret_cast<uint4*>(b2s + core_offset(o + cc, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+                *reinterpret_cast<uint4*>(b2s + core_offset(o + cc, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+            }
             // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8;
             // X21 goes straight into -B2: row 16 + rr, columns cc, cc + 1
             float t[2][4];
