@@ -40,6 +40,27 @@ def load_peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "kda_fwd_tc_traffic.json")
+
+
+def measured_traffic(workload_name: str):
+    """DRAM bytes (read + write) of one forward launch from the committed ncu record, if the
+    record is for this workload and the kernel sources are byte-identical to the measured ones."""
+    import hashlib
+    try:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+        if rec.get("workload") != workload_name:
+            return None
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return float(rec["dram_bytes_per_launch"]) if h.hexdigest() == rec["sources_sha256"] else None
+    except Exception:
+        return None
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
 
@@ -291,7 +312,9 @@ def run_ours(args):
         "tflops": tflops,
         "tensor_frac": tflops / tc_peak,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": args.traffic, "peak_source": peak_src,
+                     "frac": achieved_gbs / hbm_peak,
+                     "traffic": args.traffic if args.traffic is not None else measured_traffic(w.name),
+                     "peak_source": peak_src,
                      "kernel_ms": kernel_ms, "algorithmic_bytes": alg_bytes},
         "clocks": clocks,
         "gpu_launches": (2 if w.packed else 1) * args.steps,
@@ -371,7 +394,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--traffic", type=float, default=None,
-                    help="ncu dram bytes (read+write) of one launch of the forward kernel, if measured")
+                    help="ncu dram bytes (read+write) of one launch of the forward kernel; by default the "
+                         "committed record in profiles/, used only while the kernel sources match it")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
