@@ -151,6 +151,16 @@ def barrier(world: int):
         dist.barrier()
 
 
+METRIC = "KDA prefill tokens/s at 1 GB300 (TFLOP/s and roofline fractions alongside)"
+
+
+def bench_config(w, world: int) -> dict:
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": w.name, "tokens": w.total_tokens, "heads": w.H, "sequences": w.num_seqs,
+            "head_dim": w.K, "chunk": 32, "state": "fp32 in/out, in place, 2 rotating buffers",
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
+
+
 def workload_totals(w):
     tokens = w.total_tokens
     th = tokens * w.H
@@ -225,12 +235,11 @@ def run_reference(args):
         tot_th += th
         tot_s += s
     value = tot_th / w.H / tot_s
-    line = {"impl": "reference", "metric": "KDA prefill tokens/s (fp64 CPU oracle)", "value": value,
+    line = {"impl": "reference", "metric": METRIC, "value": value,
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * tot_s / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": w.total_tokens, "heads": w.H, "sequences": w.num_seqs,
-                       "head_dim": w.K, "state": "fp32 in/out"},
+            "config": bench_config(w, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -302,13 +311,11 @@ def run_ours(args):
         e2e = run_e2e(kda, inp, w, dev, stream, args)
 
     line = {
-        "metric": "KDA prefill tokens/s at 1 GB300 (TFLOP/s and roofline fractions alongside)",
+        "metric": METRIC,
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": tokens, "heads": w.H, "sequences": w.num_seqs,
-                   "head_dim": w.K, "chunk": 32, "state": "fp32 in/out, in place, 2 rotating buffers",
-                   "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"},
+        "config": bench_config(w, world),
         "tflops": tflops,
         "tensor_frac": tflops / tc_peak,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
