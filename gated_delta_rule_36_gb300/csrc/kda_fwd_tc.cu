@@ -601,7 +601,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
                     make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
         }
-        fence_proxy_async_smem();
+        // (the slot operands written here are read by the tensor core only after FULL, and
+        // the proxy fence before the end-of-chunk barrier orders them)
         named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_AREADY + s));   // the chain may decay S by a
 
