@@ -674,15 +674,23 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
             for (int k = 0; k < 15; ++k) {
-                const float xk = x[k];
+                const float2 mxk = make_float2(-x[k], -x[k]);
                 const float* col = Lc + (o + k) * LC + o;
 #pragma unroll
                 for (int r4 = (k + 1) >> 2; r4 < 4; ++r4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(col + 4 * r4);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (4 * r4 + e > k) x[4 * r4 + e] = fmaf(-lv[e], xk, x[4 * r4 + e]);
+                    for (int pr = 0; pr < 2; ++pr) {   // rows 4 r4 + 2 pr and 4 r4 + 2 pr + 1 below row k
+                        const int r = 4 * r4 + 2 * pr;
+                        const float la = pr ? l4.z : l4.x, lb = pr ? l4.w : l4.y;
+                        if (r > k) {
+                            const float2 y = __ffma2_rn(make_float2(la, lb), mxk, make_float2(x[r], x[r + 1]));
+                            x[r] = y.x;
+                            x[r + 1] = y.y;
+                        } else if (r + 1 > k) {
+                            x[r + 1] = fmaf(lb, mxk.x, x[r + 1]);
+                        }
+                    }
                 }
             }
 #pragma unroll
@@ -701,7 +709,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 *reinterpret_cast<uint4*>(b2s + core_offset(o + cc, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 *reinterpret_cast<uint4*>(b2s + core_offset(o + cc, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
             }
-            // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8;
+            // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8 (fp32
+            // operands passed as they are: the tensor core uses their top 19 bits);
             // X21 goes straight into -B2: row 16 + rr, columns cc, cc + 1
             float t[2][4];
 #pragma unroll
@@ -710,11 +719,11 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             for (int ks = 0; ks < 2; ++ks) {
                 const int k0 = ks * 8 + tq;
                 // A = L21 [16 rr][16 n]: L21[rr][n] = L[16 + rr][n] = Lc[n * LC + 16 + rr]
-                const uint32_t a[4] = {f2tf32(Lc[k0 * LC + 16 + gq]), f2tf32(Lc[k0 * LC + 24 + gq]),
-                                       f2tf32(Lc[(k0 + 4) * LC + 16 + gq]), f2tf32(Lc[(k0 + 4) * LC + 24 + gq])};
+                const uint32_t a[4] = {__float_as_uint(Lc[k0 * LC + 16 + gq]), __float_as_uint(Lc[k0 * LC + 24 + gq]),
+                                       __float_as_uint(Lc[(k0 + 4) * LC + 16 + gq]), __float_as_uint(Lc[(k0 + 4) * LC + 24 + gq])};
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {   // B = X11 [16 n][16 cc]
-                    const uint32_t b0 = f2tf32(X[k0 * 33 + nt * 8 + gq]), b1 = f2tf32(X[(k0 + 4) * 33 + nt * 8 + gq]);
+                    const uint32_t b0 = __float_as_uint(X[k0 * 33 + nt * 8 + gq]), b1 = __float_as_uint(X[(k0 + 4) * 33 + nt * 8 + gq]);
                     mma_tf32_1688(t[nt], a, b0, b1);
                 }
             }
@@ -731,11 +740,11 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             for (int ks = 0; ks < 2; ++ks) {
                 const int k0 = ks * 8 + tq;
                 // A = X22 [16 rr][16 m] = X[16 + rr][16 + m]
-                const uint32_t a[4] = {f2tf32(X[(16 + gq) * 33 + 16 + k0]), f2tf32(X[(24 + gq) * 33 + 16 + k0]),
-                                       f2tf32(X[(16 + gq) * 33 + 20 + k0]), f2tf32(X[(24 + gq) * 33 + 20 + k0])};
+                const uint32_t a[4] = {__float_as_uint(X[(16 + gq) * 33 + 16 + k0]), __float_as_uint(X[(24 + gq) * 33 + 16 + k0]),
+                                       __float_as_uint(X[(16 + gq) * 33 + 20 + k0]), __float_as_uint(X[(24 + gq) * 33 + 20 + k0])};
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {   // B = T2 [16 m][16 cc]
-                    const uint32_t b0 = f2tf32(T2[k0 * 16 + nt * 8 + gq]), b1 = f2tf32(T2[(k0 + 4) * 16 + nt * 8 + gq]);
+                    const uint32_t b0 = __float_as_uint(T2[k0 * 16 + nt * 8 + gq]), b1 = __float_as_uint(T2[(k0 + 4) * 16 + nt * 8 + gq]);
                     mma_tf32_1688(x21[nt], a, b0, b1);
                 }
             }
