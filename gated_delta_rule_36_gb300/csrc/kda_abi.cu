@@ -192,13 +192,16 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     p.scale = scale;
     p.lower_bound = lower_bound;
 
-    // KDA_FWD_KERNEL=mma selects the register-state ablation kernel; the default is
-    // the tcgen05 kernel with the state resident in TMEM.
-    static const bool use_mma = [] {
+    // KDA_FWD_KERNEL selects an ablation variant: "mma" keeps the state in mma.sync
+    // registers, "tc16" uses 16-token chunks without the exponent anchor; the default is
+    // the tcgen05 kernel with 32-token chunks and the state resident in TMEM.
+    static const int variant = [] {
         const char* v = getenv("KDA_FWD_KERNEL");
-        return v != nullptr && strcmp(v, "mma") == 0;
+        if (v != nullptr && strcmp(v, "mma") == 0) return 1;
+        if (v != nullptr && strcmp(v, "tc16") == 0) return 2;
+        return 0;
     }();
-    e = use_mma ? kda::launch_fwd_mma(p, s) : kda::launch_fwd_tc(p, s);
+    e = variant == 1 ? kda::launch_fwd_mma(p, s) : variant == 2 ? kda::launch_fwd_tc16(p, s) : kda::launch_fwd_tc(p, s);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }

@@ -26,6 +26,9 @@ size_t fwd_mma_smem_bytes();
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream);
 size_t fwd_tc_smem_bytes();
 
+// The same with 16-token chunks and no exponent anchor: the chunk-size ablation.
+cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t stream);
+
 }  // namespace kda
 
 namespace kda {
