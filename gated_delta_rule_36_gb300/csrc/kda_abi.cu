@@ -193,15 +193,19 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     p.lower_bound = lower_bound;
 
     // KDA_FWD_KERNEL selects an ablation variant: "mma" keeps the state in mma.sync
-    // registers, "tc16" uses 16-token chunks without the exponent anchor; the default is
-    // the tcgen05 kernel with 32-token chunks and the state resident in TMEM.
+    // registers, "tc16" uses 16-token chunks without the exponent anchor, "tcbf16" rounds
+    // the carried state to bf16 at every chunk; the default is the tcgen05 kernel with
+    // 32-token chunks and the fp32 state resident in TMEM.
     static const int variant = [] {
         const char* v = getenv("KDA_FWD_KERNEL");
         if (v != nullptr && strcmp(v, "mma") == 0) return 1;
         if (v != nullptr && strcmp(v, "tc16") == 0) return 2;
+        if (v != nullptr && strcmp(v, "tcbf16") == 0) return 3;
         return 0;
     }();
-    e = variant == 1 ? kda::launch_fwd_mma(p, s) : variant == 2 ? kda::launch_fwd_tc16(p, s) : kda::launch_fwd_tc(p, s);
+    e = variant == 1   ? kda::launch_fwd_mma(p, s)
+        : variant == 2 ? kda::launch_fwd_tc16(p, s)
+                       : kda::launch_fwd_tc(p, s, variant == 3);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }

@@ -179,6 +179,9 @@ __device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr) {
 
 // One pass over S: its bf16 copy (the next GEMM1 operand, taken before the decay), then
 // S = S diag(a) in place with the next chunk's a (its GEMM3 adds to the decayed S).
+// kBf16State (the state-precision ablation) decays the bf16 copy instead, i.e. rounds the
+// carried state to bf16 at every chunk boundary, as a bf16 state store would.
+template <bool kBf16State>
 __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* a_s) {
 #pragma unroll 1
     for (int piece = 0; piece < 8; ++piece) {
@@ -189,6 +192,13 @@ __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* 
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
         tmem_st8(lane_addr + TM_SB + piece * 8, b);
+        if (kBf16State) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                r[2 * j] = b[j] << 16;
+                r[2 * j + 1] = b[j] & 0xffff0000u;
+            }
+        }
         const float4* a4 = reinterpret_cast<const float4*>(a_s + piece * 16);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -255,6 +265,7 @@ __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b
     mbar_arrive(bar_addr(u, B_FULLTMA + (c & 1)));
 }
 
+template <bool kBf16State>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
@@ -293,7 +304,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     tmem_wait_st();
     bool ok = warp_wait(bar_addr(u, B_AREADY), 0, p.status, 256);   // a of chunk 0
     if (ok) {
-        copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
+        copy_and_decay<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
         tmem_wait_st();
         tc_fence_before();
         named_bar_sync(2, 128);
@@ -415,7 +426,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
             if (!warp_wait(bar_addr(u, B_AREADY + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 256)) break;
-            copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
+            copy_and_decay<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
             tmem_wait_st();
             tc_fence_before();
             named_bar_sync(2, 128);
@@ -767,6 +778,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     }
 }
 
+template <bool kBf16State>
 __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
@@ -810,7 +822,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
     u.tmem = *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR);
 
     if (warp < W_PREP0) {
-        chain_group(p, maps, u, tid);
+        chain_group<kBf16State>(p, maps, u, tid);
     } else {
         prep_group(p, u, tid - W_PREP0 * 32);
     }
@@ -858,7 +870,7 @@ bool encode_tokens_map(CUtensorMap* m, const void* ptr, int64_t T_total, int H, 
 
 size_t fwd_tc_smem_bytes() { return SMEM_BYTES; }
 
-cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state) {
     const int units = p.nseq * p.H;
     if (units == 0) return cudaSuccess;
     TmaMaps maps;
@@ -866,10 +878,10 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream) {
         !encode_tokens_map(&maps.v, p.v, p.T_total, p.H, true) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
         !encode_tokens_map(&maps.out, p.out, p.T_total, p.H))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(kda_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+    auto kernel = bf16_state ? kda_fwd_tc_kernel<true> : kda_fwd_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kda_fwd_tc_kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
+    kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
     return cudaGetLastError();
 }
 

@@ -22,8 +22,9 @@ cudaError_t launch_schedule(const int64_t* cu_seqlens, int nseq, int64_t T_total
 cudaError_t launch_fwd_mma(const FwdParams& p, cudaStream_t stream);
 size_t fwd_mma_smem_bytes();
 
-// tcgen05 forward (one CTA per unit, two per SM, state resident in TMEM).
-cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream);
+// tcgen05 forward (one CTA per unit, two per SM, state resident in TMEM).  bf16_state
+// rounds the carried state to bf16 at every chunk boundary: the state-precision ablation.
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state = false);
 size_t fwd_tc_smem_bytes();
 
 // The same with 16-token chunks and no exponent anchor: the chunk-size ablation.

@@ -220,3 +220,17 @@ def test_forward_replays_from_a_cuda_graph():
         for row0, row1 in zip(src.cu_seqlens[:-1].tolist(), src.cu_seqlens[1:].tolist()):
             assert torch.equal(out[:, row0:row1].cpu(), ref_out[:, row0:row1].cpu())
         assert torch.equal(final.cpu(), ref_final.cpu())
+
+
+@pytest.mark.parametrize("T", [1024, 4096])
+def test_long_memory_keeps_state_precision(T):
+    """Without decay (lower_bound = 0) the state remembers every token.  The fp32 state
+    held in TMEM must stay within the fp32 tolerance over thousands of tokens; a state
+    rounded to bf16 at every chunk boundary (KDA_FWD_KERNEL=tcbf16) drifts past it."""
+    w = Workload(f"mem{T}", 31, H=4, B=1, T=T, init_dtype=f32, final_dtype=f32, lower_bound=0.0)
+    inp = make_inputs(w, "cpu")
+    inp.beta.mul_(0.2)   # moderate writes: the memory stays long
+    out, final, bits = run_gpu(inp)
+    assert bits == 0
+    ref_out, ref_final = oracle_full(inp)
+    check_full(inp, out, final, ref_out, ref_final)
