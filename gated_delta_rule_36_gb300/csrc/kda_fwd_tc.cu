@@ -484,6 +484,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
 
+    if (pt < 64)   // -B2[i][j] = 0 for i < 16 <= j, in both slots (nothing else writes there)
+        *reinterpret_cast<uint4*>(u.gbase + (pt >> 5) * SLOT_BYTES + SL_INV +
+                                  core_offset((pt & 31) >> 1, 16 + 8 * (pt & 1), 32)) = make_uint4(0, 0, 0, 0);
+
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
@@ -706,20 +710,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             }
 #pragma unroll
             for (int r = 0; r < 16; ++r) X[(o + r) * 33 + o + cc] = x[r];
-            // rows i < 16, columns j >= 16 lie above the diagonal: zero
-            *reinterpret_cast<uint4*>(b2s + core_offset(lane >> 1, 16 + 8 * (lane & 1), 32)) = make_uint4(0, 0, 0, 0);
             __syncwarp();
-            {   // -B2 row o + cc of the diagonal block: read back from X, two 16-byte stores
-                const float* xr = X + (o + cc) * 33 + o;
-                const float4 b0 = *reinterpret_cast<const float4*>(bs + o), b1 = *reinterpret_cast<const float4*>(bs + o + 4);
-                const float4 b2 = *reinterpret_cast<const float4*>(bs + o + 8), b3 = *reinterpret_cast<const float4*>(bs + o + 12);
-                const float bv[16] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w, b2.x, b2.y, b2.z, b2.w, b3.x, b3.y, b3.z, b3.w};
-                uint32_t wv[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) wv[j] = pack_bf16x2(-bv[2 * j] * xr[2 * j], -bv[2 * j + 1] * xr[2 * j + 1]);
-                *reinterpret_cast<uint4*>(b2s + core_offset(o + cc, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                *reinterpret_cast<uint4*>(b2s + core_offset(o + cc, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
-            }
+            named_bar_arrive(3, 64);   // warp 1 writes the diagonal blocks of -B2 from X
             // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8 (fp32
             // operands passed as they are: the tensor core uses their top 19 bits);
             // X21 goes straight into -B2: row 16 + rr, columns cc, cc + 1
@@ -767,6 +759,18 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     *reinterpret_cast<uint32_t*>(b2s + core_offset(16 + rr, cc, 32)) =
                         pack_bf16x2(x21[nt][2 * hf] * bs[cc], x21[nt][2 * hf + 1] * bs[cc + 1]);
                 }
+        } else if (pw == 1) {   // -B2 row n = lane of a diagonal block, read back from X: two 16-byte stores
+            named_bar_sync(3, 64);
+            const int n = lane, o = n & 16;
+            const float* xr = X + n * 33 + o;
+            const float4 b0 = *reinterpret_cast<const float4*>(bs + o), b1 = *reinterpret_cast<const float4*>(bs + o + 4);
+            const float4 b2 = *reinterpret_cast<const float4*>(bs + o + 8), b3 = *reinterpret_cast<const float4*>(bs + o + 12);
+            const float bv[16] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w, b2.x, b2.y, b2.z, b2.w, b3.x, b3.y, b3.z, b3.w};
+            uint32_t wv[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) wv[j] = pack_bf16x2(-bv[2 * j] * xr[2 * j], -bv[2 * j + 1] * xr[2 * j + 1]);
+            *reinterpret_cast<uint4*>(b2s + core_offset(n, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            *reinterpret_cast<uint4*>(b2s + core_offset(n, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
         }
         fence_proxy_async_smem();
         // the next chunk's boxes (normally landed long ago) are checked before the barrier,
