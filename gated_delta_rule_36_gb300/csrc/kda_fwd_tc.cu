@@ -11,17 +11,19 @@
 //          S = S diag(a)                              CUDA cores, during GEMM1
 //   GEMM2  U = (-R) (-B2)                             M128 N32  K32   (A = -R in bf16 from TMEM)
 //   GEMM3  S += U K_r,  O += U Mqk^T                  M128 N128 + N32, K32 (A = U in bf16 from TMEM)
-// The prep warps build Q_d, K_d, K_r, Mqk and -B2 for a chunk (mma.sync for the 32 x 32
-// products and the inverse) while the chain runs the previous one.
+// The prep warps build Q_d, K_d, K_r, Mqk and L for a chunk (mma.sync for the 32 x 32
+// products) and the inverse warp turns L into -B2, while the chain runs the previous one.
 //
-// Warp roles (384 threads, up to 80 registers each):
+// Warp roles (416 threads, up to 72 registers each):
 //   warps 0-3   chain group: thread v owns state row v (TMEM lane v): initial/final
 //               state I/O, the bf16 copy of S, the decay, R' and the chunk output O.
-//               Its thread 0 also issues the tensor-core MMAs, the TMA loads of each
-//               chunk's q, k, v, g boxes and the TMA store of each output tile; its
-//               warp 0 loads beta and owns the TMEM allocation.
+//               Single threads of its warps issue the tensor-core MMAs (warp 1), the
+//               TMA loads of q, k, g and beta (warp 2), and the output store and v
+//               loads (warp 3); warp 0 owns the TMEM allocation.
 //   warps 4-11  prep group: gate, prefix, q/k norms, centered operands (section 2),
-//               K_c K_i^T and Q_c K_i^T with mma.sync, the 32x32 inverse, W_beta.
+//               K_c K_i^T and Q_c K_i^T with mma.sync.
+//   warp 12     inverse warp: (I + L)^-1 and -B2 of chunk c while the prep group
+//               builds chunk c + 1.
 // A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
 // consumer (section 4): the chain refills a slot as soon as GEMM3 has read it, and
 // every mbarrier wait is bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
@@ -38,8 +40,9 @@
 namespace kda {
 namespace {
 
-constexpr int TC_THREADS = 384;
+constexpr int TC_THREADS = 416;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
+constexpr int W_INV = W_PREP0 + PREP_WARPS;   // the inverse warp: (I + L)^-1 of chunk c while the prep warps take c + 1
 // Single-thread duties of the chain group, spread over its warps (one per SM sub-partition):
 // warp 1 issues the MMAs, warp 2 refills q, k, g and beta, warp 3 stores each output tile
 // and then refills v, whose slot region held the tile.
@@ -63,23 +66,42 @@ constexpr uint32_t SLOT_BYTES = 37888;
 
 // Prep scratch (per CTA).  32 x 128 bf16 tiles with 16-byte chunks XOR-swizzled by
 // (row % 8), so that both the row-wise stores and ldmatrix reads are conflict-free.
-constexpr uint32_t OFF_QC = NSLOT * SLOT_BYTES;   // Q_c, then T2 (fp32 [16][16])
-constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c, then X = INV (fp32 [32][33])
+constexpr uint32_t OFF_QC = NSLOT * SLOT_BYTES;   // Q_c
+constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c
 constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i
-constexpr uint32_t OFF_MISC = OFF_KI + 8192;      // tot[8][128], rq[32], rk[32], then L
-constexpr uint32_t MISC_L_BYTES = 32 * 36 * 4;    // L (fp32, column-major [32][36]) over tot, rq, rk
-constexpr uint32_t OFF_NEGI = OFF_MISC + MISC_L_BYTES;   // -I (bf16 32 x 32, K-major core layout)
+constexpr uint32_t OFF_MISC = OFF_KI + 8192;      // tot[8][128], rq[32], rk[32]
+constexpr uint32_t MISC_BYTES = (8 * 128 + 64) * 4;
+// L = strictLower(diag(beta) K_c K_i^T) in fp32, its three nonzero 16 x 16 blocks, each
+// column-major with a column stride of LB floats: L11 at 0, L22 at 336 (16 floats past its
+// 320-float block, so that the two half-warps of the substitution read different banks), L21 at 672.
+constexpr int LB = 20;
+constexpr int LB_11 = 0, LB_22 = 336, LB_21 = 672;
+constexpr uint32_t OFF_L = OFF_MISC + MISC_BYTES;
+constexpr uint32_t L_BYTES = (LB_21 + 16 * LB) * 4;
+// X = INV's two diagonal blocks (fp32, row-major, row stride XB floats): X11 at 0, X22 at
+// XB_22 (16 floats past its block for the same reason).  Private to the inverse warp.
+constexpr int XB = 24;
+constexpr int XB_22 = 16 * XB + 16;
+constexpr uint32_t OFF_X = OFF_L + L_BYTES;
+constexpr uint32_t X_BYTES = (XB_22 + 16 * XB) * 4;
+constexpr uint32_t OFF_NEGI = OFF_X + X_BYTES;   // -I (bf16 32 x 32, K-major core layout)
 constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
 // Per slot: FULLTMA (q, k, g boxes and beta landed), FULLV (v box landed), AREADY (the prep
-// warps wrote a), FULL (the prep warps finished the chunk).  Chain: G1, G2, G3 (MMA commits).
-enum { B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 4, B_FULL = 6, B_G1 = 8, B_G2, B_G3, B_COUNT };
+// warps wrote a), FULLP (the prep warps finished the chunk's operands and L), FULLD (the
+// inverse warp wrote -B2).  LFREE: the inverse warp has read L.  Chain: G1, G2, G3 (MMA commits).
+enum { B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 4, B_FULLP = 6, B_FULLD = 8, B_LFREE = 10, B_G1, B_G2, B_G3, B_COUNT };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
 static_assert(SLOT_BYTES % 1024 == 0, "slots must keep the 128-B swizzle atoms 1 KB aligned");
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs must fit one SM");
 static_assert(OFF_QC % 256 == 0 && OFF_KC % 256 == 0 && OFF_KI % 256 == 0, "scratch tiles must be 256-B aligned");
-constexpr int LC = 36;   // fp32 row stride of L (column-major)
+static_assert(OFF_L % 16 == 0 && OFF_X % 16 == 0 && OFF_NEGI % 16 == 0, "float4 / descriptor alignment");
+
+// Index of element (i, j), j < 16 or i, j >= 16, of L in its block layout.
+__host__ __device__ constexpr int l_index(int i, int j) {
+    return (i < 16 ? LB_11 : (j < 16 ? LB_21 : LB_22)) + (j & 15) * LB + (i & 15);
+}
 
 // TMEM columns: S (fp32), O, P then U (fp32), and the bf16 copy of S whose first 16
 // columns carry -R and then U between the GEMMs.
@@ -316,13 +338,13 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const uint32_t cpar = c & 1, kpar = (c >> 1) & 1;
         const uint32_t slot = u.base + s * SLOT_BYTES;
 
-        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T and P -= V^T, once the prep warps finished
-        // the chunk and its v box landed
+        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T and P -= V^T, once the prep warps wrote the
+        // chunk's operands and its v box landed
         const bool refill = c + NSLOT < u.nchunks;
         if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
         // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
-        if (!warp_wait(bar_addr(u, B_FULL + s), kpar, p.status, 256)) break;
-        // the prep warps are done with the slot's beta: chunk c + 2's goes in after GEMM1
+        if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) break;
+        // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
         float beta_next = 0.f;
         if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
         if (w == 1) {
@@ -341,11 +363,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             }
         }
 
-        // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2
+        // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
-        if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
         p_cols_to_bf16(lane_addr);
+        if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) break;
+        if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
         tc_fence_before();
         named_bar_sync(2, 128);
         if (pt == T_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
@@ -477,23 +500,17 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     unsigned char* qcs = u.gbase + OFF_QC;
     unsigned char* kcs = u.gbase + OFF_KC;
     unsigned char* kis = u.gbase + OFF_KI;
-    float* Lc = reinterpret_cast<float*>(u.gbase + OFF_MISC);             // after the prefix and norms are used
-    float* T2 = reinterpret_cast<float*>(u.gbase + OFF_QC);               // after Q_c is consumed, 16 x 16
-    float* X = reinterpret_cast<float*>(u.gbase + OFF_KC);                // after K_c is consumed
+    float* Lb = reinterpret_cast<float*>(u.gbase + OFF_L);
     float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
-
-    if (pt < 64)   // -B2[i][j] = 0 for i < 16 <= j, in both slots (nothing else writes there)
-        *reinterpret_cast<uint4*>(u.gbase + (pt >> 5) * SLOT_BYTES + SL_INV +
-                                  core_offset((pt & 31) >> 1, 16 + 8 * (pt & 1), 32)) = make_uint4(0, 0, 0, 0);
 
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int s = c & 1;
         const uint32_t kpar = (c >> 1) & 1;
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        if (c == 0 && !warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) return;
+        if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) return;
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
         const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
@@ -616,13 +633,14 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 *reinterpret_cast<float4*>(gslot + SL_A + c0 * 4) =
                     make_float4(ex2_approx(T01.x), ex2_approx(T01.y), ex2_approx(T23.x), ex2_approx(T23.y));
         }
-        // (the slot operands written here are read by the tensor core only after FULL, and
+        // (the slot operands written here are read by the tensor core only after FULLP, and
         // the proxy fence before the end-of-chunk barrier orders them)
         named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_AREADY + s));   // the chain may decay S by a
 
         // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp.
-        //      The upper-right block of both is masked to zero, so its warps (0 and 4) skip the products.
+        //      The upper-right block of both is masked to zero, so its warps (0 and 4) skip the products
+        //      (and L keeps no such block).
         {
             // blocks (mt, nb) of warp pw: (0,1) [all zero], (0,0), (1,0), (1,1) for pw & 3 = 0..3
             const int bi = pw & 3, mat = pw >> 2, mt = bi >> 1, nb = (bi & 1) ^ (1 - mt);
@@ -653,6 +671,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 for (int t = 0; t < 2; ++t)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[t][e] += acc2[t][e];
+                // L is rewritten only once the inverse warp has read the previous chunk's
+                if (mat == 0 && c > 0 && !warp_wait(bar_addr(u, B_LFREE), (c - 1) & 1, p.status)) return;
             }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -664,8 +684,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     // select, never multiply: the masked upper triangle may hold inf/NaN
                     if (mat == 0) {
                         if (nb <= mt) {
-                            Lc[j * LC + i] = (j < i) ? bs[i] * v0 : 0.f;
-                            Lc[(j + 1) * LC + i] = (j + 1 < i) ? bs[i] * v1 : 0.f;
+                            Lb[l_index(i, j)] = (j < i) ? bs[i] * v0 : 0.f;
+                            Lb[l_index(i, j + 1)] = (j + 1 < i) ? bs[i] * v1 : 0.f;
                         }
                     } else {
                         *reinterpret_cast<uint32_t*>(gslot + SL_MQT + core_offset(i, j, 32)) =
@@ -674,23 +694,53 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 }
             }
         }
+        fence_proxy_async_smem();   // Q_d, K_d, K_r, Mqk are read by the tensor core
         named_bar_sync(1, PREP_THREADS);
+        if (pt == 0) mbar_arrive(bar_addr(u, B_FULLP + s));
+    }
+}
 
-        // ---- D: INV = X = (I + L)^-1 in fp32: the two diagonal 16x16 blocks by forward
-        //      substitution (lane = column), then X21 = -X22 L21 X11 with tf32 mma.sync, all in warp 0.
-        //      -B2[i][j] = -beta_j X[i][j] goes to the slot in the K-major core layout (the B
-        //      operand of GEMM2); X is row-major [32][33] (its diagonal blocks hold zeros above
-        //      the diagonal; the upper-right block is never read).
-        unsigned char* b2s = gslot + SL_INV;
-        if (pw == 0) {
-            const int o = (lane >> 4) * 16, cc = lane & 15;
+// ------------------------------------------------------------------------------
+// Inverse warp: INV = X = (I + L)^-1 of chunk c, in fp32, while the prep warps take chunk
+// c + 1.  The two diagonal 16 x 16 blocks by forward substitution (lane = column; lanes
+// 0-15 block 1, lanes 16-31 block 2), then X21 = -X22 L21 X11, computed transposed with tf32
+// mma.sync (fp32 operands passed as they are: the tensor core uses their top 19 bits):
+// T2^T = X11^T L21^T, then X21^T = -T2^T X22^T, whose A operand is the first product's
+// accumulator with its k index permuted (k slot t <-> column 2t, slot t + 4 <-> column
+// 2t + 1, and the B operand rows permuted alike).
+// -B2[i][j] = -beta_j X[i][j] goes to the slot in the K-major core layout (the B operand
+// of GEMM2); its upper-right block is zero and written once.
+// ------------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t bf16_bits(float x) { return (uint16_t)(pack_bf16x2(x, 0.f) & 0xffffu); }
+
+__device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
+    const int gq = lane >> 2, tq = lane & 3;
+    const int b = lane >> 4, cc = lane & 15;   // substitution: block b, column cc
+    const float* Lb = reinterpret_cast<const float*>(u.gbase + OFF_L);
+    float* Xb = reinterpret_cast<float*>(u.gbase + OFF_X);
+#pragma unroll
+    for (int s = 0; s < NSLOT; ++s)   // -B2[i][j] = 0 for i < 16 <= j (nothing else writes there)
+        *reinterpret_cast<uint4*>(u.gbase + s * SLOT_BYTES + SL_INV + core_offset(lane >> 1, 16 + 8 * (lane & 1), 32)) =
+            make_uint4(0, 0, 0, 0);
+
+#pragma unroll 1
+    for (int c = 0; c < u.nchunks; ++c) {
+        const int s = c & 1;
+        const uint32_t kpar = (c >> 1) & 1;
+        unsigned char* b2s = u.gbase + s * SLOT_BYTES + SL_INV;
+        const float* bs = reinterpret_cast<const float*>(u.gbase + s * SLOT_BYTES + SL_BETA);
+        if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 128)) return;
+
+        // ---- diagonal blocks: x[r] = X_bb[r][cc]
+        {
+            const float* Ld = Lb + (b ? LB_22 : LB_11);
             float x[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
             for (int k = 0; k < 15; ++k) {
                 const float2 mxk = make_float2(-x[k], -x[k]);
-                const float* col = Lc + (o + k) * LC + o;
+                const float* col = Ld + k * LB;
 #pragma unroll
                 for (int r4 = (k + 1) >> 2; r4 < 4; ++r4) {
                     const float4 l4 = *reinterpret_cast<const float4*>(col + 4 * r4);
@@ -708,77 +758,61 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     }
                 }
             }
+            // X_bb to shared memory for the block product; -B2 of the diagonal block from registers
+            float* xc = Xb + (b ? XB_22 : 0) + cc;
+            const float nbeta = -bs[16 * b + cc];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) X[(o + r) * 33 + o + cc] = x[r];
-            __syncwarp();
-            named_bar_arrive(3, 64);   // warp 1 writes the diagonal blocks of -B2 from X
-            // T2 = L21 X11 and X21 = -X22 T2 (16 x 16 x 16 each) with tf32 mma.sync m16n8k8 (fp32
-            // operands passed as they are: the tensor core uses their top 19 bits);
-            // X21 goes straight into -B2: row 16 + rr, columns cc, cc + 1
-            float t[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) t[nt][0] = t[nt][1] = t[nt][2] = t[nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = ks * 8 + tq;
-                // A = L21 [16 rr][16 n]: L21[rr][n] = L[16 + rr][n] = Lc[n * LC + 16 + rr]
-                const uint32_t a[4] = {__float_as_uint(Lc[k0 * LC + 16 + gq]), __float_as_uint(Lc[k0 * LC + 24 + gq]),
-                                       __float_as_uint(Lc[(k0 + 4) * LC + 16 + gq]), __float_as_uint(Lc[(k0 + 4) * LC + 24 + gq])};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {   // B = X11 [16 n][16 cc]
-                    const uint32_t b0 = __float_as_uint(X[k0 * 33 + nt * 8 + gq]), b1 = __float_as_uint(X[(k0 + 4) * 33 + nt * 8 + gq]);
-                    mma_tf32_1688(t[nt], a, b0, b1);
-                }
+            for (int r = 0; r < 16; ++r) {
+                xc[r * XB] = x[r];
+                *reinterpret_cast<uint16_t*>(b2s + core_offset(16 * b + r, 16 * b + cc, 32)) = bf16_bits(nbeta * x[r]);
             }
-            // T2 to shared memory (the second product reads it as its B operand)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) T2[(gq + (e >> 1) * 8) * 16 + nt * 8 + 2 * tq + (e & 1)] = t[nt][e];
-            __syncwarp();
-            float x21[2][4];
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) x21[nt][0] = x21[nt][1] = x21[nt][2] = x21[nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int k0 = ks * 8 + tq;
-                // A = X22 [16 rr][16 m] = X[16 + rr][16 + m]
-                const uint32_t a[4] = {__float_as_uint(X[(16 + gq) * 33 + 16 + k0]), __float_as_uint(X[(24 + gq) * 33 + 16 + k0]),
-                                       __float_as_uint(X[(16 + gq) * 33 + 20 + k0]), __float_as_uint(X[(24 + gq) * 33 + 20 + k0])};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {   // B = T2 [16 m][16 cc]
-                    const uint32_t b0 = __float_as_uint(T2[k0 * 16 + nt * 8 + gq]), b1 = __float_as_uint(T2[(k0 + 4) * 16 + nt * 8 + gq]);
-                    mma_tf32_1688(x21[nt], a, b0, b1);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {   // -B2[16 + rr][cc] = -beta_cc X21[rr][cc] = beta_cc x21
-                    const int rr = gq + hf * 8, cc = nt * 8 + 2 * tq;
-                    *reinterpret_cast<uint32_t*>(b2s + core_offset(16 + rr, cc, 32)) =
-                        pack_bf16x2(x21[nt][2 * hf] * bs[cc], x21[nt][2 * hf + 1] * bs[cc + 1]);
-                }
-        } else if (pw == 1) {   // -B2 row n = lane of a diagonal block, read back from X: two 16-byte stores
-            named_bar_sync(3, 64);
-            const int n = lane, o = n & 16;
-            const float* xr = X + n * 33 + o;
-            const float4 b0 = *reinterpret_cast<const float4*>(bs + o), b1 = *reinterpret_cast<const float4*>(bs + o + 4);
-            const float4 b2 = *reinterpret_cast<const float4*>(bs + o + 8), b3 = *reinterpret_cast<const float4*>(bs + o + 12);
-            const float bv[16] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w, b2.x, b2.y, b2.z, b2.w, b3.x, b3.y, b3.z, b3.w};
-            uint32_t wv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) wv[j] = pack_bf16x2(-bv[2 * j] * xr[2 * j], -bv[2 * j + 1] * xr[2 * j + 1]);
-            *reinterpret_cast<uint4*>(b2s + core_offset(n, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            *reinterpret_cast<uint4*>(b2s + core_offset(n, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
         }
-        fence_proxy_async_smem();
-        // the next chunk's boxes (normally landed long ago) are checked before the barrier,
-        // where the wait overlaps the slower warps
-        if (c + 1 < u.nchunks && !warp_wait(bar_addr(u, B_FULLTMA + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 128))
-            return;
-        named_bar_sync(1, PREP_THREADS);
-        if (pt == 0) mbar_arrive(bar_addr(u, B_FULL + s));
+        __syncwarp();
+
+        // ---- T2^T = X11^T L21^T: t[nt][e] = T2^T[gq + 8 (e >> 1)][8 nt + 2 tq + (e & 1)]
+        float t[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) t[nt][0] = t[nt][1] = t[nt][2] = t[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const int k0 = ks * 8 + tq;
+            const uint32_t a[4] = {__float_as_uint(Xb[k0 * XB + gq]), __float_as_uint(Xb[k0 * XB + gq + 8]),
+                                   __float_as_uint(Xb[(k0 + 4) * XB + gq]), __float_as_uint(Xb[(k0 + 4) * XB + gq + 8])};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {   // B[k][n] = L21[8 nt + n][k]
+                const float* l21 = Lb + LB_21 + nt * 8 + gq;
+                mma_tf32_1688(t[nt], a, __float_as_uint(l21[k0 * LB]), __float_as_uint(l21[(k0 + 4) * LB]));
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(u, B_LFREE));   // L has been read: the prep warps may rewrite it
+
+        // ---- y = T2^T X22^T = (X22 T2)^T = -X21^T: y[nt][e] = y[gq + 8 (e >> 1)][8 nt + 2 tq + (e & 1)]
+        float y[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) y[nt][0] = y[nt][1] = y[nt][2] = y[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+            const uint32_t a[4] = {__float_as_uint(t[ks][0]), __float_as_uint(t[ks][2]), __float_as_uint(t[ks][1]),
+                                   __float_as_uint(t[ks][3])};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {   // B[slot][n]: X22[8 nt + n][8 ks + 2 tq] and [.. + 1]
+                const float2 x2 = *reinterpret_cast<const float2*>(Xb + XB_22 + (nt * 8 + gq) * XB + ks * 8 + 2 * tq);
+                mma_tf32_1688(y[nt], a, __float_as_uint(x2.x), __float_as_uint(x2.y));
+            }
+        }
+        // -B2[16 + rr][cc] = -beta_cc X21[rr][cc] = beta_cc y[cc][rr]
+        const float bl = bs[gq], bh = bs[gq + 8];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int ci = gq + 8 * (e >> 1), rr = 8 * nt + 2 * tq + (e & 1);
+                *reinterpret_cast<uint16_t*>(b2s + core_offset(16 + rr, ci, 32)) = bf16_bits((e >> 1 ? bh : bl) * y[nt][e]);
+            }
+        fence_proxy_async_smem();   // -B2 is read by the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(u, B_FULLD + s));
     }
 }
 
@@ -804,9 +838,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
             mbar_init(bar_addr(u, B_FULLTMA + s), 33);
             mbar_init(bar_addr(u, B_FULLV + s), 1);
             mbar_init(bar_addr(u, B_AREADY + s), 1);
-            mbar_init(bar_addr(u, B_FULL + s), 1);
+            mbar_init(bar_addr(u, B_FULLP + s), 1);
+            mbar_init(bar_addr(u, B_FULLD + s), 1);
         }
-        for (int b = B_G1; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
+        for (int b = B_LFREE; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
         mbar_fence_init();
     }
     if (tid == 32) {
@@ -827,8 +862,10 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
 
     if (warp < W_PREP0) {
         chain_group<kBf16State>(p, maps, u, tid);
-    } else {
+    } else if (warp < W_INV) {
         prep_group(p, u, tid - W_PREP0 * 32);
+    } else {
+        inverse_warp(p, u, tid & 31);
     }
 
     tc_fence_before();
