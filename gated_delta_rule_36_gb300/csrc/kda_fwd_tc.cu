@@ -493,7 +493,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     const float2 gmv = make_float2(gm, gm);
     const float2 gb01 = make_float2(gm * dt.x, gm * dt.y), gb23 = make_float2(gm * dt.z, gm * dt.w);
     const float bcoef = p.lower_bound * LOG2E;          // b
-    const float Cst = 16.f * bcoef;                     // fixed anchor C = 16 b
+    // fixed anchor C = rint(16 b): an integer, so 2^C is exact in bf16 and Q_d = Q_c 2^C,
+    // K_d = K_c 2^C are exact rescalings of the bf16 Q_c, K_c (one packed bf16 multiply);
+    // |G - C| and |C - G| stay <= 126 for every lower_bound >= -5.4585 (G lies in [32 b, 0])
+    const float Cst = rintf(16.f * bcoef);
     const float twoC = ex2_approx(Cst);
     const float2 bcv = make_float2(bcoef, bcoef);
 
@@ -595,7 +598,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     G23[r] = __fadd2_rn(G23[r], off23);
                 }
             }
-            const float2 twoCv = make_float2(twoC, twoC);
+            const __nv_bfloat162 twoC2 = __float2bfloat162_rn(twoC);   // exact: C is an integer
             // rho = 2^(G_T - C) of this thread's channels: K_r = K_i diag(rho) = k 2^(G_T - G)
             const float2 rho01 = make_float2(ex2_approx(T01.x - Cst), ex2_approx(T01.y - Cst));
             const float2 rho23 = make_float2(ex2_approx(T23.x - Cst), ex2_approx(T23.y - Cst));
@@ -612,13 +615,18 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                     const float2 ep23 = make_float2(ex2_approx(G23[r].x), ex2_approx(G23[r].y));
                     const float2 qc01 = __fmul2_rn(__fmul2_rn(bf2_to_f2(qv[r].x), make_float2(qs, qs)), ep01);
                     const float2 qc23 = __fmul2_rn(__fmul2_rn(bf2_to_f2(qv[r].y), make_float2(qs, qs)), ep23);
-                    *reinterpret_cast<uint2*>(qcs + o) = make_uint2(f2_to_bf2(qc01), f2_to_bf2(qc23));
-                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + od) =
-                        make_uint2(f2_to_bf2(__fmul2_rn(qc01, twoCv)), f2_to_bf2(__fmul2_rn(qc23, twoCv)));   // Q_d
+                    uint2 w = make_uint2(f2_to_bf2(qc01), f2_to_bf2(qc23));
+                    *reinterpret_cast<uint2*>(qcs + o) = w;
+                    __nv_bfloat162* hw = reinterpret_cast<__nv_bfloat162*>(&w);
+                    hw[0] = __hmul2(hw[0], twoC2);
+                    hw[1] = __hmul2(hw[1], twoC2);
+                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + od) = w;   // Q_d
                     const float2 kc01 = __fmul2_rn(k01, ep01), kc23 = __fmul2_rn(k23, ep23);
-                    *reinterpret_cast<uint2*>(kcs + o) = make_uint2(f2_to_bf2(kc01), f2_to_bf2(kc23));
-                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + (od + 32 * 128)) =
-                        make_uint2(f2_to_bf2(__fmul2_rn(kc01, twoCv)), f2_to_bf2(__fmul2_rn(kc23, twoCv)));   // K_d
+                    w = make_uint2(f2_to_bf2(kc01), f2_to_bf2(kc23));
+                    *reinterpret_cast<uint2*>(kcs + o) = w;
+                    hw[0] = __hmul2(hw[0], twoC2);
+                    hw[1] = __hmul2(hw[1], twoC2);
+                    *reinterpret_cast<uint2*>(gslot + SL_QDKD + (od + 32 * 128)) = w;   // K_d
                 }
                 {   // 2^(C - G): K_i and K_r = K_i 2^(G_T - C)
                     const float2 em01 = make_float2(ex2_approx(-G01[r].x), ex2_approx(-G01[r].y));
