@@ -125,6 +125,13 @@ __device__ __forceinline__ void ldmatrix_x4_trans_s(uint32_t (&r)[4], uint32_t s
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(saddr));
 }
+// Four 8x8 b16 matrices from fragment registers to shared memory, each stored transposed:
+// memory row k (address from lane 8 j + k for matrix j) receives column k of matrix j.
+__device__ __forceinline__ void stmatrix_x4_trans_s(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};\n" ::"r"(saddr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
 __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], const void* p) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

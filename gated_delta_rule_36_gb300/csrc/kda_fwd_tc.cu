@@ -108,7 +108,7 @@ __host__ __device__ constexpr int l_index(int i, int j) {
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 160, TM_SB = 192, TM_COLS = 256;
 
 struct TmaMaps {
-    CUtensorMap q, k, v, g, out;   // v: boxes of 64 channels with the 128-byte swizzle
+    CUtensorMap q, k, v, g, out;   // v, out: boxes of 64 channels with the 128-byte swizzle
 };
 
 struct Unit {
@@ -408,9 +408,35 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
 
         // O of this chunk -> staging tile [token][v] in the slot's v region (GEMM1 has read
-        // v) -> one tensor store (row copies for a tail chunk); once the store has read the
-        // tile, the region takes chunk c + 2's v
-        {
+        // v) -> tensor stores (row copies for a tail chunk); once the stores have read the
+        // tile, the region takes chunk c + 2's v.  A full chunk's tile has the v boxes'
+        // layout (two [32][64] blocks, 128-byte swizzle): the 16x256b TMEM load gives each
+        // thread two adjacent tokens of one state row, and stmatrix.trans writes 8 tokens x
+        // 8 rows per matrix as 16-byte rows, conflict-free under the swizzle.
+        const bool full = chunk_valid(u, c) == CH;
+        if (full) {
+            const uint32_t tile = slot + SL_V;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {   // lanes 32 w + 16 hf .. + 15
+                const int base = 32 * w + 16 * hf;
+                uint32_t o[16];
+                tmem_ld_16x256b_x4(u.tmem + ((uint32_t)base << 16) + TM_O, o);
+                tmem_wait_ld();
+                // matrix j of a store: (row block lb, token block tb) = (j & 1, 2 st + (j >> 1));
+                // its register: rows base + 8 lb + t / 4, tokens 8 tb + 2 (t % 4) + {0, 1}
+                const int j = lane >> 3, k = lane & 7;
+                const int v0 = base + 8 * (j & 1);
+#pragma unroll
+                for (int st = 0; st < 2; ++st) {
+                    const int tok = 8 * (2 * st + (j >> 1)) + k;
+                    const uint32_t r0 = pack_bf16x2(u2f(o[8 * st + 0]), u2f(o[8 * st + 1]));
+                    const uint32_t r1 = pack_bf16x2(u2f(o[8 * st + 2]), u2f(o[8 * st + 3]));
+                    const uint32_t r2 = pack_bf16x2(u2f(o[8 * st + 4]), u2f(o[8 * st + 5]));
+                    const uint32_t r3 = pack_bf16x2(u2f(o[8 * st + 6]), u2f(o[8 * st + 7]));
+                    stmatrix_x4_trans_s(tile + sw128_offset(tok, v0, 32), r0, r1, r2, r3);
+                }
+            }
+        } else {
             unsigned char* ost = u.gbase + s * SLOT_BYTES + SL_V + 2 * v;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
@@ -435,6 +461,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             const uint32_t ost = slot + SL_V;
             if (nvalid == CH) {
                 tma_store_3d(&maps.out, ost, 0, u.h, (int)t0);
+                tma_store_3d(&maps.out, ost + 4096, 64, u.h, (int)t0);
             } else {
                 for (int i = 0; i < nvalid; ++i)
                     bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
@@ -925,7 +952,7 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
     TmaMaps maps;
     if (!encode_tokens_map(&maps.q, p.q, p.T_total, p.H) || !encode_tokens_map(&maps.k, p.k, p.T_total, p.H) ||
         !encode_tokens_map(&maps.v, p.v, p.T_total, p.H, true) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
-        !encode_tokens_map(&maps.out, p.out, p.T_total, p.H))
+        !encode_tokens_map(&maps.out, p.out, p.T_total, p.H, true))
         return cudaErrorInvalidValue;
     auto kernel = bf16_state ? kda_fwd_tc_kernel<true> : kda_fwd_tc_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
