@@ -43,10 +43,12 @@ namespace {
 constexpr int TC_THREADS = 416;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
 constexpr int W_INV = W_PREP0 + PREP_WARPS;   // the inverse warp: (I + L)^-1 of chunk c while the prep warps take c + 1
-// Single-thread duties of the chain group, spread over its warps (one per SM sub-partition):
-// warp 1 issues the MMAs, warp 2 refills q, k, g and beta, warp 3 stores each output tile
-// and then refills v, whose slot region held the tile.
-constexpr int T_MMA = 32, T_TMA = 64, W_BETA = 2, T_STORE = 96;
+// Duties of the chain group, spread over its warps (one per SM sub-partition): warp 1
+// issues the MMAs, warp 2 refills q, k, g and beta, warp 3 stores each output tile and
+// then refills v, whose slot region held the tile.  With two CTAs on an SM, lane 0 of
+// warp 1 issues alone (the trickle leaves the tensor pipe to the other warps' mma.sync);
+// with one CTA per SM the whole warp issues through elect.sync, which is faster.
+constexpr int W_MMA = 1, T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
@@ -287,7 +289,7 @@ __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b
     mbar_arrive(bar_addr(u, B_FULLTMA + (c & 1)));
 }
 
-template <bool kBf16State>
+template <bool kBf16State, bool kWarpIssue>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
@@ -347,18 +349,23 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
         float beta_next = 0.f;
         if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
-        if (w == 1) {
+        if (w == W_MMA) {
             if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) break;
             tc_fence_after();
-            if (pt == T_MMA) {
+            auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
+            auto av = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024); };
+            auto bv = [&](int kk) { return make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512); };
+            if constexpr (kWarpIssue) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
-                              make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32), idesc1, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) tc_mma_ts_warp(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk)   // P -= V^T: tokens 16 kk .. 16 kk + 15
-                    tc_mma_ss(u.tmem + TM_P, make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024),
-                              make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512), idescv, 1u);
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // P -= V^T
+                tc_commit_warp(bar_addr(u, B_G1));
+            } else if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ss(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // tokens 16 kk ..
                 tc_commit(bar_addr(u, B_G1));
             }
         }
@@ -371,13 +378,18 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
         tc_fence_before();
         named_bar_sync(2, 128);
-        if (pt == T_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
+        if (w == W_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
             tc_fence_after();
+            auto b2 = [&](int kk) { return make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512); };
+            if constexpr (kWarpIssue) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-                tc_mma_ts(u.tmem + TM_P, u.tmem + TM_SB + kk * 8,
-                          make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512), idesc2, kk > 0);
-            tc_commit(bar_addr(u, B_G2));
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ts_warp(u.tmem + TM_P, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
+                tc_commit_warp(bar_addr(u, B_G2));
+            } else if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ts(u.tmem + TM_P, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
+                tc_commit(bar_addr(u, B_G2));
+            }
         }
 
         // U -> bf16 -> TMEM: A operand of GEMM3
@@ -386,16 +398,25 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         p_cols_to_bf16(lane_addr);
         tc_fence_before();
         named_bar_sync(2, 128);
-        if (pt == T_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
+        if (w == W_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
             tc_fence_after();
+            auto br = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_KR + kk * 2048, 4096, 1024); };
+            auto bm = [&](int kk) { return make_sdesc_kmajor_noswizzle(slot + SL_MQT + kk * 256, 128, 512); };
+            if constexpr (kWarpIssue) {
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8,
-                          make_sdesc_mnmajor_sw128(slot + SL_KR + kk * 2048, 4096, 1024), idesc3, 1u);
-                tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8,
-                          make_sdesc_kmajor_noswizzle(slot + SL_MQT + kk * 256, 128, 512), idesc2, 1u);
+                for (int kk = 0; kk < 2; ++kk) {
+                    tc_mma_ts_warp(u.tmem + TM_S, u.tmem + TM_SB + kk * 8, br(kk), idesc3, 1u);
+                    tc_mma_ts_warp(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, bm(kk), idesc2, 1u);
+                }
+                tc_commit_warp(bar_addr(u, B_G3));
+            } else if (lane == 0) {
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8, br(kk), idesc3, 1u);
+                    tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, bm(kk), idesc2, 1u);
+                }
+                tc_commit(bar_addr(u, B_G3));
             }
-            tc_commit(bar_addr(u, B_G3));
         }
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) break;
         tc_fence_after();
@@ -851,7 +872,7 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
     }
 }
 
-template <bool kBf16State>
+template <bool kBf16State, bool kWarpIssue>
 __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
@@ -896,7 +917,7 @@ __global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdPara
     u.tmem = *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR);
 
     if (warp < W_PREP0) {
-        chain_group<kBf16State>(p, maps, u, tid);
+        chain_group<kBf16State, kWarpIssue>(p, maps, u, tid);
     } else if (warp < W_INV) {
         prep_group(p, u, tid - W_PREP0 * 32);
     } else {
@@ -954,7 +975,13 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
         !encode_tokens_map(&maps.v, p.v, p.T_total, p.H, true) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
         !encode_tokens_map(&maps.out, p.out, p.T_total, p.H, true))
         return cudaErrorInvalidValue;
-    auto kernel = bf16_state ? kda_fwd_tc_kernel<true> : kda_fwd_tc_kernel<false>;
+    // one CTA per SM when the units fit the SMs: the chain then issues its MMAs warp-wide
+    // (the bf16-state ablation keeps the single-thread issue)
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 0;
+    auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false>
+                             : (units <= sms ? kda_fwd_tc_kernel<false, true> : kda_fwd_tc_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
