@@ -913,8 +913,10 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
     }
 }
 
+// kWarpIssue: the instantiation for one CTA per SM (warp-wide MMA issue, pipelined state
+// pass, and the register file to itself: up to 128 registers a thread instead of 72).
 template <bool kBf16State, bool kWarpIssue>
-__global__ void __launch_bounds__(TC_THREADS, 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
+__global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
 
