@@ -354,6 +354,9 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         for (int c = 0; c < first; ++c) load_v(maps, u, c);
     if (w == W_BETA)
         for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta(p, u, c, lane));
+    // beta of chunk c + 2 goes into the slot during iteration c; it is loaded an iteration
+    // ahead (its 2-byte loads, 2H bytes apart, miss the caches)
+    float beta_ahead = (w == W_BETA && NSLOT < u.nchunks) ? load_beta(p, u, NSLOT, lane) : 0.f;
     int issued = first;   // chunks whose boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
         const int n = pt >> 2, kb = pt & 3;
@@ -385,8 +388,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
         if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) break;
         // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
-        float beta_next = 0.f;
-        if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
+        const float beta_next = beta_ahead;
+        if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta(p, u, c + NSLOT + 1, lane);
         if (w == W_MMA) {
             if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) break;
             tc_fence_after();
@@ -526,10 +529,6 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                     bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
             }
             bulk_commit();
-            if (refill) {
-                bulk_wait_read_all();
-                load_v(maps, u, c + NSLOT);
-            }
         }
 
         if (c + 1 < u.nchunks) {
@@ -542,6 +541,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             tmem_wait_st();
             tc_fence_before();
             named_bar_sync(2, 128);
+            // the output store has had the copy-and-decay pass to read the staging tile: the
+            // region takes chunk c + 2's v
+            if (pt == T_STORE && refill) {
+                bulk_wait_read_all();
+                load_v(maps, u, c + NSLOT);
+            }
         } else {
 #pragma unroll 1
             for (int piece = 0; piece < 8; ++piece) {
