@@ -340,40 +340,26 @@ def run_ours(args):
 
 
 def run_e2e(kda, inp, w, dev, stream, args):
+    """End to end through the host-buffer entry point kda_fwd_host: pinned host inputs
+    in, forward, output and final state back to pinned host memory, every step."""
     import torch
-    host = {n: getattr(inp, n).detach().cpu().pin_memory() for n in ("q", "k", "v", "g", "beta")}
-    host_small = {n: getattr(inp, n).detach().cpu().pin_memory() for n in ("A_log", "dt_bias")}
+    from gated_delta_rule_36_gb300 import binding as kb
+    host = {n: getattr(inp, n).detach().cpu().pin_memory() for n in ("q", "k", "v", "g", "beta", "A_log", "dt_bias")}
     h_init = inp.initial_state.detach().cpu().pin_memory() if inp.initial_state is not None else None
     h_cu = inp.cu_seqlens.detach().cpu().pin_memory() if inp.cu_seqlens is not None else None
-    d = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
-    ds = {n: torch.empty_like(t, device=dev) for n, t in host_small.items()}
-    d_init = torch.empty_like(h_init, device=dev) if h_init is not None else None
-    d_cu = torch.empty_like(h_cu, device=dev) if h_cu is not None else None
-    d_out = torch.empty_like(d["q"])
-    d_final = torch.empty((w.num_seqs, w.H, w.V, w.K), dtype=w.final_dtype, device=dev)
     h_out = torch.empty_like(host["q"]).pin_memory()
-    h_final = torch.empty(d_final.shape, dtype=d_final.dtype).pin_memory()
-    ws = torch.empty(kda.kda_workspace_size(w.total_tokens, w.H, w.num_seqs), dtype=torch.uint8, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in list(host.values()) + list(host_small.values()))
+    h_final = torch.empty((w.num_seqs, w.H, w.V, w.K), dtype=w.final_dtype).pin_memory()
+    nbytes = kb.kda_fwd_host_device_bytes(host["q"], cu_seqlens=h_cu, initial_state=h_init, final_state=h_final)
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
     h2d += (h_init.numel() * h_init.element_size() if h_init is not None else 0)
     h2d += (h_cu.numel() * h_cu.element_size() if h_cu is not None else 0)
     d2h = h_out.numel() * h_out.element_size() + h_final.numel() * h_final.element_size()
 
     def step():
-        with torch.cuda.stream(stream):
-            for n in host:
-                d[n].copy_(host[n], non_blocking=True)
-            for n in host_small:
-                ds[n].copy_(host_small[n], non_blocking=True)
-            if d_init is not None:
-                d_init.copy_(h_init, non_blocking=True)
-            if d_cu is not None:
-                d_cu.copy_(h_cu, non_blocking=True)
-            kda.kda_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], inp.scale, d_out, ds["A_log"], ds["dt_bias"],
-                        inp.lower_bound, initial_state=d_init, final_state=d_final, cu_seqlens=d_cu,
-                        workspace=ws, stream=stream)
-            h_out.copy_(d_out, non_blocking=True)
-            h_final.copy_(d_final, non_blocking=True)
+        kb.kda_fwd_host(host["q"], host["k"], host["v"], host["g"], host["beta"], inp.scale, h_out, host["A_log"],
+                        host["dt_bias"], inp.lower_bound, initial_state=h_init, final_state=h_final,
+                        cu_seqlens=h_cu, device_buffer=buf, groups=args.e2e_groups, stream=stream)
 
     step()
     torch.cuda.synchronize()
@@ -386,7 +372,8 @@ def run_e2e(kda, inp, w, dev, stream, args):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / n
     return {"value": w.total_tokens / (ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": n}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": n, "groups": args.e2e_groups,
+            "api": "kda_fwd_host"}
 
 
 def main():
@@ -397,6 +384,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-groups", type=int, default=8, help="sequence groups kda_fwd_host pipelines over")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")

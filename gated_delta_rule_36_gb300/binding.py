@@ -23,7 +23,8 @@ HEAD_DIM = 128
 
 # Every function include/kda.h declares.
 EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
-            "kda_read_device_status", "kda_fwd_no_alloc")
+            "kda_read_device_status", "kda_fwd_no_alloc", "kda_fwd_host_device_bytes", "kda_fwd_host",
+            "kda_fwd_host_workspace_offset")
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
 
@@ -74,6 +75,14 @@ def load(path: Optional[str] = None):
         lib.kda_fwd_no_alloc.restype = ctypes.c_int
         lib.kda_fwd_no_alloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
                                          ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+        lib.kda_fwd_host_device_bytes.restype = ctypes.c_size_t
+        lib.kda_fwd_host_device_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                                  ctypes.c_int, ctypes.c_int]
+        lib.kda_fwd_host_workspace_offset.restype = ctypes.c_size_t
+        lib.kda_fwd_host_workspace_offset.argtypes = lib.kda_fwd_host_device_bytes.argtypes
+        lib.kda_fwd_host.restype = ctypes.c_int
+        lib.kda_fwd_host.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
+                                     ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
         if path is None:
             _lib = lib
         return lib
@@ -99,6 +108,70 @@ def _desc(t: Optional[torch.Tensor], name: str):
     for i, s in enumerate(t.shape):
         d.shape[i] = int(s)
     return d
+
+
+def _hdesc(t: Optional[torch.Tensor], name: str):
+    """Descriptor of a host (CPU) tensor for kda_fwd_host."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor")
+    if t.is_cuda:
+        raise ValueError(f"{name}: kda_fwd_host takes host tensors")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.dim() > 4 or t.dtype not in _DTYPE:
+        raise ValueError(f"{name}: unsupported shape or dtype")
+    d = KdaTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else (t.data_ptr() or 16)
+    d.dtype = _DTYPE[t.dtype]
+    d.ndim = t.dim()
+    for i, s in enumerate(t.shape):
+        d.shape[i] = int(s)
+    return d
+
+
+def _state_code(t):
+    return -1 if t is None else _DTYPE[t.dtype]
+
+
+def kda_fwd_host_device_bytes(q, cu_seqlens=None, initial_state=None, final_state=None) -> int:
+    """Device bytes kda_fwd_host needs for these (host) tensors."""
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else 0
+    return int(load().kda_fwd_host_device_bytes(B, T, H, N, _state_code(initial_state), _state_code(final_state)))
+
+
+def kda_fwd_host_workspace_offset(q, cu_seqlens=None, initial_state=None, final_state=None) -> int:
+    B, T, H = q.shape[0], q.shape[1], q.shape[2]
+    N = (cu_seqlens.shape[0] - 1) if cu_seqlens is not None else 0
+    return int(load().kda_fwd_host_workspace_offset(B, T, H, N, _state_code(initial_state),
+                                                    _state_code(final_state)))
+
+
+def kda_fwd_host(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
+                 final_state=None, cu_seqlens=None, device_buffer=None, groups=0, stream=None):
+    """The forward on host tensors (pinned for asynchronous copies): copies in, computes
+    and copies ``out`` / ``final_state`` back, pipelined over groups of sequences.
+    ``device_buffer`` is a uint8 CUDA tensor of at least kda_fwd_host_device_bytes bytes.
+    Returns once the work is enqueued on ``stream`` (torch's current stream by default)."""
+    lib = load()
+    descs = [_hdesc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (out, "out"),
+                                       (A_log, "A_log"), (dt_bias, "dt_bias"), (initial_state, "initial_state"),
+                                       (final_state, "final_state"), (cu_seqlens, "cu_seqlens"))]
+    dq, dk, dv, dg, db, do, da, dd, di, df, dc = descs
+    if device_buffer is None or not (isinstance(device_buffer, torch.Tensor) and device_buffer.is_cuda
+                                     and device_buffer.dtype == torch.uint8):
+        raise ValueError("device_buffer: must be a uint8 CUDA tensor")
+    if stream is None:
+        stream = torch.cuda.current_stream(device_buffer.device)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = lib.kda_fwd_host(_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)),
+                          _ref(do), _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di),
+                          _ref(df), _ref(dc), ctypes.c_void_p(device_buffer.data_ptr()),
+                          ctypes.c_size_t(device_buffer.numel()), ctypes.c_int(int(groups)), ctypes.c_void_p(sh))
+    _check(lib, st)
+    return device_buffer
 
 
 def _ref(d):

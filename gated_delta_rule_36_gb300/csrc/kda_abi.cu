@@ -99,6 +99,19 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
                    const kda_tensor* final_state, const kda_tensor* cu_seqlens,
                    void* workspace, size_t workspace_bytes, kda_stream_t stream) {
     g_last_error[0] = '\0';
+    return kda::fwd_device(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
+                           cu_seqlens, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true, true);
+}
+
+}  // extern "C"
+
+// The body of kda_fwd: every host-side check, then (with `enqueue`) the status reset
+// (with `reset_status`), the schedule and the forward on `s`.
+kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
+                           const kda_tensor* beta, float scale, const kda_tensor* out, const kda_tensor* A_log,
+                           const kda_tensor* dt_bias, float lower_bound, const kda_tensor* initial_state,
+                           const kda_tensor* final_state, const kda_tensor* cu_seqlens, void* workspace,
+                           size_t workspace_bytes, cudaStream_t s, bool reset_status, bool enqueue) {
     if (!present(q)) return fail(KDA_ERR_INVALID_ARG, "q: missing");
     if (q->ndim != 4) return fail(KDA_ERR_INVALID_ARG, "q: ndim %d, expected 4 [B,T,H,128]", q->ndim);
     const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2];
@@ -157,11 +170,11 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     if (workspace_bytes < need)
         return fail(KDA_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
 
+    if (!enqueue) return KDA_OK;
     uint32_t* status = static_cast<uint32_t*>(workspace);
     int32_t* order = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + kHeaderBytes);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), s);
+    cudaError_t e = reset_status ? cudaMemsetAsync(status, 0, sizeof(uint32_t), s) : cudaSuccess;
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "status reset: %s", cudaGetErrorString(e));
     if (packed) {
         e = kda::launch_schedule(static_cast<const int64_t*>(cu_seqlens->data), (int)nseq, B * T, order, status, s);
@@ -209,6 +222,8 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }
+
+extern "C" {
 
 kda_status kda_read_device_status(const void* workspace, kda_stream_t stream, uint32_t* bits) {
     if (workspace == nullptr || bits == nullptr) return fail(KDA_ERR_INVALID_ARG, "null argument");

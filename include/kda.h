@@ -160,6 +160,47 @@ kda_status kda_fwd_no_alloc(const kda_tensor* q, const kda_tensor* k, const kda_
                             const kda_tensor* final_state, const kda_tensor* cu_seqlens,
                             kda_stream_t stream, const void** workspace_used);
 
+/*
+ * Device bytes kda_fwd_host needs for a request: q/k/v/g/out [B, T, H, 128], beta, A_log,
+ * dt_bias, the states (init_dtype / final_dtype: KDA_BF16, KDA_F32, or -1 when absent),
+ * N = number of cu_seqlens intervals (0 for batched mode), and the workspace.  Returns
+ * 0 for invalid arguments.
+ */
+size_t kda_fwd_host_device_bytes(int64_t B, int64_t T, int H, int64_t N, int init_dtype, int final_dtype);
+
+/*
+ * kda_fwd on HOST buffers: every tensor descriptor (q ... cu_seqlens) points to host
+ * memory, with the shapes, dtypes and meaning of kda_fwd.  The call copies the inputs to
+ * `device_buffer` (>= kda_fwd_host_device_bytes bytes, 256-byte aligned, owned by the
+ * caller and holding nothing the caller needs), runs the forward, and copies `out` and
+ * `final_state` back.  It splits the sequences into up to `groups` consecutive groups of
+ * about equal token counts (groups <= 0: 8) and pipelines them over three streams: the
+ * host-to-device copies of group j + 1 run while group j computes and its results are
+ * copied back.  The work is ordered after everything already on `stream` and `stream`
+ * is ordered after all of it; the call itself returns once the work is enqueued, so the
+ * host buffers must stay untouched until `stream` reaches that point.  Host buffers should
+ * be page-locked (cudaHostAlloc / pinned): pageable ones work but are copied synchronously.
+ * Output rows of tokens that belong to no sequence are not written, as with kda_fwd.
+ * initial_state and final_state may be the same host buffer (in place).
+ *
+ * Errors: the checks of kda_fwd, plus cu_seqlens validated on the host (cu[0] == 0,
+ * non-decreasing, cu[N] <= B*T: KDA_ERR_INVALID_ARG) and a missing or too small
+ * device_buffer (KDA_ERR_WORKSPACE); all before anything is enqueued.  Device-side status
+ * bits go to the workspace inside device_buffer: read them with kda_read_device_status on
+ * (char*)device_buffer + kda_fwd_host_workspace_offset(...).  Not capturable in a CUDA
+ * graph (the per-group cu_seqlens are staged from pageable memory).
+ */
+kda_status kda_fwd_host(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                        const kda_tensor* g, const kda_tensor* beta, float scale,
+                        const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                        float lower_bound, const kda_tensor* initial_state,
+                        const kda_tensor* final_state, const kda_tensor* cu_seqlens,
+                        void* device_buffer, size_t device_bytes, int groups, kda_stream_t stream);
+
+/* Byte offset of the workspace (and so of the device status word) inside the
+ * device_buffer of a kda_fwd_host call with these arguments; 0 for invalid ones. */
+size_t kda_fwd_host_workspace_offset(int64_t B, int64_t T, int H, int64_t N, int init_dtype, int final_dtype);
+
 #ifdef __cplusplus
 }
 #endif

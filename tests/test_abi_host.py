@@ -122,3 +122,40 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         kb.kda_fwd(x, x, x, x, torch.zeros(1, 4, 1, dtype=torch.bfloat16), 1.0, x.clone(),
                    torch.zeros(1), torch.zeros(1, 128), -5.0, workspace=torch.zeros(512, dtype=torch.uint8))
+
+
+def test_host_entry_device_bytes(lib):
+    tok = 64 * 2 * 128 * 2
+    n = lib.kda_fwd_host_device_bytes(1, 64, 2, 0, -1, -1)
+    assert n >= 5 * tok and n % 256 == 0
+    assert lib.kda_fwd_host_device_bytes(1, 64, 2, 3, kb.KDA_F32, kb.KDA_F32) >= n + 2 * 3 * 2 * 128 * 128 * 4
+    assert lib.kda_fwd_host_device_bytes(-1, 64, 2, 0, -1, -1) == 0
+    off = lib.kda_fwd_host_workspace_offset(1, 64, 2, 0, -1, -1)
+    assert 5 * tok <= off < n and off % 256 == 0
+
+
+def test_host_entry_rejects_before_enqueueing(lib):
+    """Host-side checks of kda_fwd_host return before any CUDA call: the tensors are host
+    descriptors (only cu_seqlens is read, from real host memory) and the device buffer a
+    fake aligned address."""
+    import numpy as np
+    H, Tn = 2, 64
+    host = BASE  # never dereferenced except cu_seqlens below
+
+    def run(cu_vals=None, dev=BASE + 0x10000000, nbytes=1 << 40, lb=-5.0):
+        cu_arr = None if cu_vals is None else np.asarray(cu_vals, dtype=np.int64)
+        cu = None if cu_arr is None else T(kb.KDA_I64, (len(cu_vals),), cu_arr.ctypes.data)
+        d = lambda dt, shape: T(dt, shape, host)
+        r = lambda x: None if x is None else ctypes.byref(x)
+        q = d(kb.KDA_BF16, (1, Tn, H, 128))
+        return lib.kda_fwd_host(r(q), r(q), r(q), r(q), r(d(kb.KDA_BF16, (1, Tn, H))), ctypes.c_float(0.1), r(q),
+                                r(d(kb.KDA_F32, (H,))), r(d(kb.KDA_F32, (H, 128))), ctypes.c_float(lb), None,
+                                None, r(cu), ctypes.c_void_p(dev), ctypes.c_size_t(nbytes), 4, ctypes.c_void_p(0))
+
+    assert run(cu_vals=[1, 10, 64]) == kb.KDA_ERR_INVALID_ARG        # cu_seqlens[0] != 0
+    assert run(cu_vals=[0, 40, 30]) == kb.KDA_ERR_INVALID_ARG        # decreasing
+    assert run(cu_vals=[0, 40, 65]) == kb.KDA_ERR_INVALID_ARG        # past the tokens
+    assert run(nbytes=1024) == kb.KDA_ERR_WORKSPACE                  # device buffer too small
+    assert run(dev=BASE + 0x10000000 + 16) == kb.KDA_ERR_WORKSPACE   # misaligned
+    assert run(lb=-6.0) == kb.KDA_ERR_UNSUPPORTED                    # the checks of kda_fwd
+    assert lib.kda_last_error()
