@@ -24,7 +24,7 @@ HEAD_DIM = 128
 # Every function include/kda.h declares.
 EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
             "kda_read_device_status", "kda_fwd_no_alloc", "kda_fwd_host_device_bytes", "kda_fwd_host",
-            "kda_fwd_host_workspace_offset")
+            "kda_fwd_host_workspace_offset", "kda_decode")
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
 
@@ -75,6 +75,8 @@ def load(path: Optional[str] = None):
         lib.kda_fwd_no_alloc.restype = ctypes.c_int
         lib.kda_fwd_no_alloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
                                          ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+        lib.kda_decode.restype = ctypes.c_int
+        lib.kda_decode.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, ctypes.c_void_p]
         lib.kda_fwd_host_device_bytes.restype = ctypes.c_size_t
         lib.kda_fwd_host_device_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
                                                   ctypes.c_int, ctypes.c_int]
@@ -216,6 +218,24 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
                      ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(sh))
     _check(lib, st)
     return workspace
+
+
+def kda_decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None, final_state=None,
+               stream=None):
+    """One decode step (one token per sequence) through the C ABI: q, k, v, g, out
+    [B, H, 128], beta [B, H], states [B, H, 128, 128]; final_state may be initial_state
+    itself for the in-place update."""
+    lib = load()
+    descs = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (out, "out"),
+                                      (A_log, "A_log"), (dt_bias, "dt_bias"), (initial_state, "initial_state"),
+                                      (final_state, "final_state"))]
+    dq, dk, dv, dg, db, do, da, dd, di, df = descs
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    st = lib.kda_decode(_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)), _ref(do),
+                        _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di), _ref(df), ctypes.c_void_p(sh))
+    _check(lib, st)
 
 
 def kda_read_device_status(workspace, stream=None) -> int:

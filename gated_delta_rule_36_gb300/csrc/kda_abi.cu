@@ -133,7 +133,7 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
     const int64_t ashape[1] = {H};
     if ((st = check_tensor("A_log", A_log, KDA_F32, 1, ashape, 4)) != KDA_OK) return st;
     const int64_t dshape[2] = {H, KDA_HEAD_DIM};
-    if ((st = check_tensor("dt_bias", dt_bias, KDA_F32, 2, dshape, 4)) != KDA_OK) return st;
+    if ((st = check_tensor("dt_bias", dt_bias, KDA_F32, 2, dshape, 16)) != KDA_OK) return st;
     if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
     if (!isfinite(lower_bound) || lower_bound > 0.f)
         return fail(KDA_ERR_INVALID_ARG, "lower_bound must be finite and <= 0");
@@ -224,6 +224,69 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
 }
 
 extern "C" {
+
+kda_status kda_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
+                      const kda_tensor* beta, float scale, const kda_tensor* out, const kda_tensor* A_log,
+                      const kda_tensor* dt_bias, float lower_bound, const kda_tensor* initial_state,
+                      const kda_tensor* final_state, kda_stream_t stream) {
+    g_last_error[0] = '\0';
+    if (!present(q)) return fail(KDA_ERR_INVALID_ARG, "q: missing");
+    if (q->ndim != 3) return fail(KDA_ERR_INVALID_ARG, "q: ndim %d, expected 3 [B,H,128]", q->ndim);
+    const int64_t B = q->shape[0], H = q->shape[1];
+    if (q->shape[2] != KDA_HEAD_DIM)
+        return fail(KDA_ERR_UNSUPPORTED, "head dim %lld: only %d is built", (long long)q->shape[2], KDA_HEAD_DIM);
+    if (B < 0 || H < 1) return fail(KDA_ERR_INVALID_ARG, "bad q shape [%lld,%lld,128]", (long long)B, (long long)H);
+    if (B * H > (int64_t)INT32_MAX / 4) return fail(KDA_ERR_UNSUPPORTED, "B*H too large");
+    const int64_t tshape[3] = {B, H, KDA_HEAD_DIM};
+    kda_status st;
+    if ((st = check_tensor("q", q, KDA_BF16, 3, tshape, 16)) != KDA_OK) return st;
+    if ((st = check_tensor("k", k, KDA_BF16, 3, tshape, 16)) != KDA_OK) return st;
+    if ((st = check_tensor("v", v, KDA_BF16, 3, tshape, 16)) != KDA_OK) return st;
+    if ((st = check_tensor("g", g, KDA_BF16, 3, tshape, 16)) != KDA_OK) return st;
+    if ((st = check_tensor("out", out, KDA_BF16, 3, tshape, 16)) != KDA_OK) return st;
+    const int64_t bshape[2] = {B, H};
+    if ((st = check_tensor("beta", beta, KDA_BF16, 2, bshape, 2)) != KDA_OK) return st;
+    const int64_t ashape[1] = {H};
+    if ((st = check_tensor("A_log", A_log, KDA_F32, 1, ashape, 4)) != KDA_OK) return st;
+    const int64_t dshape[2] = {H, KDA_HEAD_DIM};
+    if ((st = check_tensor("dt_bias", dt_bias, KDA_F32, 2, dshape, 16)) != KDA_OK) return st;
+    if (!isfinite(scale)) return fail(KDA_ERR_INVALID_ARG, "scale must be finite");
+    if (!isfinite(lower_bound) || lower_bound > 0.f)
+        return fail(KDA_ERR_INVALID_ARG, "lower_bound must be finite and <= 0");
+    if ((st = check_state("initial_state", initial_state, B, H)) != KDA_OK) return st;
+    if ((st = check_state("final_state", final_state, B, H)) != KDA_OK) return st;
+    if (present(initial_state) && present(final_state)) {
+        const uintptr_t a0 = (uintptr_t)initial_state->data;
+        const uintptr_t a1 = a0 + numel(initial_state) * elem_size(initial_state->dtype);
+        const uintptr_t b0 = (uintptr_t)final_state->data;
+        const uintptr_t b1 = b0 + numel(final_state) * elem_size(final_state->dtype);
+        if (a0 < b1 && b0 < a1 && !(a0 == b0 && initial_state->dtype == final_state->dtype))
+            return fail(KDA_ERR_ALIAS, "initial_state and final_state overlap but are not the same buffer and dtype");
+    }
+    kda::FwdParams p;
+    memset(&p, 0, sizeof(p));
+    p.q = static_cast<const __nv_bfloat16*>(q->data);
+    p.k = static_cast<const __nv_bfloat16*>(k->data);
+    p.v = static_cast<const __nv_bfloat16*>(v->data);
+    p.g = static_cast<const __nv_bfloat16*>(g->data);
+    p.beta = static_cast<const __nv_bfloat16*>(beta->data);
+    p.out = static_cast<__nv_bfloat16*>(out->data);
+    p.A_log = static_cast<const float*>(A_log->data);
+    p.dt_bias = static_cast<const float*>(dt_bias->data);
+    p.init_state = present(initial_state) ? initial_state->data : nullptr;
+    p.init_f32 = present(initial_state) && initial_state->dtype == KDA_F32;
+    p.final_state = present(final_state) ? final_state->data : nullptr;
+    p.final_f32 = present(final_state) && final_state->dtype == KDA_F32;
+    p.T = 1;
+    p.T_total = B;
+    p.H = (int)H;
+    p.nseq = (int)B;
+    p.scale = scale;
+    p.lower_bound = lower_bound;
+    const cudaError_t e = kda::launch_decode(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return KDA_OK;
+}
 
 kda_status kda_read_device_status(const void* workspace, kda_stream_t stream, uint32_t* bits) {
     if (workspace == nullptr || bits == nullptr) return fail(KDA_ERR_INVALID_ARG, "null argument");

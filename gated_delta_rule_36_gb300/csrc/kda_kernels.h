@@ -31,6 +31,9 @@ size_t fwd_tc_smem_bytes();
 // The same with 16-token chunks and no exponent anchor: the chunk-size ablation.
 cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t stream);
 
+// Single-token decode step (T = 1 per sequence, batched layout [B, H, 128]).
+cudaError_t launch_decode(const FwdParams& p, cudaStream_t stream);
+
 }  // namespace kda
 
 namespace kda {

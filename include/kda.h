@@ -161,6 +161,31 @@ kda_status kda_fwd_no_alloc(const kda_tensor* q, const kda_tensor* k, const kda_
                             kda_stream_t stream, const void** workspace_used);
 
 /*
+ * One decode step: every sequence takes one token, in the order of the recurrence of
+ * kda_fwd (decay the state by exp(lambda) per key channel, delta-rule correction with the
+ * normalised key, read-out of the written state with the normalised, scaled query).
+ * The result equals kda_fwd with T = 1 in batched mode; the kernel is a separate one, a
+ * single pass over each state row (the step is bound by the state's HBM traffic).
+ *
+ *   q, k, g, v, out  bf16 [B, H, 128]     one token per sequence
+ *   beta             bf16 [B, H]          used as given
+ *   scale, A_log, dt_bias, lower_bound    as for kda_fwd (lower_bound only needs to be
+ *                                         finite and <= 0: no chunk operands to keep in range)
+ *   initial_state    NULL/absent (zero) or bf16/fp32 [B, H, 128, 128]
+ *   final_state      NULL/absent or bf16/fp32 [B, H, 128, 128]; may be exactly the same
+ *                    allocation as initial_state (the usual in-place decode update)
+ *   stream           stream the work is enqueued on
+ *
+ * No workspace and no device-side error: every check is made on the host before the
+ * launch (KDA_ERR_INVALID_ARG / UNSUPPORTED / ALIAS / CUDA as for kda_fwd).
+ */
+kda_status kda_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                      const kda_tensor* g, const kda_tensor* beta, float scale,
+                      const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                      float lower_bound, const kda_tensor* initial_state,
+                      const kda_tensor* final_state, kda_stream_t stream);
+
+/*
  * Device bytes kda_fwd_host needs for a request: q/k/v/g/out [B, T, H, 128], beta, A_log,
  * dt_bias, the states (init_dtype / final_dtype: KDA_BF16, KDA_F32, or -1 when absent),
  * N = number of cu_seqlens intervals (0 for batched mode), and the workspace.  Returns

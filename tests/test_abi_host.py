@@ -159,3 +159,34 @@ def test_host_entry_rejects_before_enqueueing(lib):
     assert run(dev=BASE + 0x10000000 + 16) == kb.KDA_ERR_WORKSPACE   # misaligned
     assert run(lb=-6.0) == kb.KDA_ERR_UNSUPPORTED                    # the checks of kda_fwd
     assert lib.kda_last_error()
+
+
+def test_decode_rejects_before_enqueueing(lib):
+    B, H = 2, 3
+    t = lambda shape, dt=kb.KDA_BF16, off=0: T(dt, shape, BASE + off)
+
+    def call_dec(**over):
+        a = dict(q=t((B, H, 128)), k=t((B, H, 128), off=0x100000), v=t((B, H, 128), off=0x200000),
+                 g=t((B, H, 128), off=0x300000), beta=t((B, H), off=0x400000), out=t((B, H, 128), off=0x500000),
+                 A_log=t((H,), kb.KDA_F32, 0x600000), dt_bias=t((H, 128), kb.KDA_F32, 0x700000), lb=-5.0,
+                 init=None, final=None)
+        a.update(over)
+        r = lambda d: None if d is None else ctypes.byref(d)
+        return lib.kda_decode(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]), ctypes.c_float(0.1),
+                              r(a["out"]), r(a["A_log"]), r(a["dt_bias"]), ctypes.c_float(a["lb"]), r(a["init"]),
+                              r(a["final"]), ctypes.c_void_p(0))
+
+    st4 = lambda dt, off: t((B, H, 128, 128), dt, 0x800000 + off)
+    cases = [
+        (dict(q=t((B, H, 128, 1))), kb.KDA_ERR_INVALID_ARG),
+        (dict(q=t((B, H, 64))), kb.KDA_ERR_UNSUPPORTED),
+        (dict(k=t((B, H + 1, 128), off=0x100000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(beta=t((B, H, 1), off=0x400000)), kb.KDA_ERR_INVALID_ARG),
+        (dict(dt_bias=t((H, 128), kb.KDA_F32, 0x700000 + 4)), kb.KDA_ERR_INVALID_ARG),
+        (dict(lb=0.5), kb.KDA_ERR_INVALID_ARG),
+        (dict(init=st4(kb.KDA_F32, 0), final=st4(kb.KDA_F32, 4096)), kb.KDA_ERR_ALIAS),
+        (dict(init=t((B, H, 128, 64), kb.KDA_F32, 0x800000)), kb.KDA_ERR_INVALID_ARG),
+    ]
+    for over, expect in cases:
+        got = call_dec(**over)
+        assert got == expect, (over, got, lib.kda_last_error())
