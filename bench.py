@@ -376,6 +376,52 @@ def run_e2e(kda, inp, w, dev, stream, args):
             "api": "kda_fwd_host"}
 
 
+def run_decode(args):
+    """The single-token decode step (kda_decode), one line of its own: B sequences x H heads,
+    each step one token per sequence with the fp32 state updated in place (268 MB at
+    B = H = 64, larger than L2, so no flush).  Bound by the state's HBM traffic."""
+    import torch
+    import gated_delta_rule_36_gb300 as kda
+    B, H = args.decode_batch, args.decode_heads
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    kda.load()
+    gen = torch.Generator(device=dev).manual_seed(7)
+    bf = lambda *s: torch.randn(*s, generator=gen, device=dev).to(torch.bfloat16)
+    q, k, v, g = bf(B, H, 128), bf(B, H, 128), bf(B, H, 128), bf(B, H, 128)
+    beta = torch.rand(B, H, generator=gen, device=dev).to(torch.bfloat16)
+    A_log = torch.rand(H, generator=gen, device=dev)
+    dt_bias = torch.rand(H, 128, generator=gen, device=dev)
+    state = 0.1 * torch.randn(B, H, 128, 128, generator=gen, device=dev)
+    out = torch.empty(B, H, 128, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: kda.kda_decode(q, k, v, g, beta, 128 ** -0.5, out, A_log, dt_bias, -5.0,
+                                  initial_state=state, final_state=state, stream=stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    alg = B * H * (2 * 128 * 128 * 4 + 4 * 128 * 2 + 128 * 2 + 2)   # state in + out, q k v g, out, beta
+    hbm_peak, _, _, peak_src = load_peaks()
+    gbs = alg / (ms / 1000.0) / 1e9
+    print(json.dumps({
+        "metric": "KDA decode tokens/s (one token per sequence per step)", "value": B / (ms / 1000.0),
+        "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": "bf16 inputs, fp32 state", "data": "synthetic",
+        "config": {"workload": f"decode B={B} H={H}", "state": "fp32, in place", "l2": "state larger than L2"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s", "frac": gbs / hbm_peak,
+                     "peak_source": peak_src, "algorithmic_bytes": alg},
+        "clocks": clk.summary(), "gpu_launches": args.steps}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -391,9 +437,14 @@ def main():
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) of one launch of the forward kernel; by default the "
                          "committed record in profiles/, used only while the kernel sources match it")
+    ap.add_argument("--decode", action="store_true", help="time the single-token decode step instead")
+    ap.add_argument("--decode-batch", type=int, default=64)
+    ap.add_argument("--decode-heads", type=int, default=64)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
-    if args.impl == "reference":
+    if args.decode:
+        run_decode(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)
