@@ -24,7 +24,8 @@ HEAD_DIM = 128
 # Every function include/kda.h declares.
 EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
             "kda_read_device_status", "kda_fwd_no_alloc", "kda_fwd_host_device_bytes", "kda_fwd_host",
-            "kda_fwd_host_workspace_offset", "kda_decode")
+            "kda_fwd_host_workspace_offset", "kda_decode", "kda_fwd_ex", "kda_decode_ex")
+KDA_FLAG_BETA_LOGIT, KDA_FLAG_GATE_SOFTPLUS = 0x1, 0x2
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
 
@@ -75,6 +76,12 @@ def load(path: Optional[str] = None):
         lib.kda_fwd_no_alloc.restype = ctypes.c_int
         lib.kda_fwd_no_alloc.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
                                          ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+        lib.kda_fwd_ex.restype = ctypes.c_int
+        lib.kda_fwd_ex.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, T,
+                                   ctypes.c_void_p, ctypes.c_size_t, ctypes.c_uint32, ctypes.c_void_p]
+        lib.kda_decode_ex.restype = ctypes.c_int
+        lib.kda_decode_ex.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T,
+                                      ctypes.c_uint32, ctypes.c_void_p]
         lib.kda_decode.restype = ctypes.c_int
         lib.kda_decode.argtypes = [T, T, T, T, T, ctypes.c_float, T, T, T, ctypes.c_float, T, T, ctypes.c_void_p]
         lib.kda_fwd_host_device_bytes.restype = ctypes.c_size_t
@@ -191,12 +198,13 @@ def kda_workspace_size(T_total: int, H: int, N: int) -> int:
 
 
 def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None,
-            final_state=None, cu_seqlens=None, workspace=None, stream=None):
+            final_state=None, cu_seqlens=None, workspace=None, stream=None, flags=0):
     """Run the forward through the C ABI.  Tensors as in ``include/kda.h``.
 
     ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted;
-    ``stream`` defaults to torch's current stream of q's device.  Returns the
-    workspace (its first word is the device status).
+    ``stream`` defaults to torch's current stream of q's device; ``flags`` (KDA_FLAG_*)
+    selects the interface variants through kda_fwd_ex.  Returns the workspace (its
+    first word is the device status).
     """
     lib = load()
     descs = [_desc(t, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (g, "g"), (beta, "beta"), (out, "out"),
@@ -212,16 +220,19 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    st = lib.kda_fwd(_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)),
-                     _ref(do), _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di),
-                     _ref(df), _ref(dc), ctypes.c_void_p(workspace.data_ptr()),
-                     ctypes.c_size_t(workspace.numel()), ctypes.c_void_p(sh))
+    args = (_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)),
+            _ref(do), _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di),
+            _ref(df), _ref(dc), ctypes.c_void_p(workspace.data_ptr()), ctypes.c_size_t(workspace.numel()))
+    if flags:
+        st = lib.kda_fwd_ex(*args, ctypes.c_uint32(int(flags)), ctypes.c_void_p(sh))
+    else:
+        st = lib.kda_fwd(*args, ctypes.c_void_p(sh))
     _check(lib, st)
     return workspace
 
 
 def kda_decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state=None, final_state=None,
-               stream=None):
+               stream=None, flags=0):
     """One decode step (one token per sequence) through the C ABI: q, k, v, g, out
     [B, H, 128], beta [B, H], states [B, H, 128, 128]; final_state may be initial_state
     itself for the in-place update."""
@@ -233,8 +244,12 @@ def kda_decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initia
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
     sh = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
-    st = lib.kda_decode(_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)), _ref(do),
-                        _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di), _ref(df), ctypes.c_void_p(sh))
+    args = (_ref(dq), _ref(dk), _ref(dv), _ref(dg), _ref(db), ctypes.c_float(float(scale)), _ref(do),
+            _ref(da), _ref(dd), ctypes.c_float(float(lower_bound)), _ref(di), _ref(df))
+    if flags:
+        st = lib.kda_decode_ex(*args, ctypes.c_uint32(int(flags)), ctypes.c_void_p(sh))
+    else:
+        st = lib.kda_decode(*args, ctypes.c_void_p(sh))
     _check(lib, st)
 
 

@@ -100,7 +100,20 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
                    void* workspace, size_t workspace_bytes, kda_stream_t stream) {
     g_last_error[0] = '\0';
     return kda::fwd_device(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
-                           cu_seqlens, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true, true);
+                           cu_seqlens, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true, true,
+                           0u);
+}
+
+kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                      const kda_tensor* g, const kda_tensor* beta, float scale,
+                      const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                      float lower_bound, const kda_tensor* initial_state,
+                      const kda_tensor* final_state, const kda_tensor* cu_seqlens,
+                      void* workspace, size_t workspace_bytes, uint32_t flags, kda_stream_t stream) {
+    g_last_error[0] = '\0';
+    return kda::fwd_device(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state,
+                           cu_seqlens, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream), true, true,
+                           flags);
 }
 
 }  // extern "C"
@@ -111,7 +124,10 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
                            const kda_tensor* beta, float scale, const kda_tensor* out, const kda_tensor* A_log,
                            const kda_tensor* dt_bias, float lower_bound, const kda_tensor* initial_state,
                            const kda_tensor* final_state, const kda_tensor* cu_seqlens, void* workspace,
-                           size_t workspace_bytes, cudaStream_t s, bool reset_status, bool enqueue) {
+                           size_t workspace_bytes, cudaStream_t s, bool reset_status, bool enqueue,
+                           uint32_t flags) {
+    if (flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
+        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x", flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
     if (!present(q)) return fail(KDA_ERR_INVALID_ARG, "q: missing");
     if (q->ndim != 4) return fail(KDA_ERR_INVALID_ARG, "q: ndim %d, expected 4 [B,T,H,128]", q->ndim);
     const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2];
@@ -204,6 +220,7 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
     p.nseq = (int)nseq;
     p.scale = scale;
     p.lower_bound = lower_bound;
+    p.flags = flags;
 
     // KDA_FWD_KERNEL selects an ablation variant: "mma" keeps the state in mma.sync
     // registers, "tc16" uses 16-token chunks without the exponent anchor, "tcbf16" rounds
@@ -216,6 +233,8 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
         if (v != nullptr && strcmp(v, "tcbf16") == 0) return 3;
         return 0;
     }();
+    if (variant != 0 && flags != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "the ablation kernel chosen with KDA_FWD_KERNEL takes no interface flags");
     e = variant == 1   ? kda::launch_fwd_mma(p, s)
         : variant == 2 ? kda::launch_fwd_tc16(p, s)
                        : kda::launch_fwd_tc(p, s, variant == 3);
@@ -229,7 +248,17 @@ kda_status kda_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor
                       const kda_tensor* beta, float scale, const kda_tensor* out, const kda_tensor* A_log,
                       const kda_tensor* dt_bias, float lower_bound, const kda_tensor* initial_state,
                       const kda_tensor* final_state, kda_stream_t stream) {
+    return kda_decode_ex(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_state, final_state, 0u,
+                         stream);
+}
+
+kda_status kda_decode_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
+                         const kda_tensor* beta, float scale, const kda_tensor* out, const kda_tensor* A_log,
+                         const kda_tensor* dt_bias, float lower_bound, const kda_tensor* initial_state,
+                         const kda_tensor* final_state, uint32_t flags, kda_stream_t stream) {
     g_last_error[0] = '\0';
+    if (flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
+        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits");
     if (!present(q)) return fail(KDA_ERR_INVALID_ARG, "q: missing");
     if (q->ndim != 3) return fail(KDA_ERR_INVALID_ARG, "q: ndim %d, expected 3 [B,H,128]", q->ndim);
     const int64_t B = q->shape[0], H = q->shape[1];
@@ -277,6 +306,7 @@ kda_status kda_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor
     p.init_f32 = present(initial_state) && initial_state->dtype == KDA_F32;
     p.final_state = present(final_state) ? final_state->data : nullptr;
     p.final_f32 = present(final_state) && final_state->dtype == KDA_F32;
+    p.flags = flags;
     p.T = 1;
     p.T_total = B;
     p.H = (int)H;

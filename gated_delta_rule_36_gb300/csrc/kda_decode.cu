@@ -49,18 +49,25 @@ __global__ void __launch_bounds__(DEC_THREADS) kda_decode_kernel(const FwdParams
     const float kh[4] = {k4.x * rk, k4.y * rk, k4.z * rk, k4.w * rk};
     const float qh[4] = {q4.x * rq, q4.y * rq, q4.z * rq, q4.w * rq};
     const float kq = warp_sum(kh[0] * qh[0] + kh[1] * qh[1] + kh[2] * qh[2] + kh[3] * qh[3]);
-    // lambda = lower_bound sigmoid(exp(A_log) (g + dt_bias)); base 2: D = 2^(lambda log2 e)
-    const float gm = -expf(p.A_log[h]) * LOG2E;
+    // lambda = lower_bound sigmoid(exp(A_log) (g + dt_bias)), or with KDA_FLAG_GATE_SOFTPLUS
+    // max(-exp(A_log) softplus(g + dt_bias), lower_bound); base 2: D = 2^(lambda log2 e)
+    const float eA = expf(p.A_log[h]);
+    const float gm = -eA * LOG2E;
     const float bcoef = p.lower_bound * LOG2E;
+    const bool softplus = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
     const float gx[4] = {g4.x + dt.x, g4.y + dt.y, g4.z + dt.z, g4.w + dt.w};
     float D[4], dk[4], dq[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        D[j] = ex2_approx(bcoef * rcp_approx(1.f + ex2_approx(gm * gx[j])));
+        const float lam2 = softplus
+            ? fmaxf(-eA * fmaf(fmaxf(gx[j], 0.f), LOG2E, lg2_approx(1.f + ex2_approx(-fabsf(gx[j]) * LOG2E))), bcoef)
+            : bcoef * rcp_approx(1.f + ex2_approx(gm * gx[j]));
+        D[j] = ex2_approx(lam2);
         dk[j] = D[j] * kh[j];
         dq[j] = D[j] * qh[j];
     }
-    const float beta = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[unit]);
+    float beta = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[unit]);
+    if (p.flags & KDA_FLAG_BETA_LOGIT) beta = rcp_approx(1.f + ex2_approx(-beta * LOG2E));
     const int r0 = rb * DEC_ROWS_PER_CTA + warp * DEC_ROWS_PER_WARP;
     const float vr = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.v)[tok + r0 + (lane & 7)]);
 

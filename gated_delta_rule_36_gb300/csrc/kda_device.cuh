@@ -39,6 +39,7 @@ struct FwdParams {
     int final_f32;
     float scale;
     float lower_bound;
+    uint32_t flags;           // KDA_FLAG_* interface variants
 };
 
 // Token range [bos, eos) of sequence n, clamped to [0, T_total].
@@ -52,6 +53,12 @@ __device__ __forceinline__ void seq_range(const FwdParams& p, int n, int64_t& bo
     }
     bos = bos < 0 ? 0 : (bos > p.T_total ? p.T_total : bos);
     eos = eos < bos ? bos : (eos > p.T_total ? p.T_total : eos);
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

@@ -314,12 +314,14 @@ __device__ __forceinline__ void prefetch_chunk(const TmaMaps& maps, const Unit& 
 }
 
 // beta of token `lane` of chunk c (0 past the end), by a plain load: its token stride
-// is 2H bytes, too narrow for a tensor box when H is small.
+// is 2H bytes, too narrow for a tensor box when H is small.  With KDA_FLAG_BETA_LOGIT the
+// stored value is a logit and beta = sigmoid(logit).
 __device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, int c, int lane) {
     const int64_t t0 = u.bos + (int64_t)c * CH;
-    return lane < chunk_valid(u, c)
-               ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h])
-               : 0.f;
+    const float b = lane < chunk_valid(u, c)
+                        ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h])
+                        : 0.f;
+    return (p.flags & KDA_FLAG_BETA_LOGIT) && lane < chunk_valid(u, c) ? rcp_approx(1.f + ex2_approx(-b * LOG2E)) : b;
 }
 
 __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b) {
@@ -572,6 +574,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 // Elementwise phases: thread = (channel quad: channels 4 lane .. 4 lane + 3,
 // token quad: tokens 4 pw .. 4 pw + 3), pw = warp index within the group.
 // ------------------------------------------------------------------------------
+template <bool kSoftplus>
 __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     const int lane = pt & 31, pw = pt >> 5, gq = lane >> 2, tq = lane & 3;
     const int c0 = 4 * lane;
@@ -636,14 +639,31 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 const int i = 4 * pw + r;
-                const float2 x01 = __ffma2_rn(gmv, bf2_to_f2(gw[r].x), gb01);
-                const float2 x23 = __ffma2_rn(gmv, bf2_to_f2(gw[r].y), gb23);
-                const float bl = i < nvalid ? bcoef : 0.f;   // tokens past the end: lambda = 0
-                const float2 blv = make_float2(bl, bl);
-                acc01 = __ffma2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)), rcp_approx(1.f + ex2_approx(x01.y))),
-                                   acc01);
-                acc23 = __ffma2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)), rcp_approx(1.f + ex2_approx(x23.y))),
-                                   acc23);
+                if constexpr (kSoftplus) {
+                    // lambda2 = max(-e^A softplus(z) log2 e, b), z = g + dt_bias, with
+                    // softplus(z) log2 e = max(z, 0) log2 e + log2(1 + 2^(-|z| log2 e)); tokens past
+                    // the end: lambda = 0
+                    const float2 z01 = __fadd2_rn(bf2_to_f2(gw[r].x), make_float2(dt.x, dt.y));
+                    const float2 z23 = __fadd2_rn(bf2_to_f2(gw[r].y), make_float2(dt.z, dt.w));
+                    const float zs[4] = {z01.x, z01.y, z23.x, z23.y};
+                    float lam[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float sp2 = fmaf(fmaxf(zs[e], 0.f), LOG2E, lg2_approx(1.f + ex2_approx(-fabsf(zs[e]) * LOG2E)));
+                        lam[e] = i < nvalid ? fmaxf(-eA * sp2, bcoef) : 0.f;
+                    }
+                    acc01 = __fadd2_rn(acc01, make_float2(lam[0], lam[1]));
+                    acc23 = __fadd2_rn(acc23, make_float2(lam[2], lam[3]));
+                } else {
+                    const float2 x01 = __ffma2_rn(gmv, bf2_to_f2(gw[r].x), gb01);
+                    const float2 x23 = __ffma2_rn(gmv, bf2_to_f2(gw[r].y), gb23);
+                    const float bl = i < nvalid ? bcoef : 0.f;   // tokens past the end: lambda = 0
+                    const float2 blv = make_float2(bl, bl);
+                    acc01 = __ffma2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x01.x)), rcp_approx(1.f + ex2_approx(x01.y))),
+                                       acc01);
+                    acc23 = __ffma2_rn(blv, make_float2(rcp_approx(1.f + ex2_approx(x23.x)), rcp_approx(1.f + ex2_approx(x23.y))),
+                                       acc23);
+                }
                 G01[r] = acc01;
                 G23[r] = acc23;
             }
@@ -920,7 +940,7 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
 
 // kWarpIssue: the instantiation for one CTA per SM (warp-wide MMA issue, pipelined state
 // pass, and the register file to itself: up to 128 registers a thread instead of 72).
-template <bool kBf16State, bool kWarpIssue>
+template <bool kBf16State, bool kWarpIssue, bool kSoftplus>
 __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
@@ -967,7 +987,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     if (warp < W_PREP0) {
         chain_group<kBf16State, kWarpIssue>(p, maps, u, tid);
     } else if (warp < W_INV) {
-        prep_group(p, u, tid - W_PREP0 * 32);
+        prep_group<kSoftplus>(p, u, tid - W_PREP0 * 32);
     } else {
         inverse_warp(p, u, tid & 31);
     }
@@ -1028,8 +1048,11 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 0;
-    auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false>
-                             : (units <= sms ? kda_fwd_tc_kernel<false, true> : kda_fwd_tc_kernel<false, false>);
+    // (the softplus gate is a separate instantiation, so the default one is unchanged)
+    const bool lone = units <= sms, sp = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
+    auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false, false>
+                  : sp       ? (lone ? kda_fwd_tc_kernel<false, true, true> : kda_fwd_tc_kernel<false, false, true>)
+                             : (lone ? kda_fwd_tc_kernel<false, true, false> : kda_fwd_tc_kernel<false, false, false>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);

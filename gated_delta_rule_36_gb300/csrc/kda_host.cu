@@ -131,7 +131,7 @@ kda_status kda_fwd_host(const kda_tensor* q, const kda_tensor* k, const kda_tens
     if (packed) dc = dev_tensor(cu_seqlens, dbuf + L.cu);
     kda_status st = kda::fwd_device(&dq, &dk, &dv, &dg, &db, scale, &dout, &da, &dd, lower_bound,
                                     present(initial_state) ? &di : nullptr, present(final_state) ? &df : nullptr,
-                                    packed ? &dc : nullptr, dbuf + L.ws, L.ws_bytes, nullptr, false, false);
+                                    packed ? &dc : nullptr, dbuf + L.ws, L.ws_bytes, nullptr, false, false, 0u);
     if (st != KDA_OK) return st;
     // host states: in place (the same buffer) or disjoint, as for kda_fwd
     if (present(initial_state) && present(final_state)) {
@@ -250,7 +250,7 @@ kda_status kda_fwd_host(const kda_tensor* q, const kda_tensor* k, const kda_tens
         }
         st = kda::fwd_device(&gq, &gk, &gv, &gg, &gb, scale, &gout, &da, &dd, lower_bound,
                              present(initial_state) ? &gi : nullptr, present(final_state) ? &gf : nullptr,
-                             packed ? &gc : nullptr, dbuf + L.ws, L.ws_bytes, s_user, j == 0, true);
+                             packed ? &gc : nullptr, dbuf + L.ws, L.ws_bytes, s_user, j == 0, true, 0u);
         if (st != KDA_OK) return st;
         if ((e = cudaEventRecord(ev_fwd, s_user)) == cudaSuccess) e = cudaStreamWaitEvent(r.s_out, ev_fwd, 0);
 

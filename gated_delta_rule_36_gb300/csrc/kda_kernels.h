@@ -41,11 +41,13 @@ namespace kda {
 void set_last_error(const char* msg);
 
 // The body of kda_fwd (include/kda.h): every host-side check of the request and, with
-// `enqueue`, its launches on `stream`; `reset_status` clears the device status word first.
+// `enqueue`, its launches on `stream`; `reset_status` clears the device status word first;
+// `flags` are the KDA_FLAG_* interface variants.
 // With enqueue == false nothing touches the device: the call only validates.
 kda_status fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
                       const kda_tensor* beta, float scale, const kda_tensor* out, const kda_tensor* A_log,
                       const kda_tensor* dt_bias, float lower_bound, const kda_tensor* initial_state,
                       const kda_tensor* final_state, const kda_tensor* cu_seqlens, void* workspace,
-                      size_t workspace_bytes, cudaStream_t stream, bool reset_status, bool enqueue);
+                      size_t workspace_bytes, cudaStream_t stream, bool reset_status, bool enqueue,
+                      uint32_t flags);
 }  // namespace kda

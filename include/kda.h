@@ -66,6 +66,14 @@ typedef struct {
  * (FlashInfer PR #4262 notes, sections 2 and 14). */
 #define KDA_MIN_LOWER_BOUND (-5.4585f)
 
+/* Interface variants (the flags of kda_fwd_ex and kda_decode_ex; 0 = kda_fwd / kda_decode):
+ * KDA_FLAG_BETA_LOGIT     beta holds logits; the step uses sigmoid(beta)
+ * KDA_FLAG_GATE_SOFTPLUS  lambda = max(-exp(A_log) softplus(g + dt_bias), lower_bound)
+ *                         instead of lower_bound sigmoid(exp(A_log) (g + dt_bias)); both lie in
+ *                         [lower_bound, 0] (FlashInfer PR #4262 notes, sections 2 and 12) */
+#define KDA_FLAG_BETA_LOGIT    0x1u
+#define KDA_FLAG_GATE_SOFTPLUS 0x2u
+
 /* Device-side status bits, in the first 32-bit word of the workspace. */
 #define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] > T */
 #define KDA_DEVERR_TIMEOUT    0x2u  /* a bounded on-chip wait expired; outputs are invalid  */
@@ -113,6 +121,18 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
                    float lower_bound, const kda_tensor* initial_state,
                    const kda_tensor* final_state, const kda_tensor* cu_seqlens,
                    void* workspace, size_t workspace_bytes, kda_stream_t stream);
+
+/*
+ * kda_fwd with interface variants: `flags` is a combination of KDA_FLAG_* (other bits:
+ * KDA_ERR_INVALID_ARG).  The ablation kernels chosen with KDA_FWD_KERNEL support no flag
+ * (KDA_ERR_UNSUPPORTED).  Everything else is as for kda_fwd.
+ */
+kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                      const kda_tensor* g, const kda_tensor* beta, float scale,
+                      const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                      float lower_bound, const kda_tensor* initial_state,
+                      const kda_tensor* final_state, const kda_tensor* cu_seqlens,
+                      void* workspace, size_t workspace_bytes, uint32_t flags, kda_stream_t stream);
 
 /* Static description of a status code. */
 const char* kda_status_string(kda_status s);
@@ -184,6 +204,13 @@ kda_status kda_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor
                       const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
                       float lower_bound, const kda_tensor* initial_state,
                       const kda_tensor* final_state, kda_stream_t stream);
+
+/* kda_decode with interface variants (`flags` as for kda_fwd_ex). */
+kda_status kda_decode_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                         const kda_tensor* g, const kda_tensor* beta, float scale,
+                         const kda_tensor* out, const kda_tensor* A_log, const kda_tensor* dt_bias,
+                         float lower_bound, const kda_tensor* initial_state,
+                         const kda_tensor* final_state, uint32_t flags, kda_stream_t stream);
 
 /*
  * Device bytes kda_fwd_host needs for a request: q/k/v/g/out [B, T, H, 128], beta, A_log,

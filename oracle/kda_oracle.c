@@ -35,6 +35,13 @@
  *  - packed mode: sequence n starts from initial_state[n] when one is given,
  *    else from zero; tokens at or beyond cu_seqlens[N] are not written.
  *  - beta is used as given (no sigmoid).
+ * Interface variants (kda_oracle_fwd_ex flags; the pages name both, neither is the default):
+ *  - KDA_ORACLE_BETA_LOGIT: beta is a logit, the step uses sigmoid(beta) ("logit beta" is
+ *    an eligibility condition of the FlashInfer page, section 12).
+ *  - KDA_ORACLE_GATE_SOFTPLUS: the gate max(-exp(A_log) softplus(g + dt_bias), lower_bound),
+ *    the other public lower-bounded form of the KDA gate; it also lies in [lower_bound, 0].
+ *    PARITY UNPINNED for its functional form, like the default gate; its special values
+ *    (g + dt_bias = 0, large |g + dt_bias|) and range are pinned by tests.
  */
 #include <math.h>
 #include <stdint.h>
@@ -45,6 +52,8 @@
 #endif
 
 #define KDA_ORACLE_EPS 1e-6
+#define KDA_ORACLE_BETA_LOGIT 0x1u
+#define KDA_ORACLE_GATE_SOFTPLUS 0x2u
 
 /* Gate: natural-log decay of one key channel (reading stated in the header). */
 double kda_oracle_gate(double g, double A_log, double dt_bias, double lower_bound)
@@ -54,12 +63,22 @@ double kda_oracle_gate(double g, double A_log, double dt_bias, double lower_boun
     return lower_bound * sig;
 }
 
+/* The alternative gate: max(-exp(A_log) softplus(g + dt_bias), lower_bound), with
+ * softplus(z) = log(1 + exp(z)) evaluated without overflow. */
+double kda_oracle_gate_softplus(double g, double A_log, double dt_bias, double lower_bound)
+{
+    double z = g + dt_bias;
+    double sp = z > 0.0 ? z + log1p(exp(-z)) : log1p(exp(z));
+    double lam = -exp(A_log) * sp;
+    return lam > lower_bound ? lam : lower_bound;
+}
+
 /* One (sequence, head) unit over tokens [bos, eos) of the flattened token axis. */
 static void oracle_unit(int64_t H, int64_t K, int64_t V, int64_t h, int64_t bos, int64_t eos,
                         const double* q, const double* k, const double* v, const double* g,
                         const double* beta, double scale, const double* A_log,
                         const double* dt_bias, double lower_bound, const double* S0,
-                        double* out, double* S_final, double* S, double* work)
+                        double* out, double* S_final, double* S, double* work, unsigned flags)
 {
     double* decay = work;        /* [K] exp(lambda)     */
     double* qh = work + K;       /* [K] normalised q    */
@@ -76,11 +95,14 @@ static void oracle_unit(int64_t H, int64_t K, int64_t V, int64_t h, int64_t bos,
         const double* kt = k + (t * H + h) * K;
         const double* gt = g + (t * H + h) * K;
         const double* vt = v + (t * H + h) * V;
-        const double bt = beta[t * H + h];
+        const double braw = beta[t * H + h];
+        const double bt = (flags & KDA_ORACLE_BETA_LOGIT) ? 1.0 / (1.0 + exp(-braw)) : braw;
 
         double sq = 0.0, sk = 0.0;
         for (int64_t d = 0; d < K; ++d) {
-            decay[d] = exp(kda_oracle_gate(gt[d], A_log[h], dt_bias[h * K + d], lower_bound));
+            decay[d] = exp((flags & KDA_ORACLE_GATE_SOFTPLUS)
+                               ? kda_oracle_gate_softplus(gt[d], A_log[h], dt_bias[h * K + d], lower_bound)
+                               : kda_oracle_gate(gt[d], A_log[h], dt_bias[h * K + d], lower_bound));
             sq += qt[d] * qt[d];
             sk += kt[d] * kt[d];
         }
@@ -118,11 +140,11 @@ static void oracle_unit(int64_t H, int64_t K, int64_t V, int64_t h, int64_t bos,
  * Rows of out that belong to no sequence are left untouched.
  * Returns 0 on success, a negative code on invalid arguments.
  */
-int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
-                   const double* q, const double* k, const double* v, const double* g,
-                   const double* beta, double scale, const double* A_log, const double* dt_bias,
-                   double lower_bound, const double* initial_state, const int64_t* cu_seqlens,
-                   int64_t N, double* out, double* final_state, int nthreads)
+int kda_oracle_fwd_ex(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                      const double* q, const double* k, const double* v, const double* g,
+                      const double* beta, double scale, const double* A_log, const double* dt_bias,
+                      double lower_bound, const double* initial_state, const int64_t* cu_seqlens,
+                      int64_t N, double* out, double* final_state, int nthreads, unsigned flags)
 {
     if (B < 1 || T < 0 || H < 1 || K < 1 || V < 1) return -1;
     int64_t nseq = B;
@@ -166,13 +188,24 @@ int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
                 const double* S0 = initial_state ? initial_state + (size_t)u * state_elems : NULL;
                 double* Sf = final_state ? final_state + (size_t)u * state_elems : NULL;
                 oracle_unit(H, K, V, h, bos, eos, q, k, v, g, beta, scale, A_log, dt_bias,
-                            lower_bound, S0, out, Sf, S, work);
+                            lower_bound, S0, out, Sf, S, work, flags);
             }
         }
         free(S);
         free(work);
     }
     return rc;
+}
+
+/* The forward with neither interface variant (beta as given, the sigmoid gate). */
+int kda_oracle_fwd(int64_t B, int64_t T, int64_t H, int64_t K, int64_t V,
+                   const double* q, const double* k, const double* v, const double* g,
+                   const double* beta, double scale, const double* A_log, const double* dt_bias,
+                   double lower_bound, const double* initial_state, const int64_t* cu_seqlens,
+                   int64_t N, double* out, double* final_state, int nthreads)
+{
+    return kda_oracle_fwd_ex(B, T, H, K, V, q, k, v, g, beta, scale, A_log, dt_bias, lower_bound,
+                             initial_state, cu_seqlens, N, out, final_state, nthreads, 0u);
 }
 
 /* Number of OpenMP threads a parallel region of this library would use. */

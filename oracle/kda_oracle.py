@@ -48,8 +48,12 @@ def _load():
             lib.kda_oracle_fwd.restype = ctypes.c_int
             lib.kda_oracle_fwd.argtypes = [i64, i64, i64, i64, i64, p, p, p, p, p, d, p, p, d,
                                            p, p, i64, p, p, ctypes.c_int]
+            lib.kda_oracle_fwd_ex.restype = ctypes.c_int
+            lib.kda_oracle_fwd_ex.argtypes = lib.kda_oracle_fwd.argtypes + [ctypes.c_uint]
             lib.kda_oracle_gate.restype = d
             lib.kda_oracle_gate.argtypes = [d, d, d, d]
+            lib.kda_oracle_gate_softplus.restype = d
+            lib.kda_oracle_gate_softplus.argtypes = [d, d, d, d]
             lib.kda_oracle_max_threads.restype = ctypes.c_int
             lib.kda_oracle_max_threads.argtypes = []
             _lib = lib
@@ -71,9 +75,17 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+BETA_LOGIT, GATE_SOFTPLUS = 0x1, 0x2   # kda_oracle_fwd_ex flags (interface variants)
+
+
 def gate(g, A_log, dt_bias, lower_bound):
     """Scalar gate (natural log-decay), for tests of its range and special cases."""
     return _load().kda_oracle_gate(float(g), float(A_log), float(dt_bias), float(lower_bound))
+
+
+def gate_softplus(g, A_log, dt_bias, lower_bound):
+    """Scalar alternative gate max(-exp(A_log) softplus(g + dt_bias), lower_bound)."""
+    return _load().kda_oracle_gate_softplus(float(g), float(A_log), float(dt_bias), float(lower_bound))
 
 
 def max_threads() -> int:
@@ -82,7 +94,7 @@ def max_threads() -> int:
 
 def kda_oracle_fwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound,
                    initial_state=None, cu_seqlens=None, nthreads: int = 0,
-                   out_fill: float = np.nan):
+                   out_fill: float = np.nan, flags: int = 0):
     """Run the oracle.  Shapes: q,k,g [B,T,H,K]; v [B,T,H,V]; beta [B,T,H];
     A_log [H]; dt_bias [H,K]; initial_state [Nseq,H,V,K] or None;
     cu_seqlens [N+1] (int64) or None.
@@ -112,9 +124,9 @@ def kda_oracle_fwd(q, k, v, g, beta, scale, A_log, dt_bias, lower_bound,
         assert S0.shape == (nseq, H, V, K), f"initial_state shape {S0.shape}"
     out = np.full((B, T, H, V), out_fill, dtype=np.float64)
     final = np.empty((nseq, H, V, K), dtype=np.float64)
-    rc = _load().kda_oracle_fwd(B, T, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
-                                float(scale), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
-                                _ptr(S0), _ptr(cu), N, _ptr(out), _ptr(final), int(nthreads))
+    rc = _load().kda_oracle_fwd_ex(B, T, H, K, V, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   float(scale), _ptr(A_log), _ptr(dt_bias), float(lower_bound),
+                                   _ptr(S0), _ptr(cu), N, _ptr(out), _ptr(final), int(nthreads), int(flags))
     if rc != 0:
         raise ValueError(f"kda_oracle_fwd rejected its arguments (code {rc})")
     return out, final

@@ -375,3 +375,59 @@ def test_centering_constants():
     # bf16 normal range (2^-126 .. 2^127) holds the centered factors iff 16|b| <= 126.
     lb_limit = -126.0 / (16 * LOG2E)
     assert abs(lb_limit - (-5.4585)) < 1e-4
+
+
+# ----------------------------------------------------------------------------
+# Interface variants (oracle flags): beta as a logit, the softplus gate
+# ----------------------------------------------------------------------------
+
+def _oracle_flags(u, flags):
+    T, K = u["q"].shape
+    V = u["v"].shape[1]
+    out, fin = O.kda_oracle_fwd(u["q"][None, :, None], u["k"][None, :, None], u["v"][None, :, None],
+                                u["g"][None, :, None], u["beta"][None, :, None], u["scale"],
+                                np.array([u["A_log"]]), u["dt_bias"][None], u["lb"],
+                                initial_state=None if u["S0"] is None else u["S0"][None, None], flags=flags)
+    return out[0, :, 0], fin[0, 0]
+
+
+def test_beta_logit_special_values():
+    """sigmoid(0) = 1/2 exactly; sigmoid(40) = 1 to within 5e-18."""
+    rng = np.random.default_rng(7000)
+    u = rand_unit(rng, 23, 16, 8)
+    for logit, value, tol in ((0.0, 0.5, 0.0), (40.0, 1.0, 1e-14)):
+        ul = dict(u, beta=np.full(23, logit))
+        uv = dict(u, beta=np.full(23, value))
+        a, fa = _oracle_flags(ul, O.BETA_LOGIT)
+        b, fb = _oracle_flags(uv, 0)
+        assert rel(a, b) <= tol and rel(fa, fb) <= tol
+
+
+def test_softplus_gate_special_values():
+    """softplus(0) = ln 2, so g + dt_bias = 0 gives lambda = max(-exp(A_log) ln 2, lb);
+    far below zero the gate vanishes, far above it sits on lower_bound; it is monotone."""
+    assert O.gate_softplus(0.3, 0.0, -0.3, -5.0) == pytest.approx(-math.log(2.0), rel=1e-15)
+    assert O.gate_softplus(-1.0, math.log(3.0), 1.0, -5.0) == pytest.approx(-3.0 * math.log(2.0), rel=1e-14)
+    assert O.gate_softplus(0.0, math.log(3.0), 0.0, -1.5) == -1.5                # clamped
+    assert -1e-20 < O.gate_softplus(-50.0, 0.0, 0.0, -5.0) < 0.0
+    assert O.gate_softplus(50.0, 0.0, 0.0, -5.0) == -5.0
+    rng = np.random.default_rng(7100)
+    for _ in range(2000):
+        g, A, dt = rng.standard_normal() * 6, rng.uniform(-2, 2), rng.uniform(-2, 2)
+        lb = -rng.uniform(0, 8)
+        assert lb <= O.gate_softplus(g, A, dt, lb) <= 0.0
+    xs = np.linspace(-6, 6, 101)
+    vals = [O.gate_softplus(x, 0.2, 0.1, -5.0) for x in xs]
+    assert all(b <= a for a, b in zip(vals, vals[1:]))
+
+
+def test_softplus_gate_decays_columns_by_ln2():
+    """beta = 0 and g = -dt_bias everywhere: every channel decays by exp(-exp(A_log) ln 2)
+    per token, so the final state is S0 (1/2)^(exp(A_log) T) column for column."""
+    rng = np.random.default_rng(7200)
+    T, K, V = 9, 16, 8
+    u = rand_unit(rng, T, K, V, lb=-5.0)
+    u["beta"] = np.zeros(T)
+    u["g"] = -np.broadcast_to(u["dt_bias"], (T, K)).copy()
+    _, fin = _oracle_flags(u, O.GATE_SOFTPLUS)
+    assert rel(fin, u["S0"] * 0.5 ** (math.exp(u["A_log"]) * T)) < 1e-13
