@@ -32,12 +32,14 @@ __device__ __forceinline__ float4 bf16x4_to_f4(uint2 w) {
     return make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
 }
 
+template <bool kBetaLogit, bool kSoftplus>
 __global__ void __launch_bounds__(DEC_THREADS) kda_decode_kernel(const FwdParams p) {
     const int unit = blockIdx.x / DEC_BLOCKS_PER_UNIT, rb = blockIdx.x % DEC_BLOCKS_PER_UNIT;
     const int h = unit % p.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = 4 * lane;
     const size_t tok = (size_t)unit * HD;   // the (sequence, head) row of q, k, v, g, out
+    const int r0 = rb * DEC_ROWS_PER_CTA + warp * DEC_ROWS_PER_WARP;
 
     // per key channel (this lane's four): k^, q^, D = exp(lambda)
     const float4 q4 = bf16x4_to_f4(*reinterpret_cast<const uint2*>(p.q + tok + c0));
@@ -54,23 +56,24 @@ __global__ void __launch_bounds__(DEC_THREADS) kda_decode_kernel(const FwdParams
     const float eA = expf(p.A_log[h]);
     const float gm = -eA * LOG2E;
     const float bcoef = p.lower_bound * LOG2E;
-    const bool softplus = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
     const float gx[4] = {g4.x + dt.x, g4.y + dt.y, g4.z + dt.z, g4.w + dt.w};
     float D[4], dk[4], dq[4];
+    if constexpr (kSoftplus) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            D[j] = ex2_approx(fmaxf(-eA * fmaf(fmaxf(gx[j], 0.f), LOG2E, lg2_approx(1.f + ex2_approx(-fabsf(gx[j]) * LOG2E))),
+                                    bcoef));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) D[j] = ex2_approx(bcoef * rcp_approx(1.f + ex2_approx(gm * gx[j])));
+    }
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const float lam2 = softplus
-            ? fmaxf(-eA * fmaf(fmaxf(gx[j], 0.f), LOG2E, lg2_approx(1.f + ex2_approx(-fabsf(gx[j]) * LOG2E))), bcoef)
-            : bcoef * rcp_approx(1.f + ex2_approx(gm * gx[j]));
-        D[j] = ex2_approx(lam2);
         dk[j] = D[j] * kh[j];
         dq[j] = D[j] * qh[j];
     }
     float beta = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[unit]);
-    if (p.flags & KDA_FLAG_BETA_LOGIT) beta = rcp_approx(1.f + ex2_approx(-beta * LOG2E));
-    const int r0 = rb * DEC_ROWS_PER_CTA + warp * DEC_ROWS_PER_WARP;
-    const float vr = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.v)[tok + r0 + (lane & 7)]);
-
+    if constexpr (kBetaLogit) beta = rcp_approx(1.f + ex2_approx(-beta * LOG2E));
     // the warp's 8 state rows, all loads in flight at once
     const size_t srow0 = ((size_t)unit * HD + r0) * HD + c0;
     float4 s[DEC_ROWS_PER_WARP];
@@ -81,6 +84,9 @@ __global__ void __launch_bounds__(DEC_THREADS) kda_decode_kernel(const FwdParams
         else if (p.init_f32) s[i] = *reinterpret_cast<const float4*>(static_cast<const float*>(p.init_state) + off);
         else s[i] = bf16x4_to_f4(*reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.init_state) + off));
     }
+
+    const float vr = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.v)[tok + r0 + (lane & 7)]);
+
     float my_out = 0.f;
 #pragma unroll
     for (int i = 0; i < DEC_ROWS_PER_WARP; ++i) {
@@ -117,7 +123,10 @@ cudaError_t launch_decode(const FwdParams& p, cudaStream_t stream) {
     const long long units = (long long)p.nseq * p.H;
     if (units == 0) return cudaSuccess;
     if (units * DEC_BLOCKS_PER_UNIT > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kda_decode_kernel<<<(unsigned)(units * DEC_BLOCKS_PER_UNIT), DEC_THREADS, 0, stream>>>(p);
+    const bool logit = (p.flags & KDA_FLAG_BETA_LOGIT) != 0, sp = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
+    auto kernel = logit ? (sp ? kda_decode_kernel<true, true> : kda_decode_kernel<true, false>)
+                        : (sp ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>);
+    kernel<<<(unsigned)(units * DEC_BLOCKS_PER_UNIT), DEC_THREADS, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
