@@ -314,14 +314,15 @@ __device__ __forceinline__ void prefetch_chunk(const TmaMaps& maps, const Unit& 
 }
 
 // beta of token `lane` of chunk c (0 past the end), by a plain load: its token stride
-// is 2H bytes, too narrow for a tensor box when H is small.  With KDA_FLAG_BETA_LOGIT the
-// stored value is a logit and beta = sigmoid(logit).
+// is 2H bytes, too narrow for a tensor box when H is small.  kBetaLogit (KDA_FLAG_BETA_LOGIT):
+// the stored value is a logit and beta = sigmoid(logit).
+template <bool kBetaLogit>
 __device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, int c, int lane) {
     const int64_t t0 = u.bos + (int64_t)c * CH;
-    const float b = lane < chunk_valid(u, c)
-                        ? bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h])
-                        : 0.f;
-    return (p.flags & KDA_FLAG_BETA_LOGIT) && lane < chunk_valid(u, c) ? rcp_approx(1.f + ex2_approx(-b * LOG2E)) : b;
+    if (lane >= chunk_valid(u, c)) return 0.f;
+    const float b = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h]);
+    if constexpr (kBetaLogit) return rcp_approx(1.f + ex2_approx(-b * LOG2E));
+    return b;
 }
 
 __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b) {
@@ -329,7 +330,7 @@ __device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b
     mbar_arrive(bar_addr(u, B_FULLTMA + (c & 1)));
 }
 
-template <bool kBf16State, bool kWarpIssue>
+template <bool kBf16State, bool kWarpIssue, bool kBetaLogit>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
@@ -355,10 +356,10 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     if (pt == T_STORE)
         for (int c = 0; c < first; ++c) load_v(maps, u, c);
     if (w == W_BETA)
-        for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta(p, u, c, lane));
+        for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta<kBetaLogit>(p, u, c, lane));
     // beta of chunk c + 2 goes into the slot during iteration c; it is loaded an iteration
     // ahead (its 2-byte loads, 2H bytes apart, miss the caches)
-    float beta_ahead = (w == W_BETA && NSLOT < u.nchunks) ? load_beta(p, u, NSLOT, lane) : 0.f;
+    float beta_ahead = (w == W_BETA && NSLOT < u.nchunks) ? load_beta<kBetaLogit>(p, u, NSLOT, lane) : 0.f;
     int issued = first;   // chunks whose boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
         const int n = pt >> 2, kb = pt & 3;
@@ -391,7 +392,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) break;
         // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
         const float beta_next = beta_ahead;
-        if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta(p, u, c + NSLOT + 1, lane);
+        if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
         if (w == W_MMA) {
             if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) break;
             tc_fence_after();
@@ -940,7 +941,7 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
 
 // kWarpIssue: the instantiation for one CTA per SM (warp-wide MMA issue, pipelined state
 // pass, and the register file to itself: up to 128 registers a thread instead of 72).
-template <bool kBf16State, bool kWarpIssue, bool kSoftplus>
+template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit>
 __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
@@ -985,7 +986,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     u.tmem = *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR);
 
     if (warp < W_PREP0) {
-        chain_group<kBf16State, kWarpIssue>(p, maps, u, tid);
+        chain_group<kBf16State, kWarpIssue, kBetaLogit>(p, maps, u, tid);
     } else if (warp < W_INV) {
         prep_group<kSoftplus>(p, u, tid - W_PREP0 * 32);
     } else {
@@ -1048,11 +1049,16 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         sms = 0;
-    // (the softplus gate is a separate instantiation, so the default one is unchanged)
+    // (the interface variants are separate instantiations, so the default one is unchanged)
     const bool lone = units <= sms, sp = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
-    auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false, false>
-                  : sp       ? (lone ? kda_fwd_tc_kernel<false, true, true> : kda_fwd_tc_kernel<false, false, true>)
-                             : (lone ? kda_fwd_tc_kernel<false, true, false> : kda_fwd_tc_kernel<false, false, false>);
+    const bool lg = (p.flags & KDA_FLAG_BETA_LOGIT) != 0;
+    using Kernel = void (*)(const FwdParams, const TmaMaps);
+    static constexpr Kernel table[2][2][2] = {   // [lone][softplus][beta logit]
+        {{kda_fwd_tc_kernel<false, false, false, false>, kda_fwd_tc_kernel<false, false, false, true>},
+         {kda_fwd_tc_kernel<false, false, true, false>, kda_fwd_tc_kernel<false, false, true, true>}},
+        {{kda_fwd_tc_kernel<false, true, false, false>, kda_fwd_tc_kernel<false, true, false, true>},
+         {kda_fwd_tc_kernel<false, true, true, false>, kda_fwd_tc_kernel<false, true, true, true>}}};
+    auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false, false, false> : table[lone][sp][lg];
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
