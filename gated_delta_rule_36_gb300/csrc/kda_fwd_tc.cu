@@ -881,14 +881,10 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
                     }
                 }
             }
-            // X_bb to shared memory for the block product; -B2 of the diagonal block from registers
+            // X_bb to shared memory, for the block product and the -B2 rows below
             float* xc = Xb + (b ? XB_22 : 0) + cc;
-            const float nbeta = -bs[16 * b + cc];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                xc[r * XB] = x[r];
-                *reinterpret_cast<uint16_t*>(b2s + core_offset(16 * b + r, 16 * b + cc, 32)) = bf16_bits(nbeta * x[r]);
-            }
+            for (int r = 0; r < 16; ++r) xc[r * XB] = x[r];
         }
         __syncwarp();
 
@@ -909,6 +905,24 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr(u, B_LFREE));   // L has been read: the prep warps may rewrite it
+
+        // -B2 rows of the diagonal blocks: lane n reads row n of its block of X and writes the
+        // row's 16 values as two 16-byte stores (a lane per row keeps the core-matrix layout's
+        // stores free of bank conflicts; a lane per column would put every lane on four banks)
+        {
+            const int n = lane, o = n & 16;
+            const float* xr = Xb + (o ? XB_22 : 0) + (n & 15) * XB;
+            uint32_t wv[8];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 xv = *reinterpret_cast<const float4*>(xr + 4 * q4);
+                const float4 bv = *reinterpret_cast<const float4*>(bs + o + 4 * q4);
+                wv[2 * q4] = pack_bf16x2(-bv.x * xv.x, -bv.y * xv.y);
+                wv[2 * q4 + 1] = pack_bf16x2(-bv.z * xv.z, -bv.w * xv.w);
+            }
+            *reinterpret_cast<uint4*>(b2s + core_offset(n, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            *reinterpret_cast<uint4*>(b2s + core_offset(n, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+        }
 
         // ---- y = T2^T X22^T = (X22 T2)^T = -X21^T: y[nt][e] = y[gq + 8 (e >> 1)][8 nt + 2 tq + (e & 1)]
         float y[2][4];
