@@ -142,7 +142,9 @@ kda_status kda_fwd_host(const kda_tensor* q, const kda_tensor* k, const kda_tens
             return fail(KDA_ERR_ALIAS, "initial_state and final_state overlap but are not the same buffer and dtype");
     }
 
-    // sequences of each group: consecutive, about the same number of tokens each
+    // sequences of each group: consecutive, with token counts falling linearly from the
+    // first group to the last (proportional to want, want - 1, ..., 1): the last group's
+    // forward and copies back are the part of the call nothing overlaps, so it is the smallest
     const int64_t* cu = packed ? static_cast<const int64_t*>(cu_seqlens->data) : nullptr;
     if (packed) {
         if (cu[0] != 0) return fail(KDA_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
@@ -154,8 +156,11 @@ kda_status kda_fwd_host(const kda_tensor* q, const kda_tensor* k, const kda_tens
     auto tok_of = [&](int64_t n) { return packed ? cu[n] : n * T; };   // first token of sequence n
     const int64_t tok_total = tok_of(nseq);
     std::vector<int64_t> cut{0};   // group j: sequences [cut[j], cut[j+1])
+    const int64_t wsum = (int64_t)want * (want + 1) / 2;
+    int64_t wacc = 0;
     for (int j = 1; j < want; ++j) {
-        const int64_t target = tok_total * j / want;
+        wacc += want - (j - 1);   // weight of group j - 1
+        const int64_t target = tok_total * wacc / wsum;
         int64_t n = cut.back();
         while (n < nseq && tok_of(n) < target) ++n;
         if (n > cut.back() && n < nseq) cut.push_back(n);

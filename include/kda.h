@@ -225,8 +225,9 @@ size_t kda_fwd_host_device_bytes(int64_t B, int64_t T, int H, int64_t N, int ini
  * memory, with the shapes, dtypes and meaning of kda_fwd.  The call copies the inputs to
  * `device_buffer` (>= kda_fwd_host_device_bytes bytes, 256-byte aligned, owned by the
  * caller and holding nothing the caller needs), runs the forward, and copies `out` and
- * `final_state` back.  It splits the sequences into up to `groups` consecutive groups of
- * about equal token counts (groups <= 0: 8) and pipelines them over three streams: the
+ * `final_state` back.  It splits the sequences into up to `groups` consecutive groups whose
+ * token counts fall from the first to the last (groups <= 0: 8; the last group's work is
+ * the only part nothing overlaps) and pipelines them over three streams: the
  * host-to-device copies of group j + 1 run while group j computes and its results are
  * copied back.  The work is ordered after everything already on `stream` and `stream`
  * is ordered after all of it; the call itself returns once the work is enqueued, so the
