@@ -24,8 +24,9 @@ HEAD_DIM = 128
 # Every function include/kda.h declares.
 EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
             "kda_read_device_status", "kda_fwd_no_alloc", "kda_fwd_host_device_bytes", "kda_fwd_host",
-            "kda_fwd_host_workspace_offset", "kda_decode", "kda_fwd_ex", "kda_decode_ex")
+            "kda_fwd_host_workspace_offset", "kda_decode", "kda_fwd_ex", "kda_decode_ex", "kda_fwd_schedule")
 KDA_FLAG_BETA_LOGIT, KDA_FLAG_GATE_SOFTPLUS = 0x1, 0x2
+KDA_SCHEDULE_TWO_PER_SM, KDA_SCHEDULE_ONE_PER_SM, KDA_SCHEDULE_CLUSTER = 0, 1, 2
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
 
@@ -70,6 +71,8 @@ def load(path: Optional[str] = None):
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []
+        lib.kda_fwd_schedule.restype = ctypes.c_int
+        lib.kda_fwd_schedule.argtypes = [ctypes.c_int64, ctypes.c_uint32, ctypes.POINTER(ctypes.c_int32)]
         lib.kda_read_device_status.restype = ctypes.c_int
         lib.kda_read_device_status.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
                                                ctypes.POINTER(ctypes.c_uint32)]
@@ -251,6 +254,15 @@ def kda_decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initia
     else:
         st = lib.kda_decode(*args, ctypes.c_void_p(sh))
     _check(lib, st)
+
+
+def kda_fwd_schedule(units: int, flags: int = 0) -> int:
+    """KDA_SCHEDULE_* that kda_fwd takes on the current device for ``units`` (sequence, head)
+    units: two CTAs per SM, one CTA per SM, or a cluster of four CTAs per unit."""
+    lib = load()
+    sched = ctypes.c_int32(-1)
+    _check(lib, lib.kda_fwd_schedule(int(units), int(flags), ctypes.byref(sched)))
+    return int(sched.value)
 
 
 def kda_read_device_status(workspace, stream=None) -> int:

@@ -318,6 +318,18 @@ kda_status kda_decode_ex(const kda_tensor* q, const kda_tensor* k, const kda_ten
     return KDA_OK;
 }
 
+kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule) {
+    if (schedule == nullptr) return fail(KDA_ERR_INVALID_ARG, "null schedule");
+    if (units < 0) return fail(KDA_ERR_INVALID_ARG, "units must be >= 0");
+    if (flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
+        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x", flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
+    int sched = KDA_SCHEDULE_TWO_PER_SM;
+    const cudaError_t e = kda::fwd_tc_schedule(units, flags, false, &sched);
+    if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "schedule query: %s", cudaGetErrorString(e));
+    *schedule = sched;
+    return KDA_OK;
+}
+
 kda_status kda_read_device_status(const void* workspace, kda_stream_t stream, uint32_t* bits) {
     if (workspace == nullptr || bits == nullptr) return fail(KDA_ERR_INVALID_ARG, "null argument");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

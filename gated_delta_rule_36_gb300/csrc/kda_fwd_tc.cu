@@ -88,10 +88,17 @@ constexpr uint32_t OFF_X = OFF_L + L_BYTES;
 constexpr uint32_t X_BYTES = (XB_22 + 16 * XB) * 4;
 constexpr uint32_t OFF_NEGI = OFF_X + X_BYTES;   // -I (bf16 32 x 32, K-major core layout)
 constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
-// Per slot: FULLTMA (q, k, g boxes and beta landed), FULLV (v box landed), AREADY (the prep
-// warps wrote a), FULLP (the prep warps finished the chunk's operands and L), FULLD (the
-// inverse warp wrote -B2).  LFREE: the inverse warp has read L.  Chain: G1, G2, G3 (MMA commits).
-enum { B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 4, B_FULLP = 6, B_FULLD = 8, B_LFREE = 10, B_G1, B_G2, B_G3, B_COUNT };
+// Per slot: FULLTMA (q, k, g boxes and beta landed), FULLV (v box landed; three slots in a
+// cluster's home CTA), AREADY (the prep warps wrote a), FULLP (the prep warps finished the
+// chunk's operands and L), FULLD (the inverse warp wrote -B2).  LFREE: the inverse warp has
+// read L.  Chain: G1, G2, G3 (MMA commits).  Cluster schedule (below): FULLOP (home slot s
+// holds a pulled chunk), HFREE (the chain is done with home slot s), READY (on the home CTA,
+// entry 2 h + b: helper h finished the chunk in its slot b), COPIED (on a helper: the home
+// CTA has pulled the chunk in its slot b).
+enum {
+    B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 5, B_FULLP = 7, B_FULLD = 9, B_LFREE = 11, B_G1, B_G2, B_G3,
+    B_FULLOP = 15, B_HFREE = 18, B_READY = 21, B_COPIED = 27, B_COUNT = 29
+};
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
@@ -99,6 +106,19 @@ static_assert(SLOT_BYTES % 1024 == 0, "slots must keep the 128-B swizzle atoms 1
 static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs must fit one SM");
 static_assert(OFF_QC % 256 == 0 && OFF_KC % 256 == 0 && OFF_KI % 256 == 0, "scratch tiles must be 256-B aligned");
 static_assert(OFF_L % 16 == 0 && OFF_X % 16 == 0 && OFF_NEGI % 16 == 0, "float4 / descriptor alignment");
+
+// Cluster schedule, for few units: a cluster of 1 + NHELP CTAs per unit.  The home CTA (rank
+// 0) runs the chain over NHELP slots; helper h (rank h + 1) prepares the chunks c = h (mod
+// NHELP) in its own two slots with the prep and inverse warps, and the home CTA's prep warps
+// pull each finished chunk over distributed shared memory into home slot h.
+constexpr int NHELP = 3, CL_SIZE = NHELP + 1;
+constexpr uint32_t OFF_SLOT2 = (SMEM_USED + 1023) & ~1023u;   // the home CTA's third slot
+constexpr uint32_t SMEM_BYTES_CL = OFF_SLOT2 + SLOT_BYTES + 1024;
+static_assert(SMEM_BYTES_CL <= 232448, "the cluster layout must fit one CTA's shared memory");
+// The pulled part of a slot: [Q_d | K_d] and K_r (bytes [0, SL_V)), then Mqk, -B2 and a
+// (bytes [SL_MQT, SL_BETA)); v is the home CTA's own.
+constexpr int PULL_VECS_A = SL_V / 16, PULL_VECS = PULL_VECS_A + (SL_BETA - SL_MQT) / 16;
+__host__ __device__ constexpr uint32_t slot_off(int s) { return s < 2 ? (uint32_t)s * SLOT_BYTES : OFF_SLOT2; }
 
 // Index of element (i, j), j < 16 or i, j >= 16, of L in its block layout.
 __host__ __device__ constexpr int l_index(int i, int j) {
@@ -282,9 +302,8 @@ __device__ __forceinline__ int chunk_valid(const Unit& u, int c) {
     return (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
 }
 
-// q, k, g boxes of chunk c into its slot (on FULLTMA, which beta completes).
-__device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int c) {
-    const int s = c & 1;
+// q, k, g boxes of chunk c into slot s (on FULLTMA, which beta completes).
+__device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int c, int s) {
     const int t0 = (int)(u.bos + (int64_t)c * CH);
     const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLTMA + s);
     mbar_arrive_expect_tx(full, 3u * CH * HD * 2u);
@@ -293,11 +312,10 @@ __device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int
     tma_load_3d(slot + SL_RAWG, &maps.g, 0, u.h, t0, full);
 }
 
-// the v box of chunk c (two 64-channel halves, 128-byte swizzle) on FULLV.
-__device__ __forceinline__ void load_v(const TmaMaps& maps, const Unit& u, int c) {
-    const int s = c & 1;
+// the v box of chunk c (two 64-channel halves, 128-byte swizzle) into slot s, on FULLV.
+__device__ __forceinline__ void load_v(const TmaMaps& maps, const Unit& u, int c, int s) {
     const int t0 = (int)(u.bos + (int64_t)c * CH);
-    const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLV + s);
+    const uint32_t slot = u.base + slot_off(s), full = bar_addr(u, B_FULLV + s);
     mbar_arrive_expect_tx(full, CH * HD * 2u);
     tma_load_3d(slot + SL_V, &maps.v, 0, u.h, t0, full);
     tma_load_3d(slot + SL_V + 4096, &maps.v, 64, u.h, t0, full);
@@ -325,13 +343,17 @@ __device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, in
     return b;
 }
 
-__device__ __forceinline__ void put_beta(const Unit& u, int c, int lane, float b) {
-    reinterpret_cast<float*>(u.gbase + (c & 1) * SLOT_BYTES + SL_BETA)[lane] = b;
-    mbar_arrive(bar_addr(u, B_FULLTMA + (c & 1)));
+__device__ __forceinline__ void put_beta(const Unit& u, int s, int lane, float b) {
+    reinterpret_cast<float*>(u.gbase + s * SLOT_BYTES + SL_BETA)[lane] = b;
+    mbar_arrive(bar_addr(u, B_FULLTMA + s));
 }
 
-template <bool kBf16State, bool kWarpIssue, bool kBetaLogit>
+// kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pulled chunks (FULLOP
+// stands for AREADY, FULLP and FULLD at once), it loads v alone, and it hands each slot back
+// (HFREE) once GEMM3 has read it.
+template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
+    constexpr int NS = kCl ? NHELP : NSLOT;   // slots in the ring
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
     constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);                // GEMM2, and O += U Mqk^T
@@ -350,17 +372,20 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         else tmem_st16(lane_addr + TM_S + piece * 16, r);
     }
     if (u.nchunks == 0) return;
-    const int first = u.nchunks < NSLOT ? u.nchunks : NSLOT;
-    if (pt == T_TMA)
-        for (int c = 0; c < first; ++c) load_qkg(maps, u, c);
+    const int first = u.nchunks < NS ? u.nchunks : NS;
+    if constexpr (!kCl) {
+        if (pt == T_TMA)
+            for (int c = 0; c < first; ++c) load_qkg(maps, u, c, c);
+        if (w == W_BETA)
+            for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta<kBetaLogit>(p, u, c, lane));
+    }
     if (pt == T_STORE)
-        for (int c = 0; c < first; ++c) load_v(maps, u, c);
-    if (w == W_BETA)
-        for (int c = 0; c < first; ++c) put_beta(u, c, lane, load_beta<kBetaLogit>(p, u, c, lane));
+        for (int c = 0; c < first; ++c) load_v(maps, u, c, c);
     // beta of chunk c + 2 goes into the slot during iteration c; it is loaded an iteration
     // ahead (its 2-byte loads, 2H bytes apart, miss the caches)
-    float beta_ahead = (w == W_BETA && NSLOT < u.nchunks) ? load_beta<kBetaLogit>(p, u, NSLOT, lane) : 0.f;
-    int issued = first;   // chunks whose boxes were requested
+    float beta_ahead = (!kCl && w == W_BETA && NSLOT < u.nchunks) ? load_beta<kBetaLogit>(p, u, NSLOT, lane) : 0.f;
+    int issued = first;    // chunks whose boxes were requested
+    int vissued = first;   // (cluster home) chunks whose v boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
         const int n = pt >> 2, kb = pt & 3;
         const uint32_t m1 = ((n >> 3) == kb) ? ((n & 1) ? 0xBF800000u : 0x0000BF80u) : 0u;   // bf16 -1 at column n
@@ -370,7 +395,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         fence_proxy_async_smem();
     }
     tmem_wait_st();
-    bool ok = warp_wait(bar_addr(u, B_AREADY), 0, p.status, 256);   // a of chunk 0
+    bool ok = warp_wait(bar_addr(u, kCl ? B_FULLOP : B_AREADY), 0, p.status, 256);   // a of chunk 0
     if (ok) {
         copy_and_decay<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
         tmem_wait_st();
@@ -378,21 +403,26 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         named_bar_sync(2, 128);
     }
 
+    int sc = 0, kq = 0;   // (cluster home) slot c % NS and round c / NS
 #pragma unroll 1
     for (int c = 0; ok && c < u.nchunks; ++c) {
-        const int s = c & 1;
-        const uint32_t cpar = c & 1, kpar = (c >> 1) & 1;
-        const uint32_t slot = u.base + s * SLOT_BYTES;
+        const int s = kCl ? sc : (c & 1);
+        const uint32_t cpar = c & 1, kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
+        const uint32_t soff = kCl ? slot_off(s) : s * SLOT_BYTES;
+        const uint32_t slot = u.base + soff;
 
         // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T and P -= V^T, once the prep warps wrote the
         // chunk's operands and its v box landed
-        const bool refill = c + NSLOT < u.nchunks;
-        if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
-        // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
-        if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) break;
-        // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
-        const float beta_next = beta_ahead;
-        if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
+        const bool refill = c + NS < u.nchunks;
+        float beta_next = 0.f;
+        if constexpr (!kCl) {
+            if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
+            // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
+            if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) break;
+            // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
+            beta_next = beta_ahead;
+            if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
+        }
         if (w == W_MMA) {
             if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) break;
             tc_fence_after();
@@ -418,8 +448,10 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
         p_cols_to_bf16(lane_addr);
-        if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) break;
-        if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
+        if constexpr (!kCl) {
+            if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) break;
+            if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
+        }
         tc_fence_before();
         named_bar_sync(2, 128);
         if (w == W_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
@@ -465,11 +497,16 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) break;
         tc_fence_after();
 
-        // The slot's q, k, g regions have been read for the last time: refill them with
-        // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
-        if (refill) {
-            if (pt == T_TMA) load_qkg(maps, u, c + NSLOT);
-            issued = c + NSLOT + 1;
+        if constexpr (kCl) {
+            // the slot's pulled operands have been read for the last time
+            if (pt == 0) mbar_arrive(bar_addr(u, B_HFREE + s));
+        } else {
+            // The slot's q, k, g regions have been read for the last time: refill them with
+            // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
+            if (refill) {
+                if (pt == T_TMA) load_qkg(maps, u, c + NSLOT, s);
+                issued = c + NSLOT + 1;
+            }
         }
 
         // O of this chunk -> staging tile [token][v] in the slot's v region (GEMM1 has read
@@ -502,7 +539,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 }
             }
         } else {
-            unsigned char* ost = u.gbase + s * SLOT_BYTES + SL_V + 2 * v;
+            unsigned char* ost = u.gbase + soff + SL_V + 2 * v;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 uint32_t o[16];
@@ -534,13 +571,19 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             bulk_commit();
         }
 
+        const int s1 = kCl ? (s + 1 == NS ? 0 : s + 1) : (s ^ 1);
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
-            if (!warp_wait(bar_addr(u, B_AREADY + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 256)) break;
+            if constexpr (kCl) {
+                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) break;
+            } else {
+                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) break;
+            }
+            const float* a_next = reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A);
             if constexpr (kWarpIssue)
-                copy_and_decay_pipelined<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
+                copy_and_decay_pipelined<kBf16State>(lane_addr, a_next);
             else
-                copy_and_decay<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
+                copy_and_decay<kBf16State>(lane_addr, a_next);
             tmem_wait_st();
             tc_fence_before();
             named_bar_sync(2, 128);
@@ -548,7 +591,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             // region takes chunk c + 2's v
             if (pt == T_STORE && refill) {
                 bulk_wait_read_all();
-                load_v(maps, u, c + NSLOT);
+                load_v(maps, u, c + NS, s);
+                vissued = c + NS + 1;
             }
         } else {
 #pragma unroll 1
@@ -559,9 +603,17 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 store_state16(p, srow + piece * 16, r);
             }
         }
+        if constexpr (kCl) {
+            sc = s1;
+            if (s1 == 0) ++kq;
+        }
     }
     if (pt == T_STORE) bulk_wait_all();   // the output must be in global memory before the kernel ends
-    if (pt == T_TMA || pt == T_STORE) {
+    if constexpr (kCl) {
+        if (pt == T_STORE)   // v boxes still in flight (only after a timeout can one be unconsumed)
+            for (int c = vissued - NS < 0 ? 0 : vissued - NS; c < vissued; ++c)
+                mbar_wait_bounded(bar_addr(u, B_FULLV + c % NS), (c / NS) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+    } else if (pt == T_TMA || pt == T_STORE) {
         // boxes still in flight must land before the CTA exits (only after a timeout can
         // one be unconsumed)
         const int b0 = pt == T_TMA ? B_FULLTMA : B_FULLV;
@@ -575,8 +627,10 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 // Elementwise phases: thread = (channel quad: channels 4 lane .. 4 lane + 3,
 // token quad: tokens 4 pw .. 4 pw + 3), pw = warp index within the group.
 // ------------------------------------------------------------------------------
-template <bool kSoftplus>
-__device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
+// The group prepares the chunks c = c_first + kStride j, j < nloc, in its slots j % 2 (all
+// of them, or one helper's share in the cluster schedule).
+template <bool kSoftplus, int kStride>
+__device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_first, int nloc) {
     const int lane = pt & 31, pw = pt >> 5, gq = lane >> 2, tq = lane & 3;
     const int c0 = 4 * lane;
     // phase B store offsets of token 4 pw (channels c0 .. c0 + 3); token 4 pw + r differs by one XOR:
@@ -607,9 +661,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
     float* rk = rq + 32;
 
 #pragma unroll 1
-    for (int c = 0; c < u.nchunks; ++c) {
-        const int s = c & 1;
-        const uint32_t kpar = (c >> 1) & 1;
+    for (int j = 0; j < nloc; ++j) {
+        const int c = c_first + kStride * j;
+        const int s = j & 1;
+        const uint32_t kpar = (j >> 1) & 1;
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
         if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) return;
         const int64_t t0 = u.bos + (int64_t)c * CH;
@@ -795,7 +850,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[t][e] += acc2[t][e];
                 // L is rewritten only once the inverse warp has read the previous chunk's
-                if (mat == 0 && c > 0 && !warp_wait(bar_addr(u, B_LFREE), (c - 1) & 1, p.status)) return;
+                if (mat == 0 && j > 0 && !warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status)) return;
             }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
@@ -836,7 +891,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
 // ------------------------------------------------------------------------------
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return (uint16_t)(pack_bf16x2(x, 0.f) & 0xffffu); }
 
-__device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
+__device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nloc) {   // nloc: as the prep group's
     const int gq = lane >> 2, tq = lane & 3;
     const int b = lane >> 4, cc = lane & 15;   // substitution: block b, column cc
     const float* Lb = reinterpret_cast<const float*>(u.gbase + OFF_L);
@@ -847,9 +902,9 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
             make_uint4(0, 0, 0, 0);
 
 #pragma unroll 1
-    for (int c = 0; c < u.nchunks; ++c) {
-        const int s = c & 1;
-        const uint32_t kpar = (c >> 1) & 1;
+    for (int j = 0; j < nloc; ++j) {
+        const int s = j & 1;
+        const uint32_t kpar = (j >> 1) & 1;
         unsigned char* b2s = u.gbase + s * SLOT_BYTES + SL_INV;
         const float* bs = reinterpret_cast<const float*>(u.gbase + s * SLOT_BYTES + SL_BETA);
         if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 128)) return;
@@ -953,34 +1008,112 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane) {
     }
 }
 
+// ------------------------------------------------------------------------------
+// Cluster schedule.  Chunk c is prepared by helper h = c % NHELP as its chunk j = c / NHELP,
+// in its slot j % 2, and pulled into home slot h.  Every barrier that one side completes for
+// the other has one instance per slot, so no wait can see a phase two ahead of its own.
+// ------------------------------------------------------------------------------
+
+// Home CTA, warps 4-11: once helper h has finished chunk c (READY) and the chain is done
+// with the chunk before it in home slot h (HFREE), copy the chunk's operands from the
+// helper's shared memory into the slot (16-byte distributed shared-memory loads, 7 or 8 a
+// thread, all in flight at once), then tell the chain (FULLOP) and the helper (COPIED).
+__device__ void home_puller(const FwdParams& p, const Unit& u, int pt) {
+    constexpr int PER = (PULL_VECS + PREP_THREADS - 1) / PREP_THREADS;
+#pragma unroll 1
+    for (int c = 0; c < u.nchunks; ++c) {
+        const int h = c % NHELP, j = c / NHELP, b = j & 1;
+        bool ok = j == 0 || mbar_wait_bounded(bar_addr(u, B_HFREE + h), (j - 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
+                                              WAIT_LIMIT, 256);
+        ok = ok && mbar_wait_bounded<true>(bar_addr(u, B_READY + 2 * h + b), (j >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
+                                           WAIT_LIMIT, 256);
+        if (!named_bar_all(1, PREP_THREADS, ok)) return;   // one verdict for the group: no thread is left at a barrier
+        const uint32_t src = mapa_shared(u.base + b * SLOT_BYTES, (uint32_t)(h + 1));
+        unsigned char* dst = u.gbase + slot_off(h);
+        uint4 x[PER];
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = pt + PREP_THREADS * i;
+            const uint32_t off = e < PULL_VECS_A ? 16u * e : SL_MQT + 16u * (e - PULL_VECS_A);
+            if (e < PULL_VECS) x[i] = ld_dsmem_v4(src + off);
+        }
+#pragma unroll
+        for (int i = 0; i < PER; ++i) {
+            const int e = pt + PREP_THREADS * i;
+            const uint32_t off = e < PULL_VECS_A ? 16u * e : SL_MQT + 16u * (e - PULL_VECS_A);
+            if (e < PULL_VECS) *reinterpret_cast<uint4*>(dst + off) = x[i];
+        }
+        fence_proxy_async_smem();   // the operands are read by the tensor core
+        named_bar_sync(1, PREP_THREADS);
+        if (pt == 0) {
+            mbar_arrive(bar_addr(u, B_FULLOP + h));
+            mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + b), (uint32_t)(h + 1)));
+        }
+    }
+}
+
+// Helper CTA, warps 0-3: warp 2 loads the q, k, g boxes (lane 0) and beta of the helper's
+// chunks into its two slots, the slot of chunk j once the home CTA has pulled chunk j - 2;
+// lane 0 of warp 3 tells the home CTA when the prep and inverse warps have finished a chunk.
+template <bool kBetaLogit>
+__device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt, int h, int nloc) {
+    const int w = pt >> 5, lane = pt & 31;
+    if (w == W_BETA) {
+        int loaded = 0;
+#pragma unroll 1
+        for (int j = 0; j < nloc; ++j) {
+            const int c = h + NHELP * j, b = j & 1;
+            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded<true>(bar_addr(u, B_COPIED + b), ((j - 2) >> 1) & 1,
+                                                                            p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)))
+                break;
+            if (lane == 0) load_qkg(maps, u, c, b);
+            put_beta(u, b, lane, load_beta<kBetaLogit>(p, u, c, lane));
+            loaded = j + 1;
+        }
+        // boxes still in flight must land before the CTA exits (only after a timeout can one
+        // be unconsumed)
+        if (lane == 0)
+            for (int j = loaded - 2 < 0 ? 0 : loaded - 2; j < loaded; ++j)
+                mbar_wait_bounded(bar_addr(u, B_FULLTMA + (j & 1)), (j >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+    } else if (pt == T_STORE) {
+#pragma unroll 1
+        for (int j = 0; j < nloc; ++j) {
+            const int b = j & 1;
+            const uint32_t par = (j >> 1) & 1;
+            if (!mbar_wait_bounded(bar_addr(u, B_FULLP + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
+            if (!mbar_wait_bounded(bar_addr(u, B_FULLD + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
+            fence_acq_rel_cluster();   // the prep and inverse warps' writes, for the home CTA's loads
+            mbar_arrive_remote(mapa_shared(bar_addr(u, B_READY + 2 * h + b), 0u));
+        }
+    }
+}
+
 // kWarpIssue: the instantiation for one CTA per SM (warp-wide MMA issue, pipelined state
 // pass, and the register file to itself: up to 128 registers a thread instead of 72).
-template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit>
+// kCl: the cluster schedule (one CTA per SM too).
+template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit, bool kCl = false>
 __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+    const int rank = kCl ? (int)cluster_ctarank() : 0;   // 0: the home CTA
+    const bool home = rank == 0;
     Unit u;
     {
         const uint32_t raw = smem_u32(smem_raw);
         u.base = (raw + 1023u) & ~1023u;
         u.gbase = smem_raw + (u.base - raw);
-        u.h = blockIdx.x % p.H;
-        const int r = blockIdx.x / p.H;
+        const int unit = kCl ? (int)(blockIdx.x / CL_SIZE) : (int)blockIdx.x;
+        u.h = unit % p.H;
+        const int r = unit / p.H;
         u.n = p.order ? p.order[r] : r;
         seq_range(p, u.n, u.bos, u.eos);
         u.nchunks = (int)((u.eos - u.bos + CH - 1) / CH);
     }
     if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) {
-            mbar_init(bar_addr(u, B_FULLTMA + s), 33);
-            mbar_init(bar_addr(u, B_FULLV + s), 1);
-            mbar_init(bar_addr(u, B_AREADY + s), 1);
-            mbar_init(bar_addr(u, B_FULLP + s), 1);
-            mbar_init(bar_addr(u, B_FULLD + s), 1);
-        }
-        for (int b = B_LFREE; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
+        for (int s = 0; s < NSLOT; ++s) mbar_init(bar_addr(u, B_FULLTMA + s), 33);
+        for (int b = B_FULLV; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
         mbar_fence_init();
     }
     if (tid == 32) {
@@ -990,29 +1123,43 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         tma_prefetch_desc(&maps.g);
         tma_prefetch_desc(&maps.out);
     }
-    if (warp == 0) {
+    if (warp == 0 && home) {
         tmem_alloc(u.base + OFF_TMEMADDR, TM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    u.tmem = *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR);
+    if constexpr (kCl) cluster_sync_all();   // every CTA's barriers are initialised before a peer arrives on one
+    u.tmem = home ? *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR) : 0u;
 
-    if (warp < W_PREP0) {
-        chain_group<kBf16State, kWarpIssue, kBetaLogit>(p, maps, u, tid);
-    } else if (warp < W_INV) {
-        prep_group<kSoftplus>(p, u, tid - W_PREP0 * 32);
+    if constexpr (!kCl) {
+        if (warp < W_PREP0) {
+            chain_group<kBf16State, kWarpIssue, kBetaLogit, false>(p, maps, u, tid);
+        } else if (warp < W_INV) {
+            prep_group<kSoftplus, 1>(p, u, tid - W_PREP0 * 32, 0, u.nchunks);
+        } else {
+            inverse_warp(p, u, tid & 31, u.nchunks);
+        }
+    } else if (home) {
+        if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
+        else if (warp < W_INV) home_puller(p, u, tid - W_PREP0 * 32);
     } else {
-        inverse_warp(p, u, tid & 31);
+        const int h = rank - 1;
+        const int nloc = u.nchunks > h ? (u.nchunks - h + NHELP - 1) / NHELP : 0;
+        if (warp < W_PREP0) helper_io<kBetaLogit>(p, maps, u, tid, h, nloc);
+        else if (warp < W_INV) prep_group<kSoftplus, NHELP>(p, u, tid - W_PREP0 * 32, h, nloc);
+        else inverse_warp(p, u, tid & 31, nloc);
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 0 && home) {
         tc_fence_after();
         tmem_dealloc(u.tmem, TM_COLS);
     }
+    // no CTA leaves while a peer may still read its shared memory or arrive on its barriers
+    if constexpr (kCl) cluster_sync_all();
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
@@ -1046,9 +1193,61 @@ bool encode_tokens_map(CUtensorMap* m, const void* ptr, int64_t T_total, int H, 
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+using Kernel = void (*)(const FwdParams, const TmaMaps);
+
+// The cluster instantiation for the flags, with its launch configuration (the attribute
+// array must outlive the configuration's use).
+Kernel cluster_config(uint32_t flags, long long units, cudaStream_t stream, cudaLaunchAttribute* attr,
+                      cudaLaunchConfig_t* cfg) {
+    static constexpr Kernel table_cl[2][2] = {   // [softplus][beta logit]
+        {kda_fwd_tc_kernel<false, true, false, false, true>, kda_fwd_tc_kernel<false, true, false, true, true>},
+        {kda_fwd_tc_kernel<false, true, true, false, true>, kda_fwd_tc_kernel<false, true, true, true, true>}};
+    const Kernel ck = table_cl[(flags & KDA_FLAG_GATE_SOFTPLUS) != 0][(flags & KDA_FLAG_BETA_LOGIT) != 0];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL_SIZE;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3((unsigned)(units * CL_SIZE));
+    cfg->blockDim = dim3(TC_THREADS);
+    cfg->dynamicSmemBytes = SMEM_BYTES_CL;
+    cfg->stream = stream;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+    return ck;
+}
+
 }  // namespace
 
 size_t fwd_tc_smem_bytes() { return SMEM_BYTES; }
+
+// One CTA per unit, two on an SM, when the units outnumber the SMs; one CTA per unit with an
+// SM to itself up to one unit per SM; with at most a quarter as many units as SMs, a cluster
+// of four CTAs per unit, if every cluster can be resident at once (clusters must fit the
+// GPCs).  The bf16-state ablation keeps its one instantiation.
+cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, int* sched) {
+    *sched = KDA_SCHEDULE_TWO_PER_SM;
+    if (bf16_state || units <= 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (units > sms) return cudaSuccess;
+    *sched = KDA_SCHEDULE_ONE_PER_SM;
+    if (units * CL_SIZE > sms) return cudaSuccess;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg;
+    const Kernel ck = cluster_config(flags, units, nullptr, attr, &cfg);
+    e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_CL);
+    if (e != cudaSuccess) return e;
+    int resident = 0;
+    if (cudaOccupancyMaxActiveClusters(&resident, ck, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();   // no cluster schedule on this device
+        return cudaSuccess;
+    }
+    if (resident >= units) *sched = KDA_SCHEDULE_CLUSTER;
+    return cudaSuccess;
+}
 
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state) {
     const int units = p.nseq * p.H;
@@ -1058,22 +1257,27 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
         !encode_tokens_map(&maps.v, p.v, p.T_total, p.H, true) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
         !encode_tokens_map(&maps.out, p.out, p.T_total, p.H, true))
         return cudaErrorInvalidValue;
-    // one CTA per SM when the units fit the SMs: the chain then issues its MMAs warp-wide
-    // (the bf16-state ablation keeps the single-thread issue)
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 0;
-    // (the interface variants are separate instantiations, so the default one is unchanged)
-    const bool lone = units <= sms, sp = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
+    int sched = KDA_SCHEDULE_TWO_PER_SM;
+    cudaError_t e = fwd_tc_schedule(units, p.flags, bf16_state, &sched);
+    if (e != cudaSuccess) return e;
+    if (sched == KDA_SCHEDULE_CLUSTER) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg;
+        const Kernel ck = cluster_config(p.flags, units, stream, attr, &cfg);
+        e = cudaLaunchKernelEx(&cfg, ck, p, maps);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
+    // one CTA per SM: the chain issues its MMAs warp-wide (the interface variants are
+    // separate instantiations, so the default one is unchanged)
+    const bool lone = sched == KDA_SCHEDULE_ONE_PER_SM, sp = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
     const bool lg = (p.flags & KDA_FLAG_BETA_LOGIT) != 0;
-    using Kernel = void (*)(const FwdParams, const TmaMaps);
     static constexpr Kernel table[2][2][2] = {   // [lone][softplus][beta logit]
         {{kda_fwd_tc_kernel<false, false, false, false>, kda_fwd_tc_kernel<false, false, false, true>},
          {kda_fwd_tc_kernel<false, false, true, false>, kda_fwd_tc_kernel<false, false, true, true>}},
         {{kda_fwd_tc_kernel<false, true, false, false>, kda_fwd_tc_kernel<false, true, false, true>},
          {kda_fwd_tc_kernel<false, true, true, false>, kda_fwd_tc_kernel<false, true, true, true>}}};
     auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false, false, false> : table[lone][sp][lg];
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
     return cudaGetLastError();

@@ -27,6 +27,9 @@ size_t fwd_mma_smem_bytes();
 // rounds the carried state to bf16 at every chunk boundary: the state-precision ablation.
 cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state = false);
 size_t fwd_tc_smem_bytes();
+// The KDA_SCHEDULE_* a launch of the tensor-core kernel over `units` units takes on the
+// current device.
+cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, int* sched);
 
 // The same with 16-token chunks and no exponent anchor: the chunk-size ablation.
 cudaError_t launch_fwd_tc16(const FwdParams& p, cudaStream_t stream);

@@ -89,27 +89,47 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
 }
 // Test the phase with `parity`; while it is pending the thread may be suspended for up
 // to the hint (ns), so waiting warps leave the issue slots to the working ones.
+// kCluster: acquire at cluster scope, for a phase that threads of another CTA of the
+// cluster complete (their prior accesses become visible to this thread).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(1000000u)
-        : "memory");
+    if constexpr (kCluster)
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(1000000u)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity), "r"(1000000u)
+            : "memory");
     return ok != 0;
 }
 
 // Non-blocking test of the phase with `parity`: on GB300 about 55 cycles when it has
 // completed, against about 90 for try_wait with a suspend hint.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if constexpr (kCluster)
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return ok != 0;
 }
 
@@ -117,13 +137,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 // cycles.  Returns false (and sets `status_bit` in *status) when the limit expires.
 // With max_sleep_ns > 0 the thread backs off between polls (exponentially, up to
 // that many ns), for waits that are long and off the critical path.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t* status,
                                                   uint32_t status_bit, long long limit,
                                                   uint32_t max_sleep_ns = 0) {
-    if (mbar_test_wait(bar, parity)) return true;   // completed: no suspend hint on the fast path
+    if (mbar_test_wait<kCluster>(bar, parity)) return true;   // completed: no suspend hint on the fast path
     const long long t0 = clock64();
     uint32_t ns = 16;
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait<kCluster>(bar, parity)) {
         if (clock64() - t0 > limit) {
             atomicOr(status, status_bit);
             return false;
@@ -173,6 +194,39 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];\n" ::"l"(tmap) : "memory");
 }
 
+// ------------------------------- cluster -----------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of shared-window address `addr` in CTA `rank` of the cluster
+// (the CTAs of one kernel share the dynamic shared-memory layout).
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+// 16 bytes of another CTA's shared memory (distributed shared memory).
+__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t cluster_addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+// Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior
+// accesses at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;\n" ::: "memory"); }
+// Every thread of every CTA of the cluster (all must call it).
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor-core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -182,6 +236,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+// Named barrier over `count` threads that also returns the AND of their `pred`: a verdict
+// every participant shares.
+__device__ __forceinline__ bool named_bar_all(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 // Arrive on a named barrier without waiting (the producer side of a bar.sync consumer).
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {

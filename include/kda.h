@@ -134,6 +134,24 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
                       const kda_tensor* final_state, const kda_tensor* cu_seqlens,
                       void* workspace, size_t workspace_bytes, uint32_t flags, kda_stream_t stream);
 
+/*
+ * The launch schedule the default (tensor-core) kernel of kda_fwd / kda_fwd_ex takes on the
+ * current device for `units`
+ * (sequence, head) units (sequences x H) with `flags`, written to *schedule:
+ *   KDA_SCHEDULE_TWO_PER_SM  one CTA per unit, two CTAs sharing each SM (more units than SMs)
+ *   KDA_SCHEDULE_ONE_PER_SM  one CTA per unit with an SM to itself (up to one unit per SM)
+ *   KDA_SCHEDULE_CLUSTER     a cluster of four CTAs per unit: one runs the recurrence, three
+ *                            prepare its chunks (up to a quarter as many units as SMs, when
+ *                            every cluster can be resident at once)
+ * A unit's arithmetic is the same in every schedule: outputs and states do not depend on it.
+ * Returns KDA_ERR_INVALID_ARG for units < 0, unknown flag bits or a null `schedule`, and
+ * KDA_ERR_CUDA when the device cannot be queried.
+ */
+#define KDA_SCHEDULE_TWO_PER_SM 0
+#define KDA_SCHEDULE_ONE_PER_SM 1
+#define KDA_SCHEDULE_CLUSTER    2
+kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule);
+
 /* Static description of a status code. */
 const char* kda_status_string(kda_status s);
 

@@ -190,3 +190,11 @@ def test_decode_rejects_before_enqueueing(lib):
     for over, expect in cases:
         got = call_dec(**over)
         assert got == expect, (over, got, lib.kda_last_error())
+
+
+def test_schedule_query_rejects_before_touching_the_device(lib):
+    sched = ctypes.c_int32(-1)
+    assert lib.kda_fwd_schedule(-1, 0, ctypes.byref(sched)) == kb.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_schedule(8, 0x4, ctypes.byref(sched)) == kb.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_schedule(8, 0, None) == kb.KDA_ERR_INVALID_ARG
+    assert sched.value == -1

@@ -1,0 +1,134 @@
+"""The launch schedules of the prefill kernel, and that they do not change the numbers.
+
+More (sequence, head) units than SMs run two CTAs to an SM; up to one unit per SM, one CTA
+per SM; up to a quarter as many units as SMs, a cluster of four CTAs per unit (one CTA runs
+the recurrence over state resident in its Tensor Memory, three prepare chunks for it and
+hand them over through distributed shared memory).  A unit's arithmetic is the same in each,
+so the same sequences must give bit-identical outputs and final states whichever schedule
+their launch takes.  The cluster and one-CTA-per-SM launches are also compared with the
+oracle over whole tensors, at and around the unit counts where the schedule changes.
+"""
+import pytest
+import torch
+
+from gated_delta_rule_36_gb300 import binding as kb
+from gated_delta_rule_36_gb300.inputs import Workload, make_inputs
+
+from kda_testutil import check_full, oracle_full, run_gpu
+
+pytestmark = pytest.mark.gpu
+f32, bf16 = torch.float32, torch.bfloat16
+
+
+def _sms():
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+def _cluster_max():
+    """The most units that still take the cluster schedule (every cluster resident at once)."""
+    u = _sms() // 4
+    while u > 0 and kb.kda_fwd_schedule(u) != kb.KDA_SCHEDULE_CLUSTER:
+        u -= 1
+    return u
+
+
+def _prefix(inp, nseq):
+    """The first `nseq` sequences of a packed input, as a packed input of their own."""
+    w = inp.w
+    lens = list(w.seq_lens[:nseq])
+    T = int(sum(lens))
+    sw = Workload(w.name + f"_first{nseq}", w.seed, H=w.H, B=1, T=T, seq_lens=lens, init_dtype=w.init_dtype,
+                  final_dtype=w.final_dtype, lower_bound=w.lower_bound)
+    sub = make_inputs(sw, "cpu")   # shapes and scalars; the tensors are replaced below
+    for name in ("q", "k", "v", "g", "beta"):
+        setattr(sub, name, getattr(inp, name)[:, :T].clone())
+    sub.A_log, sub.dt_bias = inp.A_log.clone(), inp.dt_bias.clone()
+    sub.scale, sub.lower_bound = inp.scale, inp.lower_bound
+    sub.initial_state = None if inp.initial_state is None else inp.initial_state[:nseq].clone()
+    sub.cu_seqlens = inp.cu_seqlens[: nseq + 1].clone()
+    return sub
+
+
+def _lens(n, seed):
+    gen = torch.Generator().manual_seed(seed)
+    lens = [int(x) for x in torch.randint(1, 260, (n,), generator=gen)]
+    lens[1] = 0            # an empty sequence
+    lens[2] = 32           # exactly one chunk
+    lens[3] = 65           # three chunks, the last of one token: every helper has work
+    return lens
+
+
+def test_schedule_thresholds():
+    sms, cmax = _sms(), _cluster_max()
+    print(f"[schedule] SMs {sms}, cluster schedule up to {cmax} units")
+    assert 1 <= cmax <= sms // 4
+    want = lambda u: (kb.KDA_SCHEDULE_CLUSTER if u <= cmax else
+                      kb.KDA_SCHEDULE_ONE_PER_SM if u <= sms else kb.KDA_SCHEDULE_TWO_PER_SM)
+    for u in sorted({1, 2, cmax, cmax + 1, sms // 4 + 1, sms - 1, sms, sms + 1, 4 * sms}):
+        assert kb.kda_fwd_schedule(u) == want(u), u
+    assert kb.kda_fwd_schedule(0) == kb.KDA_SCHEDULE_TWO_PER_SM
+    for flags in (kb.KDA_FLAG_BETA_LOGIT, kb.KDA_FLAG_GATE_SOFTPLUS):
+        assert kb.kda_fwd_schedule(cmax, flags) == kb.KDA_SCHEDULE_CLUSTER
+
+
+def test_schedules_give_identical_numbers():
+    """The first sequences of one packed input alone (the cluster schedule), with more
+    sequences (one CTA per SM), and with more again (two CTAs per SM)."""
+    H, sms, cmax = 4, _sms(), _cluster_max()
+    n_cl = min(6, cmax // H)
+    n_one = cmax // H + 1                        # just past the cluster schedule
+    n_two = sms // H + 1                         # past one unit per SM
+    lens = _lens(n_two, 81)
+    w = Workload("sched_same", 81, H=H, B=1, T=int(sum(lens)), seq_lens=lens, init_dtype=f32, final_dtype=f32)
+    inp = make_inputs(w, "cpu")
+    runs = {}
+    for nseq in (n_cl, n_one, n_two):
+        sub = _prefix(inp, nseq)
+        runs[nseq] = (kb.kda_fwd_schedule(nseq * H),) + run_gpu(sub)
+    assert [runs[n][0] for n in (n_cl, n_one, n_two)] == [kb.KDA_SCHEDULE_CLUSTER, kb.KDA_SCHEDULE_ONE_PER_SM,
+                                                          kb.KDA_SCHEDULE_TWO_PER_SM]
+    T_cl = int(sum(lens[:n_cl]))
+    _, out_cl, fin_cl, bits_cl = runs[n_cl]
+    assert bits_cl == 0
+    for nseq in (n_one, n_two):
+        _, out, fin, bits = runs[nseq]
+        assert bits == 0
+        torch.testing.assert_close(out[:, :T_cl].cpu(), out_cl.cpu(), rtol=0, atol=0, equal_nan=True)
+        torch.testing.assert_close(fin[:n_cl].cpu(), fin_cl.cpu(), rtol=0, atol=0)
+
+
+@pytest.mark.parametrize("units_kind", ["cluster_max", "one_per_sm_min", "one_per_sm"])
+def test_schedule_against_oracle(units_kind):
+    H, cmax = 1, _cluster_max()
+    nseq = {"cluster_max": cmax, "one_per_sm_min": cmax + 1, "one_per_sm": 100}[units_kind]
+    lens = _lens(nseq, 82)
+    w = Workload("sched_" + units_kind, 82, H=H, B=1, T=int(sum(lens)), seq_lens=lens, init_dtype=bf16,
+                 final_dtype=f32)
+    inp = make_inputs(w, "cpu")
+    want = kb.KDA_SCHEDULE_CLUSTER if units_kind == "cluster_max" else kb.KDA_SCHEDULE_ONE_PER_SM
+    assert kb.kda_fwd_schedule(w.units) == want
+    out, final, bits = run_gpu(inp)
+    assert bits == 0
+    ref_out, ref_final = oracle_full(inp)
+    check_full(inp, out, final, ref_out, ref_final)
+
+
+def test_cluster_schedule_long_sequences_and_variants():
+    """One long sequence per head (many rounds of the three-slot ring), every flag."""
+    from oracle import kda_oracle as O
+    from kda_testutil import assert_close
+    w = Workload("sched_long", 83, H=3, B=1, T=1000, seq_lens=[1000], init_dtype=f32, final_dtype=f32)
+    inp = make_inputs(w, "cpu")
+    assert kb.kda_fwd_schedule(w.units) == kb.KDA_SCHEDULE_CLUSTER
+    for kflag, oflag in ((0, 0), (kb.KDA_FLAG_BETA_LOGIT | kb.KDA_FLAG_GATE_SOFTPLUS, O.BETA_LOGIT | O.GATE_SOFTPLUS)):
+        ref_out, ref_final = O.kda_oracle_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.scale, inp.A_log,
+                                              inp.dt_bias, inp.lower_bound, initial_state=inp.initial_state,
+                                              cu_seqlens=inp.cu_seqlens, flags=oflag)
+        d = inp.to(torch.device("cuda"))
+        out = torch.zeros_like(d.q)
+        final = torch.empty((1, w.H, 128, 128), dtype=f32, device="cuda")
+        ws = kb.kda_fwd(d.q, d.k, d.v, d.g, d.beta, d.scale, out, d.A_log, d.dt_bias, d.lower_bound,
+                        initial_state=d.initial_state, final_state=final, cu_seqlens=d.cu_seqlens, flags=kflag)
+        assert kb.kda_read_device_status(ws) == 0
+        assert_close("cluster out", out.double().cpu().numpy(), ref_out, bf16)
+        assert_close("cluster state", final.double().cpu().numpy(), ref_final, f32)
