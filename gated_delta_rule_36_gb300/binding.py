@@ -24,9 +24,11 @@ HEAD_DIM = 128
 # Every function include/kda.h declares.
 EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_error",
             "kda_read_device_status", "kda_fwd_no_alloc", "kda_fwd_host_device_bytes", "kda_fwd_host",
-            "kda_fwd_host_workspace_offset", "kda_decode", "kda_fwd_ex", "kda_decode_ex", "kda_fwd_schedule")
+            "kda_fwd_host_workspace_offset", "kda_decode", "kda_fwd_ex", "kda_decode_ex", "kda_fwd_schedule",
+            "kda_fwd_set_trace")
 KDA_FLAG_BETA_LOGIT, KDA_FLAG_GATE_SOFTPLUS = 0x1, 0x2
 KDA_SCHEDULE_TWO_PER_SM, KDA_SCHEDULE_ONE_PER_SM, KDA_SCHEDULE_CLUSTER = 0, 1, 2
+KDA_TRACE_POINTS = 8
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
 
@@ -71,6 +73,8 @@ def load(path: Optional[str] = None):
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_last_error.argtypes = []
+        lib.kda_fwd_set_trace.restype = ctypes.c_int
+        lib.kda_fwd_set_trace.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64]
         lib.kda_fwd_schedule.restype = ctypes.c_int
         lib.kda_fwd_schedule.argtypes = [ctypes.c_int64, ctypes.c_uint32, ctypes.POINTER(ctypes.c_int32)]
         lib.kda_read_device_status.restype = ctypes.c_int
@@ -254,6 +258,20 @@ def kda_decode(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initia
     else:
         st = lib.kda_decode(*args, ctypes.c_void_p(sh))
     _check(lib, st)
+
+
+def kda_fwd_set_trace(buffer=None, unit: int = 0) -> None:
+    """Record the chain trace of (sequence, head) unit ``unit`` (sequence * H + head) into
+    ``buffer`` (a CUDA int64 tensor of [chunks, KDA_TRACE_POINTS]) on later forward launches
+    of this thread that take the cluster schedule; ``None`` turns it off."""
+    lib = load()
+    if buffer is None:
+        _check(lib, lib.kda_fwd_set_trace(None, 0, 0))
+        return
+    if not (isinstance(buffer, torch.Tensor) and buffer.is_cuda and buffer.is_contiguous()):
+        raise KDAError(KDA_ERR_INVALID_ARG, "trace buffer must be a contiguous CUDA tensor")
+    _check(lib, lib.kda_fwd_set_trace(ctypes.c_void_p(buffer.data_ptr()), buffer.numel() * buffer.element_size(),
+                                      int(unit)))
 
 
 def kda_fwd_schedule(units: int, flags: int = 0) -> int:

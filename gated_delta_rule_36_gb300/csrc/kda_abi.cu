@@ -13,6 +13,9 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+// kda_fwd_set_trace settings of this host thread
+thread_local unsigned long long* g_trace = nullptr;
+thread_local int64_t g_trace_chunks = 0, g_trace_unit = 0;
 
 kda_status fail(kda_status s, const char* fmt, ...) {
     va_list ap;
@@ -221,6 +224,9 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
     p.scale = scale;
     p.lower_bound = lower_bound;
     p.flags = flags;
+    p.trace = g_trace;
+    p.trace_chunks = g_trace_chunks;
+    p.trace_unit = g_trace_unit;
 
     // KDA_FWD_KERNEL selects an ablation variant: "mma" keeps the state in mma.sync
     // registers, "tc16" uses 16-token chunks without the exponent anchor, "tcbf16" rounds
@@ -315,6 +321,21 @@ kda_status kda_decode_ex(const kda_tensor* q, const kda_tensor* k, const kda_ten
     p.lower_bound = lower_bound;
     const cudaError_t e = kda::launch_decode(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return KDA_OK;
+}
+
+kda_status kda_fwd_set_trace(void* device_buffer, size_t bytes, int64_t unit) {
+    if (device_buffer == nullptr) {
+        g_trace = nullptr;
+        g_trace_chunks = 0;
+        return KDA_OK;
+    }
+    const size_t per_chunk = 8u * KDA_TRACE_POINTS;
+    if (((uintptr_t)device_buffer) % 8 != 0 || bytes < per_chunk || unit < 0)
+        return fail(KDA_ERR_INVALID_ARG, "trace buffer must be 8-byte aligned and hold a chunk; unit >= 0");
+    g_trace = static_cast<unsigned long long*>(device_buffer);
+    g_trace_chunks = (int64_t)(bytes / per_chunk);
+    g_trace_unit = unit;
     return KDA_OK;
 }
 

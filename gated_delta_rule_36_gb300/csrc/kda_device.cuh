@@ -40,6 +40,11 @@ struct FwdParams {
     float scale;
     float lower_bound;
     uint32_t flags;           // KDA_FLAG_* interface variants
+    // chain trace (kda_fwd_set_trace): KDA_TRACE_POINTS SM clock readings per chunk of unit
+    // trace_unit (sequence * H + head), chunks below trace_chunks; nullptr = off
+    unsigned long long* trace;
+    int64_t trace_chunks;
+    int64_t trace_unit;
 };
 
 // Token range [bos, eos) of sequence n, clamped to [0, T_total].

@@ -33,6 +33,8 @@
 // between GEMM1 and GEMM3.
 #include <cuda.h>
 
+#include <atomic>
+
 #include "kda_device.cuh"
 #include "kda_kernels.h"
 #include "kda_sm100.cuh"
@@ -404,9 +406,15 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     }
 
     int sc = 0, kq = 0;   // (cluster home) slot c % NS and round c / NS
+    // chain trace (cluster schedule): SM clock at KDA_TRACE_POINTS steps of each chunk of one unit
+    const bool trace_me = kCl && p.trace != nullptr && (int64_t)u.n * p.H + u.h == p.trace_unit;
+    auto stamp = [&](int c, int i) {
+        if (trace_me && c < p.trace_chunks) p.trace[(size_t)c * KDA_TRACE_POINTS + i] = (unsigned long long)clock64();
+    };
 #pragma unroll 1
     for (int c = 0; ok && c < u.nchunks; ++c) {
         const int s = kCl ? sc : (c & 1);
+        if (kCl && pt == 0) stamp(c, 0);
         const uint32_t cpar = c & 1, kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
         const uint32_t soff = kCl ? slot_off(s) : s * SLOT_BYTES;
         const uint32_t slot = u.base + soff;
@@ -424,8 +432,10 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
         }
         if (w == W_MMA) {
+            if (kCl && pt == 32) stamp(c, 1);
             if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) break;
             tc_fence_after();
+            if (kCl && pt == 32) stamp(c, 2);
             auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
             auto av = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024); };
             auto bv = [&](int kk) { return make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512); };
@@ -435,6 +445,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // P -= V^T
                 tc_commit_warp(bar_addr(u, B_G1));
+                if (kCl && pt == 32) stamp(c, 3);
             } else if (lane == 0) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
@@ -447,13 +458,16 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
         if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) break;
         tc_fence_after();
+        if (kCl && pt == 0) stamp(c, 4);
         p_cols_to_bf16(lane_addr);
+        if (kCl && pt == 0) stamp(c, 5);
         if constexpr (!kCl) {
             if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) break;
             if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
         }
         tc_fence_before();
         named_bar_sync(2, 128);
+        if (kCl && pt == 0) stamp(c, 6);
         if (w == W_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
             tc_fence_after();
             auto b2 = [&](int kk) { return make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512); };
@@ -461,6 +475,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) tc_mma_ts_warp(u.tmem + TM_P, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
                 tc_commit_warp(bar_addr(u, B_G2));
+                if (kCl && pt == 32) stamp(c, 7);
             } else if (lane == 0) {
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) tc_mma_ts(u.tmem + TM_P, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
@@ -1235,15 +1250,24 @@ cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, in
     if (units > sms) return cudaSuccess;
     *sched = KDA_SCHEDULE_ONE_PER_SM;
     if (units * CL_SIZE > sms) return cudaSuccess;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg;
-    const Kernel ck = cluster_config(flags, units, nullptr, attr, &cfg);
-    e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_CL);
-    if (e != cudaSuccess) return e;
-    int resident = 0;
-    if (cudaOccupancyMaxActiveClusters(&resident, ck, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();   // no cluster schedule on this device
-        return cudaSuccess;
+    // the resident-cluster count is a property of the device and the instantiation: ask the
+    // runtime once (the query costs more host time than a whole launch) and keep the answer
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> resident_cache[kMaxDev][4];   // zero-initialised: 0 = not asked yet
+    const int fi = (int)(flags & 3u);
+    std::atomic<int>* slot = dev < kMaxDev ? &resident_cache[dev][fi] : nullptr;
+    int resident = slot ? slot->load(std::memory_order_relaxed) - 1 : -1;
+    if (resident < 0) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg;
+        const Kernel ck = cluster_config(flags, units, nullptr, attr, &cfg);
+        e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_CL);
+        if (e != cudaSuccess) return e;
+        if (cudaOccupancyMaxActiveClusters(&resident, ck, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();   // no cluster schedule on this device
+            resident = 0;
+        }
+        if (slot) slot->store(resident + 1, std::memory_order_relaxed);
     }
     if (resident >= units) *sched = KDA_SCHEDULE_CLUSTER;
     return cudaSuccess;
@@ -1264,6 +1288,8 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t cfg;
         const Kernel ck = cluster_config(p.flags, units, stream, attr, &cfg);
+        e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_CL);
+        if (e != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, ck, p, maps);
         return e != cudaSuccess ? e : cudaGetLastError();
     }

@@ -152,6 +152,23 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
 #define KDA_SCHEDULE_CLUSTER    2
 kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule);
 
+/*
+ * Chain trace, for profiling the recurrence of one unit (a profiling aid; off by default).
+ * After kda_fwd_set_trace(buf, bytes, unit) with a device buffer, the forward launches of
+ * this host thread that take KDA_SCHEDULE_CLUSTER record, for (sequence, head) unit `unit`
+ * (sequence * H + head), KDA_TRACE_POINTS SM clock readings (uint64, one SM's clock) per
+ * chunk c < bytes / (8 * KDA_TRACE_POINTS), at buf[c * KDA_TRACE_POINTS + i]:
+ *   0 the chunk's iteration starts            4 GEMM1 has completed
+ *   1 the MMA warp waits for the chunk's v    5 -R is in bf16 in Tensor Memory
+ *   2 v has landed                            6 GEMM2's operands are ready
+ *   3 GEMM1 is issued                         7 GEMM2 is issued
+ * Other launches and entries leave the buffer untouched; outputs do not depend on tracing.
+ * kda_fwd_set_trace(NULL, 0, 0) turns it off.  Returns KDA_ERR_INVALID_ARG for a buffer
+ * that is not 8-byte aligned or holds less than one chunk, or a negative unit.
+ */
+#define KDA_TRACE_POINTS 8
+kda_status kda_fwd_set_trace(void* device_buffer, size_t bytes, int64_t unit);
+
 /* Static description of a status code. */
 const char* kda_status_string(kda_status s);
 

@@ -198,3 +198,10 @@ def test_schedule_query_rejects_before_touching_the_device(lib):
     assert lib.kda_fwd_schedule(8, 0x4, ctypes.byref(sched)) == kb.KDA_ERR_INVALID_ARG
     assert lib.kda_fwd_schedule(8, 0, None) == kb.KDA_ERR_INVALID_ARG
     assert sched.value == -1
+
+
+def test_trace_setter_checks_its_arguments(lib):
+    assert lib.kda_fwd_set_trace(ctypes.c_void_p(4), 1024, 0) == kb.KDA_ERR_INVALID_ARG     # misaligned
+    assert lib.kda_fwd_set_trace(ctypes.c_void_p(4096), 8, 0) == kb.KDA_ERR_INVALID_ARG    # under one chunk
+    assert lib.kda_fwd_set_trace(ctypes.c_void_p(4096), 1024, -1) == kb.KDA_ERR_INVALID_ARG
+    assert lib.kda_fwd_set_trace(None, 0, 0) == kb.KDA_OK                                  # off

@@ -132,3 +132,37 @@ def test_cluster_schedule_long_sequences_and_variants():
         assert kb.kda_read_device_status(ws) == 0
         assert_close("cluster out", out.double().cpu().numpy(), ref_out, bf16)
         assert_close("cluster state", final.double().cpu().numpy(), ref_final, f32)
+
+
+def test_chain_trace_records_one_unit_without_changing_the_numbers():
+    w = Workload("sched_trace", 84, H=2, B=1, T=500, seq_lens=[300, 200], init_dtype=f32, final_dtype=f32)
+    assert kb.kda_fwd_schedule(w.units) == kb.KDA_SCHEDULE_CLUSTER
+    inp = make_inputs(w, "cpu")
+    out0, fin0, bits0 = run_gpu(inp)
+    assert bits0 == 0
+    n, h = 1, 1                                  # sequence 1 (200 tokens: 7 chunks), head 1
+    nch = (200 + 31) // 32
+    buf = torch.zeros((nch + 3, kb.KDA_TRACE_POINTS), dtype=torch.int64, device="cuda")
+    kb.kda_fwd_set_trace(buf, unit=n * w.H + h)
+    try:
+        out1, fin1, bits1 = run_gpu(inp)
+        # a launch on the two-CTA schedule leaves the buffer alone
+        many = Workload("sched_trace_many", 85, H=64, B=4, T=40, init_dtype=None, final_dtype=f32)
+        assert kb.kda_fwd_schedule(many.units) == kb.KDA_SCHEDULE_TWO_PER_SM
+        snapshot = buf.clone()
+        _, _, bits2 = run_gpu(make_inputs(many, "cpu"))
+        assert bits2 == 0
+        assert torch.equal(buf, snapshot)
+    finally:
+        kb.kda_fwd_set_trace(None)
+    assert bits1 == 0
+    torch.testing.assert_close(out1.cpu(), out0.cpu(), rtol=0, atol=0, equal_nan=True)
+    torch.testing.assert_close(fin1.cpu(), fin0.cpu(), rtol=0, atol=0)
+    t = buf.cpu()
+    assert (t[:nch] > 0).all() and (t[nch:] == 0).all()
+    for c in range(nch):
+        r = t[c].tolist()
+        assert r[0] <= r[4] <= r[5] <= r[6], r      # thread 0, in program order
+        assert r[1] <= r[2] <= r[3] <= r[7], r      # the MMA warp, in program order
+        assert r[3] < r[4] and r[6] <= r[7], r      # GEMM1 completes after its issue; GEMM2 issues after its operands
+    assert (t[1:nch, 0] > t[: nch - 1, 7]).all()    # chunks run in order
