@@ -156,8 +156,13 @@ METRIC = "KDA prefill tokens/s at 1 GB300 (TFLOP/s and roofline fractions alongs
 
 def bench_config(w, world: int) -> dict:
     """The `config` object of the JSON line (the same for both arms)."""
+    name = lambda dt: {"float32": "fp32", "bfloat16": "bf16"}[str(dt).replace("torch.", "")]
+    if w.init_dtype is not None:
+        state = f"{name(w.init_dtype)} in, {name(w.final_dtype)} out, in place, 2 rotating buffers"
+    else:
+        state = f"zero initial state, {name(w.final_dtype)} final state, 2 rotating buffers"
     return {"workload": w.name, "tokens": w.total_tokens, "heads": w.H, "sequences": w.num_seqs,
-            "head_dim": w.K, "chunk": 32, "state": "fp32 in/out, in place, 2 rotating buffers",
+            "head_dim": w.K, "chunk": 32, "state": state,
             "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
 
 
