@@ -1,9 +1,12 @@
 // KDA chunked prefill forward on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// One CTA per (sequence, head) unit, two CTAs per SM.  The fp32 V x K state stays
-// resident in Tensor Memory for the whole sequence ("FlashInfer PR #4262" notes,
-// section 6); the recurrent GEMMs run as tcgen05.mma with fp32 TMEM accumulators,
-// and the small intra-chunk products as warp-level mma.sync (section 7).
+// One CTA per (sequence, head) unit, two CTAs per SM; with no more units than SMs, one CTA
+// per SM (a second instantiation); with at most a quarter as many, a cluster of four CTAs
+// per unit, three of which prepare chunks for the fourth's chain (the cluster schedule,
+// below).  The fp32 V x K state stays resident in Tensor Memory for the whole sequence
+// ("FlashInfer PR #4262" notes, section 6); the recurrent GEMMs run as tcgen05.mma with
+// fp32 TMEM accumulators, and the small intra-chunk products as warp-level mma.sync
+// (section 7).
 //
 // Per chunk (section 3 notation; R = V^T - P, B2 = diag(beta) INV^T):
 //   GEMM1  [O_0 | P] = S_bf16 [Q_d | K_d]^T           M128 N64  K128  (A = bf16 S from TMEM)

@@ -10,6 +10,7 @@ Workloads (K = V = 128, lower_bound = -5, scale = 1/sqrt(128)):
   packed3   cu_seqlens [0, 300, 1000, 2024], H=96, fp32 initial/final state
   long      B=1, T=32768, H=32, no initial state, bf16 final state
   packed64  64 sequences, lengths ~ U{64..8192} (seed 4), H=64, fp32 initial/final
+  fixed96 / fixed64  B=1, T=8192, H=96 / H=64, fp32 initial/final state (timing context)
 plus smaller variants of the same mix that the oracle evaluates in seconds.
 
 Distributions: q, k, v, g ~ N(0, 1); beta ~ U(0, 1); A_log ~ U(0, 1) [H];
@@ -82,6 +83,13 @@ def workload(name: str) -> Workload:
         return Workload("long", 3, H=32, B=1, T=32768, init_dtype=None, final_dtype=bf16)
     if name == "packed64":
         return _packed("packed64", 4, 64, _lengths(4, 64, 64, 8192), init_dtype=f32, final_dtype=f32)
+    # The fixed-length workloads of the pages' reported timings (8,192 tokens at H = 96 and
+    # H = 64), read as one sequence per head with an fp32 state updated in place: context
+    # for the timing only (the pages measured another GPU).
+    if name == "fixed96":
+        return Workload("fixed96", 5, H=96, B=1, T=8192, init_dtype=f32, final_dtype=f32)
+    if name == "fixed64":
+        return Workload("fixed64", 6, H=64, B=1, T=8192, init_dtype=f32, final_dtype=f32)
     # Smaller cases with the same mix, several chunks and ragged tails.
     if name == "batched_small":
         return Workload("batched_small", 101, H=3, B=2, T=200, init_dtype=bf16, final_dtype=bf16)
