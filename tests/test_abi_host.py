@@ -205,3 +205,26 @@ def test_trace_setter_checks_its_arguments(lib):
     assert lib.kda_fwd_set_trace(ctypes.c_void_p(4096), 8, 0) == kb.KDA_ERR_INVALID_ARG    # under one chunk
     assert lib.kda_fwd_set_trace(ctypes.c_void_p(4096), 1024, -1) == kb.KDA_ERR_INVALID_ARG
     assert lib.kda_fwd_set_trace(None, 0, 0) == kb.KDA_OK                                  # off
+
+
+def _header_constants():
+    text = open(os.path.join(ROOT, "include", "kda.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    consts = {}
+    for name, val in re.findall(r"#define\s+(KDA_[A-Z0-9_]+)\s+\(?(-?0x[0-9a-fA-F]+|-?[0-9.]+)u?f?\)?", text):
+        consts[name] = float(val) if "." in val else int(val, 0)
+    for name, val in re.findall(r"\b(KDA_[A-Z0-9_]+)\s*=\s*([0-9]+)", text):
+        consts[name] = int(val)
+    return consts
+
+
+def test_binding_constants_match_the_header():
+    consts = _header_constants()
+    mirrored = ["KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_ALIAS", "KDA_ERR_WORKSPACE",
+                "KDA_ERR_CUDA", "KDA_BF16", "KDA_F32", "KDA_I64", "KDA_DEVERR_CU_SEQLENS", "KDA_DEVERR_TIMEOUT",
+                "KDA_DEVERR_INTERNAL", "KDA_FLAG_BETA_LOGIT", "KDA_FLAG_GATE_SOFTPLUS", "KDA_SCHEDULE_TWO_PER_SM",
+                "KDA_SCHEDULE_ONE_PER_SM", "KDA_SCHEDULE_CLUSTER", "KDA_TRACE_POINTS"]
+    for name in mirrored:
+        assert name in consts, name
+        assert getattr(kb, name) == consts[name], name
+    assert kb.HEAD_DIM == consts["KDA_HEAD_DIM"]
