@@ -69,3 +69,34 @@ def test_both_arms_share_metric_and_config():
     cfg = bench.bench_config(w, 1)
     assert cfg["workload"] == "packed64" and cfg["tokens"] == w.total_tokens and cfg["heads"] == 64
     assert "GB300" in bench.METRIC
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """The reference arm (the oracle on host cores) prints one JSON line with the keys the
+    benchmark contract names, its e2e and cpu_baseline objects describing the same run."""
+    import json
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+
+    class Args:
+        workload, steps, warmup = "tiny", 1, 3
+    bench.run_reference(Args())
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == "tokens/s"
+    assert d["value"] > 0 and d["higher_is_better"] is True and d["steps"] == 1 and d["warmup"] == 3
+    assert d["config"] == bench.bench_config(bench_workload("tiny"), 1)
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def bench_workload(name):
+    from gated_delta_rule_36_gb300.inputs import workload
+    return workload(name)
