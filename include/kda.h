@@ -163,7 +163,8 @@ kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule);
  *   2 v has landed                            6 GEMM2's operands are ready
  *   3 GEMM1 is issued                         7 GEMM2 is issued
  * Other launches and entries leave the buffer untouched; outputs do not depend on tracing.
- * kda_fwd_set_trace(NULL, 0, 0) turns it off.  Returns KDA_ERR_INVALID_ARG for a buffer
+ * The caller owns the buffer, which the traced launches write on their streams: it must
+ * stay allocated until they complete.  kda_fwd_set_trace(NULL, 0, 0) turns it off.  Returns KDA_ERR_INVALID_ARG for a buffer
  * that is not 8-byte aligned or holds less than one chunk, or a negative unit.
  */
 #define KDA_TRACE_POINTS 8
