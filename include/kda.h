@@ -145,7 +145,8 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
  *                            every cluster can be resident at once)
  * A unit's arithmetic is the same in every schedule: outputs and states do not depend on it.
  * Returns KDA_ERR_INVALID_ARG for units < 0, unknown flag bits or a null `schedule`, and
- * KDA_ERR_CUDA when the device cannot be queried.
+ * KDA_ERR_CUDA when the device cannot be queried.  An addition of this library: the
+ * FlashInfer notes (section 9) choose instead between their M128 and M64 variants.
  */
 #define KDA_SCHEDULE_TWO_PER_SM 0
 #define KDA_SCHEDULE_ONE_PER_SM 1
@@ -164,7 +165,8 @@ kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule);
  *   3 GEMM1 is issued                         7 GEMM2 is issued
  * Other launches and entries leave the buffer untouched; outputs do not depend on tracing.
  * The caller owns the buffer, which the traced launches write on their streams: it must
- * stay allocated until they complete.  kda_fwd_set_trace(NULL, 0, 0) turns it off.  Returns KDA_ERR_INVALID_ARG for a buffer
+ * stay allocated until they complete.  kda_fwd_set_trace(NULL, 0, 0) turns it off.  A
+ * profiling aid of this library; the pages describe no counterpart.  Returns KDA_ERR_INVALID_ARG for a buffer
  * that is not 8-byte aligned or holds less than one chunk, or a negative unit.
  */
 #define KDA_TRACE_POINTS 8
