@@ -152,6 +152,8 @@ def barrier(world: int):
 
 
 METRIC = "KDA prefill tokens/s at 1 GB300 (TFLOP/s and roofline fractions alongside)"
+# --kernel: the default kernel or one of the design alternatives (kda_fwd_ex's kernel field)
+KERNELS = {"default": 0x000, "chunk16": 0x100, "register_state": 0x200, "bf16_state": 0x300}
 
 
 def bench_config(w, world: int) -> dict:
@@ -272,10 +274,12 @@ def run_ours(args):
         [torch.empty((w.num_seqs, w.H, w.V, w.K), dtype=w.final_dtype, device=dev) for _ in range(2)]
     ws = torch.empty(kda.kda_workspace_size(tokens, w.H, w.num_seqs), dtype=torch.uint8, device=dev)
 
+    kflags = KERNELS[args.kernel]
+
     def step(i):
         kda.kda_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.scale, out, inp.A_log, inp.dt_bias,
                     inp.lower_bound, initial_state=states[i % 2], final_state=finals[i % 2],
-                    cu_seqlens=inp.cu_seqlens, workspace=ws, stream=stream)
+                    cu_seqlens=inp.cu_seqlens, workspace=ws, stream=stream, flags=kflags)
 
     for i in range(args.warmup):
         step(i)
@@ -320,7 +324,7 @@ def run_ours(args):
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": bench_config(w, world),
+        "config": dict(bench_config(w, world), **({} if args.kernel == "default" else {"kernel": args.kernel})),
         "tflops": tflops,
         "tensor_frac": tflops / tc_peak,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
@@ -434,6 +438,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--kernel", choices=tuple(KERNELS), default="default",
+                    help="the default kernel or a design alternative (timed on the same workload)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--e2e-groups", type=int, default=8, help="sequence groups kda_fwd_host pipelines over")
     ap.add_argument("--no-e2e", action="store_true")

@@ -27,6 +27,8 @@ EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_erro
             "kda_fwd_host_workspace_offset", "kda_decode", "kda_fwd_ex", "kda_decode_ex", "kda_fwd_schedule",
             "kda_fwd_set_trace")
 KDA_FLAG_BETA_LOGIT, KDA_FLAG_GATE_SOFTPLUS = 0x1, 0x2
+KDA_FLAG_KERNEL_MASK = 0xF00
+KDA_KERNEL_DEFAULT, KDA_KERNEL_CHUNK16, KDA_KERNEL_REGISTER_STATE, KDA_KERNEL_BF16_STATE = 0x000, 0x100, 0x200, 0x300
 KDA_SCHEDULE_TWO_PER_SM, KDA_SCHEDULE_ONE_PER_SM, KDA_SCHEDULE_CLUSTER = 0, 1, 2
 KDA_TRACE_POINTS = 8
 
@@ -209,8 +211,9 @@ def kda_fwd(q, k, v, g, beta, scale, out, A_log, dt_bias, lower_bound, initial_s
     """Run the forward through the C ABI.  Tensors as in ``include/kda.h``.
 
     ``workspace`` (uint8 CUDA tensor) is allocated with torch when omitted;
-    ``stream`` defaults to torch's current stream of q's device; ``flags`` (KDA_FLAG_*)
-    selects the interface variants through kda_fwd_ex.  Returns the workspace (its
+    ``stream`` defaults to torch's current stream of q's device; ``flags`` (KDA_FLAG_*
+    bits, plus one KDA_KERNEL_* value) selects the interface variants and the kernel
+    through kda_fwd_ex.  Returns the workspace (its
     first word is the device status).
     """
     lib = load()

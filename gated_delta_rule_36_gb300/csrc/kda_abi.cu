@@ -129,8 +129,13 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
                            const kda_tensor* final_state, const kda_tensor* cu_seqlens, void* workspace,
                            size_t workspace_bytes, cudaStream_t s, bool reset_status, bool enqueue,
                            uint32_t flags) {
-    if (flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
-        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x", flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
+    const uint32_t kernel = flags & KDA_FLAG_KERNEL_MASK;
+    const uint32_t iface = flags & ~KDA_FLAG_KERNEL_MASK;
+    if (iface & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
+        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x", iface & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
+    if (kernel > KDA_KERNEL_BF16_STATE) return fail(KDA_ERR_INVALID_ARG, "flags: unknown kernel 0x%x", kernel);
+    if (kernel != KDA_KERNEL_DEFAULT && iface != 0)
+        return fail(KDA_ERR_UNSUPPORTED, "the interface flags are built into the default kernel only");
     if (!present(q)) return fail(KDA_ERR_INVALID_ARG, "q: missing");
     if (q->ndim != 4) return fail(KDA_ERR_INVALID_ARG, "q: ndim %d, expected 4 [B,T,H,128]", q->ndim);
     const int64_t B = q->shape[0], T = q->shape[1], H = q->shape[2];
@@ -223,27 +228,19 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
     p.nseq = (int)nseq;
     p.scale = scale;
     p.lower_bound = lower_bound;
-    p.flags = flags;
+    p.flags = iface;
     p.trace = g_trace;
     p.trace_chunks = g_trace_chunks;
     p.trace_unit = g_trace_unit;
 
-    // KDA_FWD_KERNEL selects an ablation variant: "mma" keeps the state in mma.sync
-    // registers, "tc16" uses 16-token chunks without the exponent anchor, "tcbf16" rounds
-    // the carried state to bf16 at every chunk; the default is the tcgen05 kernel with
-    // 32-token chunks and the fp32 state resident in TMEM.
-    static const int variant = [] {
-        const char* v = getenv("KDA_FWD_KERNEL");
-        if (v != nullptr && strcmp(v, "mma") == 0) return 1;
-        if (v != nullptr && strcmp(v, "tc16") == 0) return 2;
-        if (v != nullptr && strcmp(v, "tcbf16") == 0) return 3;
-        return 0;
-    }();
-    if (variant != 0 && flags != 0)
-        return fail(KDA_ERR_UNSUPPORTED, "the ablation kernel chosen with KDA_FWD_KERNEL takes no interface flags");
-    e = variant == 1   ? kda::launch_fwd_mma(p, s)
-        : variant == 2 ? kda::launch_fwd_tc16(p, s)
-                       : kda::launch_fwd_tc(p, s, variant == 3);
+    // the kernel field selects a design alternative (include/kda.h); the default is the
+    // tcgen05 kernel with 32-token chunks and the fp32 state resident in TMEM
+    switch (kernel) {
+        case KDA_KERNEL_CHUNK16: e = kda::launch_fwd_tc16(p, s); break;
+        case KDA_KERNEL_REGISTER_STATE: e = kda::launch_fwd_mma(p, s); break;
+        case KDA_KERNEL_BF16_STATE: e = kda::launch_fwd_tc(p, s, true); break;
+        default: e = kda::launch_fwd_tc(p, s, false); break;
+    }
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));
     return KDA_OK;
 }
@@ -343,7 +340,8 @@ kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule) {
     if (schedule == nullptr) return fail(KDA_ERR_INVALID_ARG, "null schedule");
     if (units < 0) return fail(KDA_ERR_INVALID_ARG, "units must be >= 0");
     if (flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
-        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x", flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
+        return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x (interface flags of the default kernel only)",
+                    flags & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
     int sched = KDA_SCHEDULE_TWO_PER_SM;
     const cudaError_t e = kda::fwd_tc_schedule(units, flags, false, &sched);
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "schedule query: %s", cudaGetErrorString(e));

@@ -30,7 +30,8 @@ constexpr int kMaxDevices = 256;
 std::mutex g_mu;
 void* g_workspace_addr[kMaxDevices] = {};
 
-// Device address of g_no_alloc_workspace on `dev`, resolved once with `dev` current.
+// Device address of g_no_alloc_workspace on `dev`, resolved once with `dev` current.  The
+// cached address does not survive cudaDeviceReset on that device.
 cudaError_t workspace_address(int dev, void** addr) {
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_workspace_addr[dev] == nullptr) {
@@ -73,8 +74,14 @@ extern "C" kda_status kda_fwd_no_alloc(const kda_tensor* q, const kda_tensor* k,
         }
     }
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    int dev = -1;
+    int dev = -1, cur = -1;
     cudaError_t e = cudaStreamGetDevice(s, &dev);
+    if (e == cudaSuccess) e = cudaGetDevice(&cur);
+    if (e == cudaSuccess && dev != cur) {
+        // kda_fwd launches on the current device and picks its schedule from it
+        kda::set_last_error("kda_fwd_no_alloc: the stream belongs to another device than the current one");
+        return KDA_ERR_INVALID_ARG;
+    }
     if (e == cudaSuccess && (dev < 0 || dev >= kMaxDevices)) e = cudaErrorInvalidDevice;
     void* ws = nullptr;
     if (e == cudaSuccess) e = workspace_address(dev, &ws);

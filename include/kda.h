@@ -74,6 +74,25 @@ typedef struct {
 #define KDA_FLAG_BETA_LOGIT    0x1u
 #define KDA_FLAG_GATE_SOFTPLUS 0x2u
 
+/* Kernel selection (a 4-bit field of the flags of kda_fwd_ex, one value at a time): the
+ * design alternatives the pages weigh, built beside the default kernel so that each can
+ * be measured and checked against the oracle.  Each computes the same forward; none takes
+ * an interface flag (KDA_ERR_UNSUPPORTED), and values not listed are KDA_ERR_INVALID_ARG.
+ *   KDA_KERNEL_DEFAULT           32-token chunks, fixed exponent anchor, fp32 state resident
+ *                                in Tensor Memory (FlashInfer PR #4262 notes, sections 2 and 6)
+ *   KDA_KERNEL_CHUNK16           16-token chunks without the exponent anchor (same notes,
+ *                                sections 2 and 14: the chunk-size alternative)
+ *   KDA_KERNEL_REGISTER_STATE    fp32 state in mma.sync accumulator registers, every product
+ *                                on mma.sync (the pre-tcgen05 placement of the state)
+ *   KDA_KERNEL_BF16_STATE        the default kernel with the carried state rounded to bf16 at
+ *                                every chunk boundary ("How FlashKDA Stores On-Chip Recurrent
+ *                                State in BF16": the precision of a bf16 state store) */
+#define KDA_FLAG_KERNEL_MASK        0xF00u
+#define KDA_KERNEL_DEFAULT          0x000u
+#define KDA_KERNEL_CHUNK16          0x100u
+#define KDA_KERNEL_REGISTER_STATE   0x200u
+#define KDA_KERNEL_BF16_STATE       0x300u
+
 /* Device-side status bits, in the first 32-bit word of the workspace. */
 #define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] > T */
 #define KDA_DEVERR_TIMEOUT    0x2u  /* a bounded on-chip wait expired; outputs are invalid  */
@@ -123,9 +142,10 @@ kda_status kda_fwd(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v
                    void* workspace, size_t workspace_bytes, kda_stream_t stream);
 
 /*
- * kda_fwd with interface variants: `flags` is a combination of KDA_FLAG_* (other bits:
- * KDA_ERR_INVALID_ARG).  The ablation kernels chosen with KDA_FWD_KERNEL support no flag
- * (KDA_ERR_UNSUPPORTED).  Everything else is as for kda_fwd.
+ * kda_fwd with interface variants and kernel selection: `flags` is a combination of
+ * KDA_FLAG_* bits plus at most one KDA_KERNEL_* value in the KDA_FLAG_KERNEL_MASK field
+ * (other bits or values: KDA_ERR_INVALID_ARG; an interface flag with a kernel other than
+ * the default: KDA_ERR_UNSUPPORTED).  Everything else is as for kda_fwd.
  */
 kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
                       const kda_tensor* g, const kda_tensor* beta, float scale,
@@ -144,7 +164,8 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
  *                            prepare its chunks (up to a quarter as many units as SMs, when
  *                            every cluster can be resident at once)
  * A unit's arithmetic is the same in every schedule: outputs and states do not depend on it.
- * Returns KDA_ERR_INVALID_ARG for units < 0, unknown flag bits or a null `schedule`, and
+ * Returns KDA_ERR_INVALID_ARG for units < 0, unknown flag bits, a kernel other than the
+ * default or a null `schedule`, and
  * KDA_ERR_CUDA when the device cannot be queried.  An addition of this library: the
  * FlashInfer notes (section 9) choose instead between their M128 and M64 variants.
  */
@@ -201,9 +222,11 @@ kda_status kda_read_device_status(const void* workspace, kda_stream_t stream, ui
  * (256 + 4 * KDA_NO_ALLOC_MAX_SEQS bytes), which every GPU that loads the library
  * holds until the process exits.  Nothing in this call allocates or frees memory.
  *  - More than KDA_NO_ALLOC_MAX_SEQS sequences: KDA_ERR_UNSUPPORTED, nothing enqueued.
- *  - The first call on a device looks up the array's device address on that device
- *    (the stream's device, made current for the lookup); make that first call before
- *    any stream capture.
+ *  - `stream` must belong to the current device (KDA_ERR_INVALID_ARG otherwise): the
+ *    launches go to the current device, as for kda_fwd.
+ *  - The first call on a device looks up the array's device address on that device;
+ *    make that first call before any stream capture.  The address is kept for the
+ *    rest of the process: it does not survive a cudaDeviceReset of that device.
  *  - Every call on a device shares the one array, and the array keeps what the last
  *    call left in it (kda_fwd clears the status word at the start of each call).
  *    Calls whose work overlaps on the GPU (for example on two streams at once) race

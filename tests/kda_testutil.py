@@ -22,9 +22,14 @@ BF16_MAX_ABS = 2e-2
 BF16_REL_FRO = 1e-2
 F32_REL_FRO = 5e-3
 
+# (test, tensor, dtype, max |diff|, relative Frobenius, compared elements) of every
+# whole-tensor comparison of a full-size workload; conftest prints it after the run
+PARITY_LOG = []
 
-def run_gpu(inp: Inputs, final_dtype=None, out=None, final=None, workspace=None, initial_state="same"):
-    """Run the CUDA path.  Returns (out, final_state, device status bits) on the device."""
+
+def run_gpu(inp: Inputs, final_dtype=None, out=None, final=None, workspace=None, initial_state="same", flags=0):
+    """Run the CUDA path (``flags``: KDA_FLAG_* / KDA_KERNEL_* of kda_fwd_ex).  Returns
+    (out, final_state, device status bits) on the device."""
     w = inp.w
     dev = torch.device("cuda")
     d = inp if inp.q.is_cuda else inp.to(dev)
@@ -35,7 +40,8 @@ def run_gpu(inp: Inputs, final_dtype=None, out=None, final=None, workspace=None,
         final = torch.full((w.num_seqs, w.H, w.V, w.K), float("nan"), dtype=fd, device=dev)
     init = d.initial_state if isinstance(initial_state, str) else initial_state
     ws = kb.kda_fwd(d.q, d.k, d.v, d.g, d.beta, d.scale, out, d.A_log, d.dt_bias, d.lower_bound,
-                    initial_state=init, final_state=final, cu_seqlens=d.cu_seqlens, workspace=workspace)
+                    initial_state=init, final_state=final, cu_seqlens=d.cu_seqlens, workspace=workspace,
+                    flags=flags)
     bits = kb.kda_read_device_status(ws)
     return out, final, bits
 
@@ -130,3 +136,72 @@ def check_units(inp: Inputs, out, final, ref_units):
         if final is not None:
             stats[(n, h, "final")] = assert_close(f"final[seq {n}, head {h}]", final[n, h], rf, final.dtype)
     return stats
+
+
+class _Acc:
+    """Running max |diff|, sum diff^2 and sum ref^2 over the pieces of one tensor."""
+
+    def __init__(self):
+        self.max_abs, self.d2, self.r2, self.n = 0.0, 0.0, 0.0, 0
+
+    def add(self, got, ref):
+        got = np.asarray(got, dtype=np.float64)
+        ref = np.asarray(ref, dtype=np.float64)
+        assert np.all(np.isfinite(got)), "non-finite values"
+        d = got - ref
+        if d.size:
+            self.max_abs = max(self.max_abs, float(np.max(np.abs(d))))
+        self.d2 += float(np.sum(d * d))
+        self.r2 += float(np.sum(ref * ref))
+        self.n += d.size
+
+    def rel(self):
+        return math.sqrt(self.d2) / max(math.sqrt(self.r2), 1e-30)
+
+
+def _verdict(label, name, acc, dtype):
+    rel = acc.rel()
+    kind = "fp32" if dtype == torch.float32 else "bf16"
+    PARITY_LOG.append((label, name, kind, acc.max_abs, rel, acc.n))
+    if os.environ.get("KDA_TEST_VERBOSE"):
+        print(f"[err] {label} {name}: max_abs={acc.max_abs:.3e} rel_fro={rel:.3e} ({kind}, {acc.n} elements)")
+    if dtype == torch.float32:
+        assert rel <= F32_REL_FRO, f"{label} {name}: rel Frobenius {rel:.3e} > {F32_REL_FRO}"
+    else:
+        assert acc.max_abs <= BF16_MAX_ABS and rel <= BF16_REL_FRO, \
+            f"{label} {name}: max abs {acc.max_abs:.3e} (<= {BF16_MAX_ABS}), rel Frobenius {rel:.3e} (<= {BF16_REL_FRO})"
+
+
+def check_whole_by_sequence(inp: Inputs, out, final, label, nthreads=0):
+    """Whole-tensor comparison of a full-size run with the oracle, one sequence at a time.
+
+    The oracle runs every head of one sequence per call (its OpenMP loop is over the
+    heads), so host memory stays bounded by one sequence's fp64 copies however large the
+    workload.  max |diff| and the relative Frobenius error are accumulated over the whole
+    of ``out`` (every row that belongs to a sequence) and the whole of ``final``; rows
+    outside every sequence must keep their NaN sentinel, bit for bit."""
+    w = inp.w
+    cpu = lambda t: None if t is None else t.detach().cpu()
+    flat = lambda t: t.reshape((w.B * w.T,) + tuple(t.shape[2:]))
+    q, k, v, g, beta = (flat(x) for x in (inp.q, inp.k, inp.v, inp.g, inp.beta))
+    of = flat(out)
+    A_log, dt_bias = cpu(inp.A_log), cpu(inp.dt_bias)
+    acc_o, acc_f = _Acc(), _Acc()
+    bounds = seq_bounds(w)
+    for n, (bos, eos) in enumerate(bounds):
+        sl = lambda t: cpu(t[bos:eos]).unsqueeze(0)
+        S0 = None if inp.initial_state is None else cpu(inp.initial_state[n]).unsqueeze(0)
+        ro, rf = O.kda_oracle_fwd(sl(q), sl(k), sl(v), sl(g), sl(beta), inp.scale, A_log, dt_bias,
+                                  inp.lower_bound, initial_state=S0, nthreads=nthreads)
+        acc_o.add(cpu(of[bos:eos]).double().numpy(), ro[0])
+        if final is not None:
+            acc_f.add(cpu(final[n]).double().numpy(), rf[0])
+    covered = torch.zeros(w.B * w.T, dtype=torch.bool)
+    for bos, eos in bounds:
+        covered[bos:eos] = True
+    outside = cpu(of)[~covered]
+    assert torch.isnan(outside.float()).all(), "rows outside every sequence were written"
+    _verdict(label, "out", acc_o, torch.bfloat16)
+    if final is not None:
+        _verdict(label, "final_state", acc_f, final.dtype)
+    return acc_o, acc_f

@@ -62,7 +62,7 @@ def T(dtype, shape, addr):
     return d
 
 
-def call(lib, **over):
+def args(**over):
     B, Tn, H = over.pop("BTH", (1, 64, 2))
     a = dict(
         q=T(kb.KDA_BF16, (B, Tn, H, 128), BASE + 0x0000000),
@@ -76,6 +76,11 @@ def call(lib, **over):
         init=None, final=None, cu=None, scale=0.088, lb=-5.0,
         ws=BASE + 0x9000000, ws_bytes=1 << 20)
     a.update(over)
+    return a
+
+
+def call(lib, **over):
+    a = args(**over)
     r = lambda d: None if d is None else ctypes.byref(d)
     return lib.kda_fwd(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]), ctypes.c_float(a["scale"]),
                        r(a["out"]), r(a["A_log"]), r(a["dt_bias"]), ctypes.c_float(a["lb"]), r(a["init"]),
@@ -114,6 +119,30 @@ def test_rejections(lib):
         got = call(lib, **over)
         assert got == expect, (over, got, lib.kda_last_error())
         assert lib.kda_last_error(), over
+
+
+def test_kernel_field_rejections(lib):
+    """The kernel field of kda_fwd_ex's flags: one listed value at a time, and no interface
+    flag beside a kernel other than the default; refused before anything is enqueued."""
+    a = args()
+    r = lambda t: None if t is None else ctypes.byref(t)
+
+    def call_ex(flags):
+        return lib.kda_fwd_ex(r(a["q"]), r(a["k"]), r(a["v"]), r(a["g"]), r(a["beta"]), ctypes.c_float(a["scale"]),
+                              r(a["out"]), r(a["A_log"]), r(a["dt_bias"]), ctypes.c_float(a["lb"]), r(a["init"]),
+                              r(a["final"]), r(a["cu"]), ctypes.c_void_p(a["ws"]), ctypes.c_size_t(16),
+                              ctypes.c_uint32(flags), ctypes.c_void_p(0))
+
+    assert call_ex(0xF00) == kb.KDA_ERR_INVALID_ARG
+    assert call_ex(0x4) == kb.KDA_ERR_INVALID_ARG
+    assert call_ex(0x1000) == kb.KDA_ERR_INVALID_ARG
+    for kern in (kb.KDA_KERNEL_CHUNK16, kb.KDA_KERNEL_REGISTER_STATE, kb.KDA_KERNEL_BF16_STATE):
+        assert call_ex(kern | kb.KDA_FLAG_BETA_LOGIT) == kb.KDA_ERR_UNSUPPORTED
+        assert call_ex(kern | kb.KDA_FLAG_GATE_SOFTPLUS) == kb.KDA_ERR_UNSUPPORTED
+        # a valid kernel passes the flag checks and then meets the (too small) workspace
+        assert call_ex(kern) == kb.KDA_ERR_WORKSPACE
+    sched = ctypes.c_int32(-1)
+    assert lib.kda_fwd_schedule(4, kb.KDA_KERNEL_CHUNK16, ctypes.byref(sched)) == kb.KDA_ERR_INVALID_ARG
 
 
 def test_binding_refuses_host_tensors():
@@ -222,7 +251,9 @@ def test_binding_constants_match_the_header():
     consts = _header_constants()
     mirrored = ["KDA_OK", "KDA_ERR_INVALID_ARG", "KDA_ERR_UNSUPPORTED", "KDA_ERR_ALIAS", "KDA_ERR_WORKSPACE",
                 "KDA_ERR_CUDA", "KDA_BF16", "KDA_F32", "KDA_I64", "KDA_DEVERR_CU_SEQLENS", "KDA_DEVERR_TIMEOUT",
-                "KDA_DEVERR_INTERNAL", "KDA_FLAG_BETA_LOGIT", "KDA_FLAG_GATE_SOFTPLUS", "KDA_SCHEDULE_TWO_PER_SM",
+                "KDA_DEVERR_INTERNAL", "KDA_FLAG_BETA_LOGIT", "KDA_FLAG_GATE_SOFTPLUS", "KDA_FLAG_KERNEL_MASK",
+                "KDA_KERNEL_DEFAULT", "KDA_KERNEL_CHUNK16", "KDA_KERNEL_REGISTER_STATE", "KDA_KERNEL_BF16_STATE",
+                "KDA_SCHEDULE_TWO_PER_SM",
                 "KDA_SCHEDULE_ONE_PER_SM", "KDA_SCHEDULE_CLUSTER", "KDA_TRACE_POINTS"]
     for name in mirrored:
         assert name in consts, name

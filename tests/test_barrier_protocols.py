@@ -316,3 +316,268 @@ def test_ring_without_lfree_overwrites_l():
         except AssertionError:
             broken += 1
     assert broken > 0
+
+
+# ---------------------------------------------------------------------------------------
+# Expiry and wind-down of the two-slot ring, warp by warp.  Every mbarrier wait in the
+# kernel is bounded: when its limit expires the waiting warp sets the timeout bit and gives
+# up.  The groups' named barriers (bar.sync / bar.red) are not bounded, so a warp must never
+# be left at one after a sibling has given up.  The kernel makes every group barrier that
+# follows a bounded wait a reduction of the warps' verdicts (bar.red.and): a warp whose wait
+# expired still arrives (skipping its work), and the group leaves the loop together.  The
+# model replays, per warp, the waits, arrivals and barriers of the chain group (4 warps: warp
+# 1 issues the MMAs, warp 2 the q/k/g box loads and beta, warp 3 the stores and v loads), the
+# prep group (8 warps; warps 1-3 wait for LFREE before writing L) and the inverse warp, with
+# the box loads and MMA commits as asynchronous engines.  One producer arrival is withheld,
+# or delayed past the waiters' limit, and waits may expire at any poll past the limit.  Every
+# warp must then reach the kernel's final __syncthreads.  The same model with the earlier
+# per-warp verdicts (plain bar.sync, each warp leaving on its own) must be able to hang.
+# ---------------------------------------------------------------------------------------
+
+UNBOUNDED = 2   # blocked on a named barrier: only other warps' arrivals can release it
+                # (yielded as (UNBOUNDED, barrier, generation))
+
+
+class NamedBar:
+    """bar.sync / bar.red.and over `count` warps (generation by generation)."""
+
+    def __init__(self, count):
+        self.count, self.gen, self.arrived, self.acc, self.result = count, 0, 0, True, {}
+
+    def sync(self, pred=True):
+        g = self.gen
+        self.arrived += 1
+        self.acc = self.acc and pred
+        if self.arrived == self.count:
+            self.result[g] = self.acc
+            self.gen, self.arrived, self.acc = g + 1, 0, True
+        while self.gen == g:
+            yield (UNBOUNDED, self, g)
+        return self.result[g]
+
+
+class RingRun:
+    """One CTA of the two-slot ring over n chunks.  `perturb` = (barrier name, completion
+    index, "withhold" | "late"); `limit` = polls before a wait may expire; `uniform` = the
+    kernel's reduced verdicts (False: the earlier per-warp verdicts)."""
+
+    def __init__(self, n, seed, perturb=None, limit=40, uniform=True):
+        self.n, self.rng, self.perturb, self.limit, self.uniform = n, random.Random(seed), perturb, limit, uniform
+        self.bars, self.engines, self.timeouts, self.consumed = {}, [], 0, []
+        self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(13)
+        self.fulltma_fill = {0: 0, 1: 0}
+        self.exited = 0
+
+    def bar(self, *key):
+        if key not in self.bars:
+            self.bars[key] = Barrier(key)
+        return self.bars[key]
+
+    def arrive(self, name, index, *key):
+        """Producer arrival `index` (0-based completion) of barrier (name, *key), unless perturbed."""
+        b = self.bar(name, *key)
+        if self.perturb and self.perturb[0] == name and self.perturb[1] == index:
+            if self.perturb[2] == "withhold":
+                return
+            self.engines.append(self._late(b, 3 * self.limit + self.rng.randrange(3 * self.limit)))
+            return
+        b.arrive()
+
+    def _late(self, b, polls):
+        for _ in range(polls):
+            yield WORK
+        b.arrive()
+
+    def bwait(self, b, k):
+        """Bounded wait for completion k of b: True when it completes, False once expired."""
+        polls = 0
+        while (b.done & 1) == (k & 1):
+            polls += 1
+            if polls > self.limit and self.rng.random() < 0.3:
+                self.timeouts += 1
+                return False
+            yield BLOCKED
+        if b.done != k + 1:
+            raise Aliased(f"{b.name}: waited for completion {k}, passed at {b.done} completions")
+        return True
+
+    def engine(self, name, index, *key):
+        def run():
+            for _ in range(self.rng.randrange(1, 6)):
+                yield WORK
+            self.arrive(name, index, *key)
+        self.engines.append(run())
+
+    def fulltma(self, c):
+        s = c & 1
+        self.fulltma_fill[s] += 1
+        if self.fulltma_fill[s] == 2:   # the box bytes and the 32 beta lanes, as two events
+            self.fulltma_fill[s] = 0
+            self.arrive("FULLTMA", c, s)
+
+    def load_qkg(self, c):
+        def run():
+            for _ in range(self.rng.randrange(1, 6)):
+                yield WORK
+            self.fulltma(c)
+        self.engines.append(run())
+
+    def group_bar(self, gbar, ok):
+        """The group barrier after a bounded wait: reduced verdict, or the earlier plain
+        bar.sync that only the warps still in the loop reach."""
+        if self.uniform:
+            return (yield from gbar.sync(ok))
+        if ok:
+            yield from gbar.sync(True)
+        return ok
+
+    def chain_warp(self, w):
+        n = self.n
+        issued_qkg = issued_v = min(n, 2)
+        if n > 0:
+            for c in range(min(n, 2)):
+                if w == 2:
+                    self.load_qkg(c)
+                    self.fulltma(c)                       # beta
+                if w == 3:
+                    self.engine("FULLV", c >> 1, c)
+            ok = yield from self.bwait(self.bar("AREADY", 0), 0)
+            ok = yield from self.group_bar(self.chain_bar, ok)
+            for c in range(n):
+                if not ok:
+                    break
+                s, k, refill = c & 1, c >> 1, c + 2 < n
+                ok = yield from self.bwait(self.bar("FULLP", s), k)
+                if ok and w == 1:
+                    ok = yield from self.bwait(self.bar("FULLV", s), k)
+                if ok and w == 1:
+                    self.engine("G1", c)
+                if ok:
+                    ok = yield from self.bwait(self.bar("G1"), c)
+                if ok:
+                    ok = yield from self.bwait(self.bar("FULLD", s), k)
+                if ok and refill and w == 2:
+                    self.fulltma(c + 2)                   # beta of chunk c + 2
+                ok = yield from self.group_bar(self.chain_bar, ok)
+                if not ok:
+                    break
+                if w == 1:
+                    self.engine("G2", c)
+                ok = yield from self.bwait(self.bar("G2"), c)
+                ok = yield from self.group_bar(self.chain_bar, ok)
+                if not ok:
+                    break
+                if w == 1:
+                    self.engine("G3", c)
+                ok = yield from self.bwait(self.bar("G3"), c)
+                if ok and refill and w == 2:
+                    self.load_qkg(c + 2)
+                    issued_qkg = c + 3
+                ok = yield from self.group_bar(self.chain_bar, ok)
+                if not ok:
+                    break
+                if w == 0:
+                    self.consumed.append(c)
+                if c + 1 < n:
+                    ok = yield from self.bwait(self.bar("AREADY", s ^ 1), (c + 1) >> 1)
+                    ok = yield from self.group_bar(self.chain_bar, ok)
+                    if not ok:
+                        break
+                    if w == 3 and refill:
+                        self.engine("FULLV", (c + 2) >> 1, s)
+                        issued_v = c + 3
+            # boxes still in flight must land before the CTA exits (bounded waits)
+            if w == 2:
+                for c in range(max(0, issued_qkg - 2), issued_qkg):
+                    yield from self.bwait(self.bar("FULLTMA", c & 1), c >> 1)
+            if w == 3:
+                for c in range(max(0, issued_v - 2), issued_v):
+                    yield from self.bwait(self.bar("FULLV", c & 1), c >> 1)
+        yield from self.cta_bar.sync()
+        self.exited += 1
+
+    def prep_warp(self, pw):
+        for j in range(self.n):
+            s, k = j & 1, j >> 1
+            ok = yield from self.bwait(self.bar("FULLTMA", s), k)
+            ok = yield from self.group_bar(self.prep_bar, ok)
+            if not ok:
+                break
+            yield from self.prep_bar.sync()               # end of phase B: no wait before it
+            if pw == 0:
+                self.arrive("AREADY", j >> 1, s)
+            ok = True
+            if pw in (1, 2, 3) and j > 0:
+                ok = yield from self.bwait(self.bar("LFREE"), j - 1)
+            ok = yield from self.group_bar(self.prep_bar, ok)
+            if not ok:
+                break
+            if pw == 0:
+                self.arrive("FULLP", j >> 1, s)
+        yield from self.cta_bar.sync()
+        self.exited += 1
+
+    def inverse_warp(self):
+        for j in range(self.n):
+            s, k = j & 1, j >> 1
+            ok = yield from self.bwait(self.bar("FULLP", s), k)
+            if not ok:
+                break
+            self.arrive("LFREE", j)
+            self.arrive("FULLD", j >> 1, s)
+        yield from self.cta_bar.sync()
+        self.exited += 1
+
+    def run(self):
+        live = [self.chain_warp(w) for w in range(4)] + [self.prep_warp(p) for p in range(8)] + [self.inverse_warp()]
+        state = {id(a): WORK for a in live}
+        while live or self.engines:
+            live += self.engines
+            for e in self.engines:
+                state[id(e)] = WORK
+            self.engines.clear()
+            # deadlock: every warp waits at a named barrier whose generation has not completed
+            blocked = lambda st: isinstance(st, tuple) and st[1].gen == st[2]
+            if all(blocked(state[id(a)]) for a in live):
+                raise Deadlock(f"{len(live)} warps left at named barriers")
+            a = self.rng.choice(live)
+            try:
+                state[id(a)] = next(a)
+            except StopIteration:
+                live.remove(a)
+        assert self.exited == 13
+        return self
+
+
+PERTURB = [("FULLD", 1), ("FULLP", 2), ("AREADY", 1), ("LFREE", 2), ("G1", 3), ("G2", 0), ("G3", 4),
+           ("FULLV", 1), ("FULLTMA", 3)]
+
+
+def test_ring_model_without_faults_finishes_every_chunk():
+    for seed in range(10):
+        r = RingRun(9, seed, limit=10 ** 9).run()
+        assert r.timeouts == 0 and r.consumed == list(range(9))
+
+
+@pytest.mark.parametrize("mode", ["withhold", "late"])
+@pytest.mark.parametrize("name,index", PERTURB)
+def test_every_warp_winds_down_after_an_expired_wait(name, index, mode):
+    """One arrival withheld (or delayed past the waiters' limit): waits expire, and every
+    warp of every role still reaches the end of the kernel."""
+    for seed in range(30):
+        r = RingRun(10, seed, perturb=(name, index, mode)).run()
+        if mode == "withhold":
+            assert r.timeouts > 0
+
+
+def test_per_warp_verdicts_can_leave_a_warp_at_a_barrier():
+    """The earlier form (each warp acting on its own verdict before a plain bar.sync) hangs
+    when a phase completes just after some of the group's waits expired."""
+    hung = 0
+    for name, index in PERTURB:
+        for seed in range(30):
+            try:
+                RingRun(10, seed, perturb=(name, index, "late"), uniform=False).run()
+            except Deadlock:
+                hung += 1
+    assert hung > 0

@@ -226,7 +226,8 @@ def test_forward_replays_from_a_cuda_graph():
 def test_long_memory_keeps_state_precision(T):
     """Without decay (lower_bound = 0) the state remembers every token.  The fp32 state
     held in TMEM must stay within the fp32 tolerance over thousands of tokens; a state
-    rounded to bf16 at every chunk boundary (KDA_FWD_KERNEL=tcbf16) drifts past it."""
+    rounded to bf16 at every chunk boundary (KDA_KERNEL_BF16_STATE) drifts past it
+    (tests/test_gpu_ablations.py)."""
     w = Workload(f"mem{T}", 31, H=4, B=1, T=T, init_dtype=f32, final_dtype=f32, lower_bound=0.0)
     inp = make_inputs(w, "cpu")
     inp.beta.mul_(0.2)   # moderate writes: the memory stays long

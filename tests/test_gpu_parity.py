@@ -3,14 +3,18 @@
 * The five workloads' smaller variants (several chunks, ragged tails, an empty
   sequence) are compared element by element over whole tensors.
 * The five full-size workloads run in the launch configuration the benchmark
-  times; the oracle recomputes sampled (sequence, head) units one by one.
+  times, and are compared with the oracle over the whole of ``out`` and the whole
+  of ``final_state`` (the oracle runs one sequence, all heads, at a time), with the
+  tolerances of the stated contract: bf16 max |diff| <= 2e-2 and relative Frobenius
+  <= 1e-2, fp32 state relative Frobenius <= 5e-3.  Rows of ``out`` outside every
+  sequence keep a NaN sentinel, bit for bit.
 """
 import pytest
 import torch
 
 from gated_delta_rule_36_gb300.inputs import FULL_WORKLOADS, SMALL_WORKLOADS, make_inputs, workload
 
-from kda_testutil import check_full, check_units, oracle_full, oracle_units, run_gpu, seq_bounds
+from kda_testutil import check_full, check_whole_by_sequence, oracle_full, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -24,32 +28,11 @@ def test_small_workloads_whole_tensor(name):
     check_full(inp, out, final, ref_out, ref_final)
 
 
-def _sample_units(w, gen):
-    bounds = seq_bounds(w)
-    lens = [e - b for b, e in bounds]
-    order = sorted(range(len(lens)), key=lambda n: (-lens[n], n))
-    seqs = {order[0], order[-1]} | {int(x) for x in torch.randint(0, len(lens), (2,), generator=gen)}
-    units = set()
-    for n in seqs:
-        units.add((n, 0))
-        units.add((n, w.H - 1))
-        units.add((n, int(torch.randint(0, w.H, (1,), generator=gen))))
-    return sorted(units)
-
-
 @pytest.mark.parametrize("name", FULL_WORKLOADS)
-def test_full_workloads_sampled_units(name):
+def test_full_workloads_whole_tensor(name):
     w = workload(name)
+    # the large ones are drawn on the GPU (the same seeded tensors the benchmark draws)
     inp = make_inputs(w, "cuda" if name in ("long", "packed64") else "cpu")
     out, final, bits = run_gpu(inp)
     assert bits == 0
-    gen = torch.Generator().manual_seed(7)
-    units = _sample_units(w, gen)
-    if name == "long":
-        units = [(0, 0), (0, w.H - 1)]
-    ref = oracle_units(inp, units)
-    check_units(inp, out, final, ref)
-    # bit-exact indexing: rows outside every sequence stay untouched
-    last = seq_bounds(w)[-1][1]
-    assert torch.isnan(out.reshape(w.B * w.T, w.H, w.V)[last:].float()).all()
-    assert torch.isfinite(out.float()).all() if last == w.B * w.T else True
+    check_whole_by_sequence(inp, out, final, name)
