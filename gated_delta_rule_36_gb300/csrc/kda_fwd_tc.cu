@@ -165,6 +165,30 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
     return __all_sync(0xffffffffu, ok);
 }
 
+// Wind-down after an expired wait.  A group's named barriers are not bounded, so a warp
+// whose wait expired keeps meeting its group at every barrier the group still has ahead
+// (plain bar.sync, no waits and no work) until the sequence ends.  Its siblings either finish
+// normally or see a wait of their own expire (whatever the wound-down warp would have
+// produced never comes) and join it, so no warp is ever left at a barrier, and the fast path
+// keeps its code as it is.
+// Chain group: barrier k of chunk c (0: after the first decay, before chunk 0; 1: after
+// GEMM1 and -B2; 2: after U; 3: after the output staging; 4: after the next decay, for every
+// chunk but the last).
+__device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
+    if (k == 0) {
+        named_bar_sync(2, 128);
+        k = 1;
+    }
+    for (; c < nchunks; ++c, k = 1)
+        for (; k <= (c + 1 < nchunks ? 4 : 3); ++k) named_bar_sync(2, 128);
+}
+// Prep group: barrier k of its local chunk j (0: after phase A, 1: after phase B, 2: after
+// phase C).
+__device__ __noinline__ void prep_wind_down(int j, int k, int nloc) {
+    for (; j < nloc; ++j, k = 0)
+        for (; k < 3; ++k) named_bar_sync(1, PREP_THREADS);
+}
+
 // 16 state values of row `off` (element offset) as fp32 bits (zeros without an initial state).
 __device__ __forceinline__ void load_state16(const FwdParams& p, size_t off, uint32_t (&r)[16]) {
     if (!p.init_state) {
@@ -400,16 +424,15 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         fence_proxy_async_smem();
     }
     tmem_wait_st();
-    // Every barrier of the group that follows a bounded wait reduces the warps' verdicts
-    // (bar.red.and): a warp whose wait expired still arrives, skipping its work, and the
-    // whole group then winds down together, so no warp is left waiting at a barrier.
     bool ok = warp_wait(bar_addr(u, kCl ? B_FULLOP : B_AREADY), 0, p.status, 256);   // a of chunk 0
     if (ok) {
         copy_and_decay<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
         tmem_wait_st();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+    } else {
+        chain_wind_down(0, 0, u.nchunks);
     }
-    tc_fence_before();
-    ok = named_bar_all(2, 128, ok);
 
     int sc = 0, kq = 0;   // (cluster home) slot c % NS and round c / NS
     // chain trace (cluster schedule): SM clock at KDA_TRACE_POINTS steps of each chunk of one unit
@@ -432,16 +455,14 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if constexpr (!kCl) {
             if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
             // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
-            ok = warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256);
+            if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) { chain_wind_down(c, 1, u.nchunks); break; }
             // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
             beta_next = beta_ahead;
-            if (ok && w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
+            if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
         }
-        if (ok && w == W_MMA) {
+        if (w == W_MMA) {
             if (kCl && pt == 32) stamp(c, 1);
-            ok = warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256);
-        }
-        if (ok && w == W_MMA) {
+            if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) { chain_wind_down(c, 1, u.nchunks); break; }
             tc_fence_after();
             if (kCl && pt == 32) stamp(c, 2);
             auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
@@ -464,19 +485,17 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
 
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
-        ok = ok && warp_wait(bar_addr(u, B_G1), cpar, p.status);
-        if (ok) {
-            tc_fence_after();
-            if (kCl && pt == 0) stamp(c, 4);
-            p_cols_to_bf16(lane_addr);
-            if (kCl && pt == 0) stamp(c, 5);
-        }
+        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) { chain_wind_down(c, 1, u.nchunks); break; }
+        tc_fence_after();
+        if (kCl && pt == 0) stamp(c, 4);
+        p_cols_to_bf16(lane_addr);
+        if (kCl && pt == 0) stamp(c, 5);
         if constexpr (!kCl) {
-            ok = ok && warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64);
-            if (ok && refill && w == W_BETA) put_beta(u, s, lane, beta_next);
+            if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) { chain_wind_down(c, 1, u.nchunks); break; }
+            if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
         }
         tc_fence_before();
-        if (!named_bar_all(2, 128, ok)) break;
+        named_bar_sync(2, 128);
         if (kCl && pt == 0) stamp(c, 6);
         if (w == W_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
             tc_fence_after();
@@ -494,13 +513,11 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
 
         // U -> bf16 -> TMEM: A operand of GEMM3
-        ok = warp_wait(bar_addr(u, B_G2), cpar, p.status);
-        if (ok) {
-            tc_fence_after();
-            p_cols_to_bf16(lane_addr);
-        }
+        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down(c, 2, u.nchunks); break; }
+        tc_fence_after();
+        p_cols_to_bf16(lane_addr);
         tc_fence_before();
-        if (!named_bar_all(2, 128, ok)) break;
+        named_bar_sync(2, 128);
         if (w == W_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
             tc_fence_after();
             auto br = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_KR + kk * 2048, 4096, 1024); };
@@ -521,19 +538,18 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 tc_commit(bar_addr(u, B_G3));
             }
         }
-        ok = warp_wait(bar_addr(u, B_G3), cpar, p.status);
-        if (ok) {
-            tc_fence_after();
-            if constexpr (kCl) {
-                // the slot's pulled operands have been read for the last time
-                if (pt == 0) mbar_arrive(bar_addr(u, B_HFREE + s));
-            } else {
-                // The slot's q, k, g regions have been read for the last time: refill them with
-                // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
-                if (refill) {
-                    if (pt == T_TMA) load_qkg(maps, u, c + NSLOT, s);
-                    issued = c + NSLOT + 1;
-                }
+        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down(c, 3, u.nchunks); break; }
+        tc_fence_after();
+
+        if constexpr (kCl) {
+            // the slot's pulled operands have been read for the last time
+            if (pt == 0) mbar_arrive(bar_addr(u, B_HFREE + s));
+        } else {
+            // The slot's q, k, g regions have been read for the last time: refill them with
+            // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
+            if (refill) {
+                if (pt == T_TMA) load_qkg(maps, u, c + NSLOT, s);
+                issued = c + NSLOT + 1;
             }
         }
 
@@ -544,9 +560,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // thread two adjacent tokens of one state row, and stmatrix.trans writes 8 tokens x
         // 8 rows per matrix as 16-byte rows, conflict-free under the swizzle.
         const bool full = chunk_valid(u, c) == CH;
-        if (!ok) {
-            // G3 never came: nothing to stage
-        } else if (full) {
+        if (full) {
             const uint32_t tile = slot + SL_V;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {   // lanes 32 w + 16 hf .. + 15
@@ -586,7 +600,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (!named_bar_all(2, 128, ok)) break;
+        named_bar_sync(2, 128);
         if (pt == T_STORE) {
             const int64_t t0 = u.bos + (int64_t)c * CH;
             const int nvalid = chunk_valid(u, c);
@@ -604,20 +618,19 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const int s1 = kCl ? (s + 1 == NS ? 0 : s + 1) : (s ^ 1);
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
-            if constexpr (kCl)
-                ok = warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256);
-            else
-                ok = warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256);
-            if (ok) {
-                const float* a_next = reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A);
-                if constexpr (kWarpIssue)
-                    copy_and_decay_pipelined<kBf16State>(lane_addr, a_next);
-                else
-                    copy_and_decay<kBf16State>(lane_addr, a_next);
-                tmem_wait_st();
+            if constexpr (kCl) {
+                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down(c, 4, u.nchunks); break; }
+            } else {
+                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down(c, 4, u.nchunks); break; }
             }
+            const float* a_next = reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A);
+            if constexpr (kWarpIssue)
+                copy_and_decay_pipelined<kBf16State>(lane_addr, a_next);
+            else
+                copy_and_decay<kBf16State>(lane_addr, a_next);
+            tmem_wait_st();
             tc_fence_before();
-            if (!named_bar_all(2, 128, ok)) break;
+            named_bar_sync(2, 128);
             // the output store has had the copy-and-decay pass to read the staging tile: the
             // region takes chunk c + 2's v
             if (pt == T_STORE && refill) {
@@ -697,9 +710,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
         const int s = j & 1;
         const uint32_t kpar = (j >> 1) & 1;
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        // a warp whose wait expires still meets the group at its next barrier, which
-        // reduces the verdicts (bar.red.and): the group then winds down together
-        const bool okA = warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128);
+        if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) { prep_wind_down(j, 0, nloc); return; }
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
         const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
@@ -708,7 +719,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
         //      4 tokens x 4 channels; the two are independent and written so that they overlap
         uint2 qv[4], kv[4];
         float2 G01[4], G23[4];
-        if (okA) {
+        {
             const int row = pt >> 2, part = pt & 3;   // rows 0-31 q, 32-63 k; 32 elements per thread
             const unsigned char* rp = gslot + (row < 32 ? SL_RAWQ + row * 256 : SL_RAWK + (row - 32) * 256);
             uint4 w4[4];
@@ -777,7 +788,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
                 if (row < 32) rq[tok] = rn; else rk[tok] = rn;
             }
         }
-        if (!named_bar_all(1, PREP_THREADS, okA)) return;   // raw q/k/g are no longer read after this point
+        named_bar_sync(1, PREP_THREADS);   // raw q/k/g are no longer read after this point
 
         // ---- B: prefix combine, centered operands
         {
@@ -856,7 +867,6 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
             // blocks (mt, nb) of warp pw: (0,1) [all zero], (0,0), (1,0), (1,1) for pw & 3 = 0..3
             const int bi = pw & 3, mat = pw >> 2, mt = bi >> 1, nb = (bi & 1) ^ (1 - mt);
             const unsigned char* Ab = mat ? qcs : kcs;
-            bool okC = true;
             float acc[2][4], acc2[2][4];
 #pragma unroll
             for (int t = 0; t < 2; ++t)
@@ -884,10 +894,10 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[t][e] += acc2[t][e];
                 // L is rewritten only once the inverse warp has read the previous chunk's
-                if (mat == 0 && j > 0) okC = warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status);
+                if (mat == 0 && j > 0 && !warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status)) { prep_wind_down(j, 2, nloc); return; }
             }
 #pragma unroll
-            for (int t = 0; t < 2 && okC; ++t) {
+            for (int t = 0; t < 2; ++t) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int i = mt * 16 + gq + hf * 8;
@@ -905,9 +915,9 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
                     }
                 }
             }
-            fence_proxy_async_smem();   // Q_d, K_d, K_r, Mqk are read by the tensor core
-            if (!named_bar_all(1, PREP_THREADS, okC)) return;
         }
+        fence_proxy_async_smem();   // Q_d, K_d, K_r, Mqk are read by the tensor core
+        named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_FULLP + s));
     }
 }

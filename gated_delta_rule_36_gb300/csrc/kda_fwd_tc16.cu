@@ -89,6 +89,25 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
     return __all_sync(0xffffffffu, ok);
 }
 
+// Wind-down after an expired wait: the warp keeps meeting its group at every named barrier
+// the group still has ahead (plain bar.sync, no waits, no work) until the sequence ends, so
+// no sibling is ever left at a barrier and the fast path keeps its code.  Chain group:
+// barrier k of chunk c (0: before chunk 0; 1: after GEMM1; 2: after U; 3: after the output
+// staging; 4: after the next decay, for every chunk but the last).
+__device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
+    if (k == 0) {
+        named_bar_sync(2, 128);
+        k = 1;
+    }
+    for (; c < nchunks; ++c, k = 1)
+        for (; k <= (c + 1 < nchunks ? 4 : 3); ++k) named_bar_sync(2, 128);
+}
+// Prep group: barrier k (0-3) of chunk c, the last one after the wait for the next boxes.
+__device__ __noinline__ void prep_wind_down(int c, int k, int nchunks) {
+    for (; c < nchunks; ++c, k = 0)
+        for (; k < 4; ++k) named_bar_sync(1, PREP_THREADS);
+}
+
 __device__ __forceinline__ void load_state16(const FwdParams& p, size_t off, uint32_t (&r)[16]) {
     if (!p.init_state) {
 #pragma unroll
@@ -252,15 +271,15 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         fence_proxy_async_smem();
     }
     tmem_wait_st();
-    // every barrier of the group that follows a bounded wait reduces the warps' verdicts
-    // (bar.red.and), so a warp whose wait expired never leaves a sibling at a barrier
     bool ok = warp_wait(bar_addr(u, B_AREADY), 0, p.status, 256);
     if (ok) {
         copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
         tmem_wait_st();
+        tc_fence_before();
+        named_bar_sync(2, 128);
+    } else {
+        chain_wind_down(0, 0, u.nchunks);
     }
-    tc_fence_before();
-    ok = named_bar_all(2, 128, ok);
 
 #pragma unroll 1
     for (int c = 0; ok && c < u.nchunks; ++c) {
@@ -269,11 +288,11 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const uint32_t slot = u.base + s * SLOT_BYTES;
         const bool refill = c + NSLOT < u.nchunks;
         if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
-        ok = warp_wait(bar_addr(u, B_FULL + s), kpar, p.status, 256);
+        if (!warp_wait(bar_addr(u, B_FULL + s), kpar, p.status, 256)) { chain_wind_down(c, 1, u.nchunks); break; }
         float beta_next = 0.f;
-        if (ok && refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
-        if (ok && w == 1) ok = warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256);
-        if (ok && w == 1) {
+        if (refill && w == W_BETA) beta_next = load_beta(p, u, c + NSLOT, lane);
+        if (w == 1) {
+            if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) { chain_wind_down(c, 1, u.nchunks); break; }
             tc_fence_after();
             if (pt == T_MMA) {
 #pragma unroll
@@ -286,40 +305,36 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             }
         }
 
-        ok = ok && warp_wait(bar_addr(u, B_G1), cpar, p.status);
-        if (ok) {
-            tc_fence_after();
-            if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
-            p_cols_to_bf16(lane_addr);   // -R = P - V^T
-        }
+        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) { chain_wind_down(c, 1, u.nchunks); break; }
+        tc_fence_after();
+        if (refill && w == W_BETA) put_beta(u, c + NSLOT, lane, beta_next);
+        p_cols_to_bf16(lane_addr);   // -R = P - V^T
         tc_fence_before();
-        if (!named_bar_all(2, 128, ok)) break;
+        named_bar_sync(2, 128);
         if (pt == T_MMA) {   // GEMM2 U = (-R) (-B2)
             tc_fence_after();
             tc_mma_ts(u.tmem + TM_P, u.tmem + TM_SB, make_sdesc_kmajor_noswizzle(slot + SL_INV, 128, 256), idesc2, 0u);
             tc_commit(bar_addr(u, B_G2));
         }
-        ok = warp_wait(bar_addr(u, B_G2), cpar, p.status);
-        if (ok) {
-            tc_fence_after();
-            p_cols_to_bf16(lane_addr);   // U
-        }
+        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down(c, 2, u.nchunks); break; }
+        tc_fence_after();
+        p_cols_to_bf16(lane_addr);   // U
         tc_fence_before();
-        if (!named_bar_all(2, 128, ok)) break;
+        named_bar_sync(2, 128);
         if (pt == T_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
             tc_fence_after();
             tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB, make_sdesc_mnmajor_sw128(slot + SL_KR, 2048, 1024), idesc3, 1u);
             tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB, make_sdesc_kmajor_noswizzle(slot + SL_MQT, 128, 256), idesc2, 1u);
             tc_commit(bar_addr(u, B_G3));
         }
-        ok = warp_wait(bar_addr(u, B_G3), cpar, p.status);
-        if (ok) tc_fence_after();
-        if (ok && refill) {
+        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down(c, 3, u.nchunks); break; }
+        tc_fence_after();
+        if (refill) {
             if (pt == T_TMA) load_qkg(maps, u, c + NSLOT);
             issued = c + NSLOT + 1;
         }
 
-        if (ok) {   // O of this chunk -> staging tile [token][v] in the slot's v region
+        {   // O of this chunk -> staging tile [token][v] in the slot's v region
             unsigned char* ost = u.gbase + s * SLOT_BYTES + SL_V + 2 * v;
             uint32_t o[16];
             tmem_ld16(lane_addr + TM_O, o);
@@ -333,7 +348,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        if (!named_bar_all(2, 128, ok)) break;
+        named_bar_sync(2, 128);
         if (pt == T_STORE) {
             const int64_t t0 = u.bos + (int64_t)c * C16;
             const int nvalid = chunk_valid(u, c);
@@ -352,13 +367,11 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
 
         if (c + 1 < u.nchunks) {
-            ok = warp_wait(bar_addr(u, B_AREADY + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 256);
-            if (ok) {
-                copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
-                tmem_wait_st();
-            }
+            if (!warp_wait(bar_addr(u, B_AREADY + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down(c, 4, u.nchunks); break; }
+            copy_and_decay(lane_addr, reinterpret_cast<const float*>(u.gbase + (s ^ 1) * SLOT_BYTES + SL_A));
+            tmem_wait_st();
             tc_fence_before();
-            if (!named_bar_all(2, 128, ok)) break;
+            named_bar_sync(2, 128);
         } else {
 #pragma unroll 1
             for (int piece = 0; piece < 8; ++piece) {
@@ -407,9 +420,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
         const int s = c & 1;
         const uint32_t kpar = (c >> 1) & 1;
         unsigned char* gslot = u.gbase + s * SLOT_BYTES;
-        // a warp whose wait expires still meets the group at its next barrier, which reduces
-        // the verdicts (bar.red.and): the group then winds down together
-        const bool okA = c > 0 || warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128);
+        if (c == 0 && !warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) { prep_wind_down(0, 0, u.nchunks); return; }
         const int64_t t0 = u.bos + (int64_t)c * C16;
         const int nvalid = (int)((u.eos - t0) < C16 ? (u.eos - t0) : C16);
         const float* bs = reinterpret_cast<const float*>(gslot + SL_BETA);
@@ -466,7 +477,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
                 if (row < C16) rq[tok] = rn; else rk[tok] = rn;
             }
         }
-        if (!named_bar_all(1, PREP_THREADS, okA)) return;   // raw q/k/g are no longer read after this point
+        named_bar_sync(1, PREP_THREADS);   // raw q/k/g are no longer read after this point
 
         // ---- B: prefix combine, operands (no anchor: 2^G and 2^-G stay normal)
         {
@@ -587,8 +598,11 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt) {
             }
         }
         fence_proxy_async_smem();
-        const bool okN = c + 1 >= u.nchunks || warp_wait(bar_addr(u, B_FULLTMA + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 128);
-        if (!named_bar_all(1, PREP_THREADS, okN)) return;
+        if (c + 1 < u.nchunks && !warp_wait(bar_addr(u, B_FULLTMA + (s ^ 1)), ((c + 1) >> 1) & 1, p.status, 128)) {
+            prep_wind_down(c, 3, u.nchunks);
+            return;
+        }
+        named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_FULL + s));
     }
 }

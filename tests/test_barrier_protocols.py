@@ -1,6 +1,6 @@
 """Models of the prefill kernel's mbarrier protocols, run under random interleavings: the
-cluster schedule's hand-offs between CTAs (first part) and the two-slot ring inside one CTA
-(second part).
+cluster schedule's hand-offs between CTAs (first part), the two-slot ring inside one CTA
+(second part), and the ring warp by warp when a bounded wait expires (third part).
 
 The cluster schedule of the prefill kernel splits a unit over four CTAs: the home CTA runs
 the chain over three slots, helper h prepares chunks c = h (mod 3) in its own two slots, and
@@ -321,17 +321,19 @@ def test_ring_without_lfree_overwrites_l():
 # ---------------------------------------------------------------------------------------
 # Expiry and wind-down of the two-slot ring, warp by warp.  Every mbarrier wait in the
 # kernel is bounded: when its limit expires the waiting warp sets the timeout bit and gives
-# up.  The groups' named barriers (bar.sync / bar.red) are not bounded, so a warp must never
-# be left at one after a sibling has given up.  The kernel makes every group barrier that
-# follows a bounded wait a reduction of the warps' verdicts (bar.red.and): a warp whose wait
-# expired still arrives (skipping its work), and the group leaves the loop together.  The
-# model replays, per warp, the waits, arrivals and barriers of the chain group (4 warps: warp
-# 1 issues the MMAs, warp 2 the q/k/g box loads and beta, warp 3 the stores and v loads), the
-# prep group (8 warps; warps 1-3 wait for LFREE before writing L) and the inverse warp, with
-# the box loads and MMA commits as asynchronous engines.  One producer arrival is withheld,
-# or delayed past the waiters' limit, and waits may expire at any poll past the limit.  Every
-# warp must then reach the kernel's final __syncthreads.  The same model with the earlier
-# per-warp verdicts (plain bar.sync, each warp leaving on its own) must be able to hang.
+# up.  The groups' named barriers (bar.sync) are not bounded, so a warp must never be left
+# at one after a sibling has given up.  In the kernel a warp whose wait expired winds down:
+# it keeps meeting its group at every named barrier the group still has ahead (plain
+# bar.sync, no waits, no work) until the sequence ends.  Its siblings either finish normally
+# or see a wait of their own expire (what the wound-down warp would have produced never
+# comes) and wind down too.  The model replays, per warp, the waits, arrivals and barriers of
+# the chain group (4 warps: warp 1 issues the MMAs, warp 2 the q/k/g box loads and beta,
+# warp 3 the stores and v loads), the prep group (8 warps; warps 1-3 wait for LFREE before
+# writing L) and the inverse warp, with the box loads and MMA commits as asynchronous
+# engines.  One producer arrival is withheld, or delayed past the waiters' limit, and waits
+# may expire at any poll past the limit.  Every warp must then reach the kernel's final
+# __syncthreads.  The same model without the wind-down (each warp leaving the loop on its own
+# verdict, the earlier form) must be able to hang.
 # ---------------------------------------------------------------------------------------
 
 UNBOUNDED = 2   # blocked on a named barrier: only other warps' arrivals can release it
@@ -339,30 +341,27 @@ UNBOUNDED = 2   # blocked on a named barrier: only other warps' arrivals can rel
 
 
 class NamedBar:
-    """bar.sync / bar.red.and over `count` warps (generation by generation)."""
+    """bar.sync over `count` warps (generation by generation)."""
 
     def __init__(self, count):
-        self.count, self.gen, self.arrived, self.acc, self.result = count, 0, 0, True, {}
+        self.count, self.gen, self.arrived = count, 0, 0
 
-    def sync(self, pred=True):
+    def sync(self):
         g = self.gen
         self.arrived += 1
-        self.acc = self.acc and pred
         if self.arrived == self.count:
-            self.result[g] = self.acc
-            self.gen, self.arrived, self.acc = g + 1, 0, True
+            self.gen, self.arrived = g + 1, 0
         while self.gen == g:
             yield (UNBOUNDED, self, g)
-        return self.result[g]
 
 
 class RingRun:
     """One CTA of the two-slot ring over n chunks.  `perturb` = (barrier name, completion
-    index, "withhold" | "late"); `limit` = polls before a wait may expire; `uniform` = the
-    kernel's reduced verdicts (False: the earlier per-warp verdicts)."""
+    index, "withhold" | "late"); `limit` = polls before a wait may expire; `wind_down` = the
+    kernel's wind-down after an expired wait (False: the earlier form, which just leaves)."""
 
-    def __init__(self, n, seed, perturb=None, limit=40, uniform=True):
-        self.n, self.rng, self.perturb, self.limit, self.uniform = n, random.Random(seed), perturb, limit, uniform
+    def __init__(self, n, seed, perturb=None, limit=40, wind_down=True):
+        self.n, self.rng, self.perturb, self.limit, self.wind_down = n, random.Random(seed), perturb, limit, wind_down
         self.bars, self.engines, self.timeouts, self.consumed = {}, [], 0, []
         self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(13)
         self.fulltma_fill = {0: 0, 1: 0}
@@ -422,14 +421,29 @@ class RingRun:
             self.fulltma(c)
         self.engines.append(run())
 
-    def group_bar(self, gbar, ok):
-        """The group barrier after a bounded wait: reduced verdict, or the earlier plain
-        bar.sync that only the warps still in the loop reach."""
-        if self.uniform:
-            return (yield from gbar.sync(ok))
-        if ok:
-            yield from gbar.sync(True)
-        return ok
+    def chain_wind_down(self, c, k):
+        """Barrier k of chunk c onwards (0: before chunk 0; 1: after GEMM1 and -B2; 2: after
+        U; 3: after the output staging; 4: after the next decay, all chunks but the last)."""
+        if not self.wind_down:
+            return
+        if k == 0:
+            yield from self.chain_bar.sync()
+            k = 1
+        while c < self.n:
+            while k <= (4 if c + 1 < self.n else 3):
+                yield from self.chain_bar.sync()
+                k += 1
+            c, k = c + 1, 1
+
+    def prep_wind_down(self, j, k):
+        """Barrier k (0: after phase A, 1: after phase B, 2: after phase C) of chunk j onwards."""
+        if not self.wind_down:
+            return
+        while j < self.n:
+            while k < 3:
+                yield from self.prep_bar.sync()
+                k += 1
+            j, k = j + 1, 0
 
     def chain_warp(self, w):
         n = self.n
@@ -442,47 +456,51 @@ class RingRun:
                 if w == 3:
                     self.engine("FULLV", c >> 1, c)
             ok = yield from self.bwait(self.bar("AREADY", 0), 0)
-            ok = yield from self.group_bar(self.chain_bar, ok)
-            for c in range(n):
-                if not ok:
-                    break
+            if ok:
+                yield from self.chain_bar.sync()
+            else:
+                yield from self.chain_wind_down(0, 0)
+            for c in range(n if ok else 0):
                 s, k, refill = c & 1, c >> 1, c + 2 < n
-                ok = yield from self.bwait(self.bar("FULLP", s), k)
-                if ok and w == 1:
-                    ok = yield from self.bwait(self.bar("FULLV", s), k)
-                if ok and w == 1:
-                    self.engine("G1", c)
-                if ok:
-                    ok = yield from self.bwait(self.bar("G1"), c)
-                if ok:
-                    ok = yield from self.bwait(self.bar("FULLD", s), k)
-                if ok and refill and w == 2:
-                    self.fulltma(c + 2)                   # beta of chunk c + 2
-                ok = yield from self.group_bar(self.chain_bar, ok)
-                if not ok:
+                if not (yield from self.bwait(self.bar("FULLP", s), k)):
+                    yield from self.chain_wind_down(c, 1)
                     break
+                if w == 1:
+                    if not (yield from self.bwait(self.bar("FULLV", s), k)):
+                        yield from self.chain_wind_down(c, 1)
+                        break
+                    self.engine("G1", c)
+                if not (yield from self.bwait(self.bar("G1"), c)):
+                    yield from self.chain_wind_down(c, 1)
+                    break
+                if not (yield from self.bwait(self.bar("FULLD", s), k)):
+                    yield from self.chain_wind_down(c, 1)
+                    break
+                if refill and w == 2:
+                    self.fulltma(c + 2)                   # beta of chunk c + 2
+                yield from self.chain_bar.sync()
                 if w == 1:
                     self.engine("G2", c)
-                ok = yield from self.bwait(self.bar("G2"), c)
-                ok = yield from self.group_bar(self.chain_bar, ok)
-                if not ok:
+                if not (yield from self.bwait(self.bar("G2"), c)):
+                    yield from self.chain_wind_down(c, 2)
                     break
+                yield from self.chain_bar.sync()
                 if w == 1:
                     self.engine("G3", c)
-                ok = yield from self.bwait(self.bar("G3"), c)
-                if ok and refill and w == 2:
+                if not (yield from self.bwait(self.bar("G3"), c)):
+                    yield from self.chain_wind_down(c, 3)
+                    break
+                if refill and w == 2:
                     self.load_qkg(c + 2)
                     issued_qkg = c + 3
-                ok = yield from self.group_bar(self.chain_bar, ok)
-                if not ok:
-                    break
+                yield from self.chain_bar.sync()
                 if w == 0:
                     self.consumed.append(c)
                 if c + 1 < n:
-                    ok = yield from self.bwait(self.bar("AREADY", s ^ 1), (c + 1) >> 1)
-                    ok = yield from self.group_bar(self.chain_bar, ok)
-                    if not ok:
+                    if not (yield from self.bwait(self.bar("AREADY", s ^ 1), (c + 1) >> 1)):
+                        yield from self.chain_wind_down(c, 4)
                         break
+                    yield from self.chain_bar.sync()
                     if w == 3 and refill:
                         self.engine("FULLV", (c + 2) >> 1, s)
                         issued_v = c + 3
@@ -499,19 +517,17 @@ class RingRun:
     def prep_warp(self, pw):
         for j in range(self.n):
             s, k = j & 1, j >> 1
-            ok = yield from self.bwait(self.bar("FULLTMA", s), k)
-            ok = yield from self.group_bar(self.prep_bar, ok)
-            if not ok:
+            if not (yield from self.bwait(self.bar("FULLTMA", s), k)):
+                yield from self.prep_wind_down(j, 0)
                 break
-            yield from self.prep_bar.sync()               # end of phase B: no wait before it
+            yield from self.prep_bar.sync()               # end of phase A
+            yield from self.prep_bar.sync()               # end of phase B
             if pw == 0:
                 self.arrive("AREADY", j >> 1, s)
-            ok = True
-            if pw in (1, 2, 3) and j > 0:
-                ok = yield from self.bwait(self.bar("LFREE"), j - 1)
-            ok = yield from self.group_bar(self.prep_bar, ok)
-            if not ok:
+            if pw in (1, 2, 3) and j > 0 and not (yield from self.bwait(self.bar("LFREE"), j - 1)):
+                yield from self.prep_wind_down(j, 2)
                 break
+            yield from self.prep_bar.sync()               # end of phase C
             if pw == 0:
                 self.arrive("FULLP", j >> 1, s)
         yield from self.cta_bar.sync()
@@ -520,8 +536,7 @@ class RingRun:
     def inverse_warp(self):
         for j in range(self.n):
             s, k = j & 1, j >> 1
-            ok = yield from self.bwait(self.bar("FULLP", s), k)
-            if not ok:
+            if not (yield from self.bwait(self.bar("FULLP", s), k)):
                 break
             self.arrive("LFREE", j)
             self.arrive("FULLD", j >> 1, s)
@@ -550,13 +565,14 @@ class RingRun:
 
 
 PERTURB = [("FULLD", 1), ("FULLP", 2), ("AREADY", 1), ("LFREE", 2), ("G1", 3), ("G2", 0), ("G3", 4),
-           ("FULLV", 1), ("FULLTMA", 3)]
+           ("FULLV", 1), ("FULLTMA", 3), ("AREADY", 0), ("FULLTMA", 0)]
 
 
-def test_ring_model_without_faults_finishes_every_chunk():
+@pytest.mark.parametrize("n", [1, 2, 3, 9])
+def test_ring_model_without_faults_finishes_every_chunk(n):
     for seed in range(10):
-        r = RingRun(9, seed, limit=10 ** 9).run()
-        assert r.timeouts == 0 and r.consumed == list(range(9))
+        r = RingRun(n, seed, limit=10 ** 9).run()
+        assert r.timeouts == 0 and r.consumed == list(range(n))
 
 
 @pytest.mark.parametrize("mode", ["withhold", "late"])
@@ -564,20 +580,21 @@ def test_ring_model_without_faults_finishes_every_chunk():
 def test_every_warp_winds_down_after_an_expired_wait(name, index, mode):
     """One arrival withheld (or delayed past the waiters' limit): waits expire, and every
     warp of every role still reaches the end of the kernel."""
-    for seed in range(30):
-        r = RingRun(10, seed, perturb=(name, index, mode)).run()
-        if mode == "withhold":
-            assert r.timeouts > 0
+    for n in (6, 10):
+        for seed in range(30):
+            r = RingRun(n, seed, perturb=(name, index, mode)).run()
+            if mode == "withhold":
+                assert r.timeouts > 0
 
 
-def test_per_warp_verdicts_can_leave_a_warp_at_a_barrier():
-    """The earlier form (each warp acting on its own verdict before a plain bar.sync) hangs
-    when a phase completes just after some of the group's waits expired."""
+def test_leaving_without_wind_down_can_leave_a_warp_at_a_barrier():
+    """The earlier form (a warp whose wait expired leaves the loop at once) hangs when a
+    phase completes just after some of the group's waits expired."""
     hung = 0
     for name, index in PERTURB:
         for seed in range(30):
             try:
-                RingRun(10, seed, perturb=(name, index, "late"), uniform=False).run()
+                RingRun(10, seed, perturb=(name, index, "late"), wind_down=False).run()
             except Deadlock:
                 hung += 1
     assert hung > 0
