@@ -77,7 +77,7 @@ constexpr uint32_t OFF_QC = NSLOT * SLOT_BYTES;   // Q_c
 constexpr uint32_t OFF_KC = OFF_QC + 8192;        // K_c
 constexpr uint32_t OFF_KI = OFF_KC + 8192;        // K_i
 constexpr uint32_t OFF_MISC = OFF_KI + 8192;      // tot[8][128], rq[32], rk[32]
-constexpr uint32_t MISC_BYTES = (8 * 128 + 64) * 4;
+constexpr uint32_t MISC_BYTES = (8 * 128 + 64 + 128) * 4;
 // L = strictLower(diag(beta) K_c K_i^T) in fp32, its three nonzero 16 x 16 blocks, each
 // column-major with a column stride of LB floats: L11 at 0, L22 at 336 (16 floats past its
 // 320-float block, so that the two half-warps of the substitution read different banks), L21 at 672.
@@ -182,11 +182,11 @@ __device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
     for (; c < nchunks; ++c, k = 1)
         for (; k <= (c + 1 < nchunks ? 4 : 3); ++k) named_bar_sync(2, 128);
 }
-// Prep group: barrier k of its local chunk j (0: after phase A, 1: after phase B, 2: after
-// phase C).
+// Prep group: barrier k of its local chunk j (0: after phase A, 1: after the prefix scan,
+// 2: after phase B, 3: after phase C).
 __device__ __noinline__ void prep_wind_down(int j, int k, int nloc) {
     for (; j < nloc; ++j, k = 0)
-        for (; k < 3; ++k) named_bar_sync(1, PREP_THREADS);
+        for (; k < 4; ++k) named_bar_sync(1, PREP_THREADS);
 }
 
 // 16 state values of row `off` (element offset) as fp32 bits (zeros without an initial state).
@@ -701,6 +701,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
     unsigned char* kis = u.gbase + OFF_KI;
     float* Lb = reinterpret_cast<float*>(u.gbase + OFF_L);
     float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
+    float* totg = tot + PREP_WARPS * HD + 64;                              // [128]
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
 
@@ -790,19 +791,32 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
         }
         named_bar_sync(1, PREP_THREADS);   // raw q/k/g are no longer read after this point
 
-        // ---- B: prefix combine, centered operands
+        // ---- prefix across the warps: thread (pw, lane) scans the 4 partials of warps 4 h .. 4 h + 3
+        //      (h = lane / 16) of channel 16 pw + lane % 16, in place: tot[qq] becomes the exclusive
+        //      prefix of warp qq, and totg the chunk total
         {
-            float2 T01 = make_float2(0.f, 0.f), T23 = make_float2(0.f, 0.f);
+            const int ch = 16 * pw + (lane & 15), h = lane >> 4;
+            float* col = tot + 4 * h * HD + ch;
+            const float x0 = col[0], x1 = col[HD], x2 = col[2 * HD], x3 = col[3 * HD];
+            const float s2 = x0 + x1, s3 = s2 + x2, s4 = s3 + x3;
+            const float other = __shfl_xor_sync(0xffffffffu, s4, 16);
+            const float base = h ? other : 0.f;
+            col[0] = base;
+            col[HD] = base + x0;
+            col[2 * HD] = base + s2;
+            col[3 * HD] = base + s3;
+            if (h == 0) totg[ch] = s4 + other;
+        }
+        named_bar_sync(1, PREP_THREADS);
+        // ---- B: centered operands
+        {
+            float2 T01, T23;
             {
-                float2 off01 = make_float2(0.f, 0.f), off23 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int qq = 0; qq < PREP_WARPS; ++qq) {
-                    const float4 t4 = *reinterpret_cast<const float4*>(tot + qq * HD + c0);
-                    const float2 a01 = make_float2(t4.x, t4.y), a23 = make_float2(t4.z, t4.w);
-                    if (qq < pw) { off01 = __fadd2_rn(off01, a01); off23 = __fadd2_rn(off23, a23); }
-                    T01 = __fadd2_rn(T01, a01);
-                    T23 = __fadd2_rn(T23, a23);
-                }
+                const float4 o4 = *reinterpret_cast<const float4*>(tot + pw * HD + c0);
+                const float4 t4 = *reinterpret_cast<const float4*>(totg + c0);
+                float2 off01 = make_float2(o4.x, o4.y), off23 = make_float2(o4.z, o4.w);
+                T01 = make_float2(t4.x, t4.y);
+                T23 = make_float2(t4.z, t4.w);
                 const float2 mC = make_float2(-Cst, -Cst);
                 off01 = __fadd2_rn(off01, mC);
                 off23 = __fadd2_rn(off23, mC);
@@ -894,7 +908,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[t][e] += acc2[t][e];
                 // L is rewritten only once the inverse warp has read the previous chunk's
-                if (mat == 0 && j > 0 && !warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status)) { prep_wind_down(j, 2, nloc); return; }
+                if (mat == 0 && j > 0 && !warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status)) { prep_wind_down(j, 3, nloc); return; }
             }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {

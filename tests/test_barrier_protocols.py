@@ -436,11 +436,12 @@ class RingRun:
             c, k = c + 1, 1
 
     def prep_wind_down(self, j, k):
-        """Barrier k (0: after phase A, 1: after phase B, 2: after phase C) of chunk j onwards."""
+        """Barrier k (0: after phase A, 1: after the prefix scan, 2: after phase B, 3: after
+        phase C) of chunk j onwards."""
         if not self.wind_down:
             return
         while j < self.n:
-            while k < 3:
+            while k < 4:
                 yield from self.prep_bar.sync()
                 k += 1
             j, k = j + 1, 0
@@ -521,11 +522,12 @@ class RingRun:
                 yield from self.prep_wind_down(j, 0)
                 break
             yield from self.prep_bar.sync()               # end of phase A
+            yield from self.prep_bar.sync()               # end of the prefix scan
             yield from self.prep_bar.sync()               # end of phase B
             if pw == 0:
                 self.arrive("AREADY", j >> 1, s)
             if pw in (1, 2, 3) and j > 0 and not (yield from self.bwait(self.bar("LFREE"), j - 1)):
-                yield from self.prep_wind_down(j, 2)
+                yield from self.prep_wind_down(j, 3)
                 break
             yield from self.prep_bar.sync()               # end of phase C
             if pw == 0:
