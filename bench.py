@@ -153,7 +153,7 @@ def barrier(world: int):
 
 METRIC = "KDA prefill tokens/s at 1 GB300 (TFLOP/s and roofline fractions alongside)"
 # --kernel: the default kernel or one of the design alternatives (kda_fwd_ex's kernel field)
-KERNELS = {"default": 0x000, "chunk16": 0x100, "register_state": 0x200, "bf16_state": 0x300}
+KERNELS = {"default": 0x000, "chunk16": 0x100, "register_state": 0x200, "bf16_state": 0x300, "smem_state": 0x400}
 
 
 def bench_config(w, world: int) -> dict:

@@ -29,6 +29,7 @@ EXPORTED = ("kda_workspace_size", "kda_fwd", "kda_status_string", "kda_last_erro
 KDA_FLAG_BETA_LOGIT, KDA_FLAG_GATE_SOFTPLUS = 0x1, 0x2
 KDA_FLAG_KERNEL_MASK = 0xF00
 KDA_KERNEL_DEFAULT, KDA_KERNEL_CHUNK16, KDA_KERNEL_REGISTER_STATE, KDA_KERNEL_BF16_STATE = 0x000, 0x100, 0x200, 0x300
+KDA_KERNEL_SMEM_STATE = 0x400
 KDA_SCHEDULE_TWO_PER_SM, KDA_SCHEDULE_ONE_PER_SM, KDA_SCHEDULE_CLUSTER = 0, 1, 2
 KDA_TRACE_POINTS = 8
 

@@ -133,7 +133,7 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
     const uint32_t iface = flags & ~KDA_FLAG_KERNEL_MASK;
     if (iface & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS))
         return fail(KDA_ERR_INVALID_ARG, "flags: unknown bits 0x%x", iface & ~(KDA_FLAG_BETA_LOGIT | KDA_FLAG_GATE_SOFTPLUS));
-    if (kernel > KDA_KERNEL_BF16_STATE) return fail(KDA_ERR_INVALID_ARG, "flags: unknown kernel 0x%x", kernel);
+    if (kernel > KDA_KERNEL_SMEM_STATE) return fail(KDA_ERR_INVALID_ARG, "flags: unknown kernel 0x%x", kernel);
     if (kernel != KDA_KERNEL_DEFAULT && iface != 0)
         return fail(KDA_ERR_UNSUPPORTED, "the interface flags are built into the default kernel only");
     if (!present(q)) return fail(KDA_ERR_INVALID_ARG, "q: missing");
@@ -239,6 +239,7 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
         case KDA_KERNEL_CHUNK16: e = kda::launch_fwd_tc16(p, s); break;
         case KDA_KERNEL_REGISTER_STATE: e = kda::launch_fwd_mma(p, s); break;
         case KDA_KERNEL_BF16_STATE: e = kda::launch_fwd_tc(p, s, true); break;
+        case KDA_KERNEL_SMEM_STATE: e = kda::launch_fwd_tc(p, s, true, true); break;
         default: e = kda::launch_fwd_tc(p, s, false); break;
     }
     if (e != cudaSuccess) return fail(KDA_ERR_CUDA, "forward launch: %s", cudaGetErrorString(e));

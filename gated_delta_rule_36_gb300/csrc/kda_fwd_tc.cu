@@ -120,6 +120,13 @@ constexpr int NHELP = 3, CL_SIZE = NHELP + 1;
 constexpr uint32_t OFF_SLOT2 = (SMEM_USED + 1023) & ~1023u;   // the home CTA's third slot
 constexpr uint32_t SMEM_BYTES_CL = OFF_SLOT2 + SLOT_BYTES + 1024;
 static_assert(SMEM_BYTES_CL <= 232448, "the cluster layout must fit one CTA's shared memory");
+
+// bf16 state resident in shared memory (a design alternative, one CTA per SM): the 128 x 128
+// state as GEMM1's A operand, K-major with the 128-byte swizzle, two 64-column blocks of 16 KB.
+constexpr uint32_t OFF_STATE = (SMEM_USED + 1023) & ~1023u;
+constexpr uint32_t STATE_BLOCK = 128 * 128;
+constexpr uint32_t SMEM_BYTES_SS = OFF_STATE + 2 * STATE_BLOCK + 1024;
+static_assert(SMEM_BYTES_SS <= 232448, "the shared-memory state layout must fit one CTA's shared memory");
 // The pulled part of a slot: [Q_d | K_d] and K_r (bytes [0, SL_V)), then Mqk, -B2 and a
 // (bytes [SL_MQT, SL_BETA)); v is the home CTA's own.
 constexpr int PULL_VECS_A = SL_V / 16, PULL_VECS = PULL_VECS_A + (SL_BETA - SL_MQT) / 16;
@@ -254,8 +261,12 @@ __device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr) {
 // S = S diag(a) in place with the next chunk's a (its GEMM3 adds to the decayed S).
 // kBf16State (the state-precision ablation) decays the bf16 copy instead, i.e. rounds the
 // carried state to bf16 at every chunk boundary, as a bf16 state store would.
-template <bool kBf16State>
-__device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* a_s) {
+// kSmem (the shared-memory state alternative): the bf16 copy goes to row `v` of the state tile
+// in shared memory (GEMM1's A operand) instead of Tensor Memory; with kBf16State it is also the
+// state that is decayed and updated.
+template <bool kBf16State, bool kSmem = false>
+__device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* a_s, unsigned char* st = nullptr,
+                                               int v = 0) {
 #pragma unroll 1
     for (int piece = 0; piece < 8; ++piece) {
         uint32_t r[16];
@@ -264,7 +275,12 @@ __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* 
         uint32_t b[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
-        tmem_st8(lane_addr + TM_SB + piece * 8, b);
+        if constexpr (kSmem) {
+            *reinterpret_cast<uint4*>(st + sw128_offset(v, 16 * piece, 128)) = make_uint4(b[0], b[1], b[2], b[3]);
+            *reinterpret_cast<uint4*>(st + sw128_offset(v, 16 * piece + 8, 128)) = make_uint4(b[4], b[5], b[6], b[7]);
+        } else {
+            tmem_st8(lane_addr + TM_SB + piece * 8, b);
+        }
         if (kBf16State) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -380,8 +396,11 @@ __device__ __forceinline__ void put_beta(const Unit& u, int s, int lane, float b
 // kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pulled chunks (FULLOP
 // stands for AREADY, FULLP and FULLD at once), it loads v alone, and it hands each slot back
 // (HFREE) once GEMM3 has read it.
-template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl>
+// kSmemState: the bf16 state resident in shared memory (with kBf16State and kWarpIssue).
+template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSmemState = false>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
+    static_assert(!kSmemState || (kBf16State && kWarpIssue && !kCl), "the shared-memory state runs one CTA per SM");
+    unsigned char* st_smem = u.gbase + OFF_STATE;
     constexpr int NS = kCl ? NHELP : NSLOT;   // slots in the ring
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
@@ -426,8 +445,9 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     tmem_wait_st();
     bool ok = warp_wait(bar_addr(u, kCl ? B_FULLOP : B_AREADY), 0, p.status, 256);   // a of chunk 0
     if (ok) {
-        copy_and_decay<kBf16State>(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A));
+        copy_and_decay<kBf16State, kSmemState>(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A), st_smem, pt);
         tmem_wait_st();
+        if constexpr (kSmemState) fence_proxy_async_smem();   // GEMM1 reads the tile
         tc_fence_before();
         named_bar_sync(2, 128);
     } else {
@@ -468,7 +488,15 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
             auto av = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024); };
             auto bv = [&](int kk) { return make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512); };
-            if constexpr (kWarpIssue) {
+            if constexpr (kSmemState) {   // A = the bf16 state tile in shared memory
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    tc_mma_ss_warp(u.tmem + TM_O, make_sdesc_kmajor_sw128(u.base + OFF_STATE + (kk >> 2) * STATE_BLOCK + (kk & 3) * 32),
+                                   b1(kk), idesc1, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // P -= V^T
+                tc_commit_warp(bar_addr(u, B_G1));
+            } else if constexpr (kWarpIssue) {
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) tc_mma_ts_warp(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
 #pragma unroll
@@ -624,11 +652,14 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down(c, 4, u.nchunks); break; }
             }
             const float* a_next = reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A);
-            if constexpr (kWarpIssue)
+            if constexpr (kSmemState)
+                copy_and_decay<kBf16State, true>(lane_addr, a_next, st_smem, pt);
+            else if constexpr (kWarpIssue)
                 copy_and_decay_pipelined<kBf16State>(lane_addr, a_next);
             else
                 copy_and_decay<kBf16State>(lane_addr, a_next);
             tmem_wait_st();
+            if constexpr (kSmemState) fence_proxy_async_smem();   // GEMM1 reads the tile
             tc_fence_before();
             named_bar_sync(2, 128);
             // the output store has had the copy-and-decay pass to read the staging tile: the
@@ -1149,7 +1180,8 @@ __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u
 // kWarpIssue: the instantiation for one CTA per SM (warp-wide MMA issue, pipelined state
 // pass, and the register file to itself: up to 128 registers a thread instead of 72).
 // kCl: the cluster schedule (one CTA per SM too).
-template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit, bool kCl = false>
+// kSmemState: the bf16 state resident in shared memory (one CTA per SM).
+template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit, bool kCl = false, bool kSmemState = false>
 __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
@@ -1193,7 +1225,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
 
     if constexpr (!kCl) {
         if (warp < W_PREP0) {
-            chain_group<kBf16State, kWarpIssue, kBetaLogit, false>(p, maps, u, tid);
+            chain_group<kBf16State, kWarpIssue, kBetaLogit, false, kSmemState>(p, maps, u, tid);
         } else if (warp < W_INV) {
             prep_group<kSoftplus, 1>(p, u, tid - W_PREP0 * 32, 0, u.nchunks);
         } else {
@@ -1316,7 +1348,7 @@ cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, in
     return cudaSuccess;
 }
 
-cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state) {
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state, bool smem_state) {
     const int units = p.nseq * p.H;
     if (units == 0) return cudaSuccess;
     TmaMaps maps;
@@ -1324,6 +1356,13 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
         !encode_tokens_map(&maps.v, p.v, p.T_total, p.H, true) || !encode_tokens_map(&maps.g, p.g, p.T_total, p.H) ||
         !encode_tokens_map(&maps.out, p.out, p.T_total, p.H, true))
         return cudaErrorInvalidValue;
+    if (smem_state) {   // the shared-memory state alternative: one CTA per unit, one per SM
+        auto ks = kda_fwd_tc_kernel<true, true, false, false, false, true>;
+        cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_SS);
+        if (e != cudaSuccess) return e;
+        ks<<<units, TC_THREADS, SMEM_BYTES_SS, stream>>>(p, maps);
+        return cudaGetLastError();
+    }
     int sched = KDA_SCHEDULE_TWO_PER_SM;
     cudaError_t e = fwd_tc_schedule(units, p.flags, bf16_state, &sched);
     if (e != cudaSuccess) return e;

@@ -24,8 +24,10 @@ cudaError_t launch_fwd_mma(const FwdParams& p, cudaStream_t stream);
 size_t fwd_mma_smem_bytes();
 
 // tcgen05 forward (one CTA per unit, two per SM, state resident in TMEM).  bf16_state
-// rounds the carried state to bf16 at every chunk boundary: the state-precision ablation.
-cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state = false);
+// rounds the carried state to bf16 at every chunk boundary: the state-precision ablation;
+// smem_state (with bf16_state) keeps that bf16 state resident in shared memory, one CTA per SM:
+// the state-placement ablation.
+cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_state = false, bool smem_state = false);
 size_t fwd_tc_smem_bytes();
 // The KDA_SCHEDULE_* a launch of the tensor-core kernel over `units` units takes on the
 // current device.

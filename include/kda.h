@@ -86,12 +86,18 @@ typedef struct {
  *                                on mma.sync (the pre-tcgen05 placement of the state)
  *   KDA_KERNEL_BF16_STATE        the default kernel with the carried state rounded to bf16 at
  *                                every chunk boundary ("How FlashKDA Stores On-Chip Recurrent
- *                                State in BF16": the precision of a bf16 state store) */
+ *                                State in BF16": the precision of a bf16 state store)
+ *   KDA_KERNEL_SMEM_STATE        that bf16 state resident in shared memory (GEMM1 reads it through
+ *                                a shared-memory descriptor; decay and update in fp32 in Tensor
+ *                                Memory, rounded to bf16 once per chunk, as the same page and
+ *                                "FlashKDA State Update Numerical Precision" describe); the extra
+ *                                32 KB of shared memory leaves room for one CTA per SM */
 #define KDA_FLAG_KERNEL_MASK        0xF00u
 #define KDA_KERNEL_DEFAULT          0x000u
 #define KDA_KERNEL_CHUNK16          0x100u
 #define KDA_KERNEL_REGISTER_STATE   0x200u
 #define KDA_KERNEL_BF16_STATE       0x300u
+#define KDA_KERNEL_SMEM_STATE       0x400u
 
 /* Device-side status bits, in the first 32-bit word of the workspace. */
 #define KDA_DEVERR_CU_SEQLENS 0x1u  /* cu_seqlens[0] != 0, decreasing, or cu_seqlens[N] > T */

@@ -134,9 +134,11 @@ def test_kernel_field_rejections(lib):
                               ctypes.c_uint32(flags), ctypes.c_void_p(0))
 
     assert call_ex(0xF00) == kb.KDA_ERR_INVALID_ARG
+    assert call_ex(0x500) == kb.KDA_ERR_INVALID_ARG
     assert call_ex(0x4) == kb.KDA_ERR_INVALID_ARG
     assert call_ex(0x1000) == kb.KDA_ERR_INVALID_ARG
-    for kern in (kb.KDA_KERNEL_CHUNK16, kb.KDA_KERNEL_REGISTER_STATE, kb.KDA_KERNEL_BF16_STATE):
+    for kern in (kb.KDA_KERNEL_CHUNK16, kb.KDA_KERNEL_REGISTER_STATE, kb.KDA_KERNEL_BF16_STATE,
+                 kb.KDA_KERNEL_SMEM_STATE):
         assert call_ex(kern | kb.KDA_FLAG_BETA_LOGIT) == kb.KDA_ERR_UNSUPPORTED
         assert call_ex(kern | kb.KDA_FLAG_GATE_SOFTPLUS) == kb.KDA_ERR_UNSUPPORTED
         # a valid kernel passes the flag checks and then meets the (too small) workspace
@@ -253,6 +255,7 @@ def test_binding_constants_match_the_header():
                 "KDA_ERR_CUDA", "KDA_BF16", "KDA_F32", "KDA_I64", "KDA_DEVERR_CU_SEQLENS", "KDA_DEVERR_TIMEOUT",
                 "KDA_DEVERR_INTERNAL", "KDA_FLAG_BETA_LOGIT", "KDA_FLAG_GATE_SOFTPLUS", "KDA_FLAG_KERNEL_MASK",
                 "KDA_KERNEL_DEFAULT", "KDA_KERNEL_CHUNK16", "KDA_KERNEL_REGISTER_STATE", "KDA_KERNEL_BF16_STATE",
+                "KDA_KERNEL_SMEM_STATE",
                 "KDA_SCHEDULE_TWO_PER_SM",
                 "KDA_SCHEDULE_ONE_PER_SM", "KDA_SCHEDULE_CLUSTER", "KDA_TRACE_POINTS"]
     for name in mirrored:

@@ -7,10 +7,13 @@ kda_fwd_ex's kernel field selects, per call:
   KDA_KERNEL_BF16_STATE      the carried state rounded to bf16 at every chunk boundary (the
                              numerics of the bf16 state store of "How FlashKDA Stores On-Chip
                              Recurrent State in BF16")
+  KDA_KERNEL_SMEM_STATE      that bf16 state resident in shared memory (GEMM1's A operand from a
+                             shared-memory descriptor), one CTA per SM
 Each must match the fp64 oracle on the small workloads and the edge cases over whole
-tensors, and give bit-identical results for packed and separate runs.  The bf16-state
-alternative is also measured on a long memory, where its error must exceed the fp32-state
-tolerance that the default kernel meets: the cost of that design, stated as a check.
+tensors, and give bit-identical results for packed and separate runs.  The two bf16-state
+alternatives are also measured on a long memory, where their error must exceed the
+fp32-state tolerance that the default kernel meets: the cost of that design, stated as a
+check.  They round at the same points, so they must agree with each other bit for bit.
 """
 import numpy as np
 import pytest
@@ -25,7 +28,7 @@ pytestmark = pytest.mark.gpu
 bf16, f32 = torch.bfloat16, torch.float32
 
 KERNELS = {"chunk16": kb.KDA_KERNEL_CHUNK16, "register_state": kb.KDA_KERNEL_REGISTER_STATE,
-           "bf16_state": kb.KDA_KERNEL_BF16_STATE}
+           "bf16_state": kb.KDA_KERNEL_BF16_STATE, "smem_state": kb.KDA_KERNEL_SMEM_STATE}
 
 
 def W(name, seed, H, B=1, T=0, lens=None, init=bf16, final=bf16, lb=-5.0):
@@ -108,11 +111,22 @@ def test_long_memory_keeps_state_precision(kernel):
     check_full(inp, out, final, ref_out, ref_final)
 
 
-def test_bf16_state_loses_long_memory_precision():
+@pytest.mark.parametrize("kernel", ["bf16_state", "smem_state"])
+def test_bf16_state_loses_long_memory_precision(kernel):
     """Rounding the carried state to bf16 at every chunk boundary drifts past the fp32-state
     tolerance over 4,096 tokens without decay (the default kernel stays inside it on the
     same input: tests/test_gpu_invariants.py)."""
-    _, _, final, _, ref_final = _long_memory(kb.KDA_KERNEL_BF16_STATE)
+    _, _, final, _, ref_final = _long_memory(KERNELS[kernel])
     _, rel = errors(final.double().cpu().numpy(), ref_final)
     assert rel > F32_REL_FRO, f"bf16-rounded state error {rel:.3e} unexpectedly within {F32_REL_FRO}"
     assert rel < 4 * F32_REL_FRO, f"bf16-rounded state error {rel:.3e}: more than the rounding explains"
+
+
+def test_smem_state_equals_bf16_state_bitwise():
+    """The shared-memory and Tensor-Memory placements of the bf16 state round at the same
+    points and feed GEMM1 the same bf16 values, so they give the same bits."""
+    inp = make_inputs(W("place", 224, H=3, lens=[45, 0, 130, 64, 7], init=f32, final=f32), "cuda")
+    o1, f1, b1 = run_gpu(inp, flags=kb.KDA_KERNEL_BF16_STATE)
+    o2, f2, b2 = run_gpu(inp, flags=kb.KDA_KERNEL_SMEM_STATE)
+    assert b1 == 0 and b2 == 0
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)) and torch.equal(f1, f2)
