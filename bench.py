@@ -373,16 +373,50 @@ def run_e2e(kda, inp, w, dev, stream, args):
     step()
     torch.cuda.synchronize()
     n = args.e2e_steps
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(n):
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    ev[0].record(stream)
+    for i in range(n):
         step()
-    b.record(stream)
+        ev[i + 1].record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / n
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(n)]
+    ms = ev[0].elapsed_time(ev[n]) / n
+
+    # the copies alone, for the bound: every input host -> device, then out and final_state back
+    dev_in = {k: torch.empty_like(t, device=dev) for k, t in host.items()}
+    d_init = torch.empty_like(h_init, device=dev) if h_init is not None else None
+    d_out = torch.empty_like(h_out, device=dev)
+    d_final = torch.empty_like(h_final, device=dev)
+
+    def copies_in():
+        for k, t in host.items():
+            dev_in[k].copy_(t, non_blocking=True)
+        if h_init is not None:
+            d_init.copy_(h_init, non_blocking=True)
+
+    def copies_out():
+        h_out.copy_(d_out, non_blocking=True)
+        h_final.copy_(d_final, non_blocking=True)
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    h2d_ms, d2h_ms = timed(copies_in), timed(copies_out)
+    del dev_in, d_init, d_out, d_final
     return {"value": w.total_tokens / (ms / 1000.0), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "steps": n, "groups": args.e2e_groups,
-            "api": "kda_fwd_host"}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms, "ms_per_step_min": min(per),
+            "ms_per_step_median": statistics.median(per), "steps": n, "groups": args.e2e_groups,
+            "api": "kda_fwd_host",
+            "copies_alone": {"h2d_ms": h2d_ms, "h2d_gbs": h2d / (h2d_ms / 1e3) / 1e9,
+                             "d2h_ms": d2h_ms, "d2h_gbs": d2h / (d2h_ms / 1e3) / 1e9}}
 
 
 def run_decode(args):
@@ -440,7 +474,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--kernel", choices=tuple(KERNELS), default="default",
                     help="the default kernel or a design alternative (timed on the same workload)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--e2e-groups", type=int, default=8, help="sequence groups kda_fwd_host pipelines over")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

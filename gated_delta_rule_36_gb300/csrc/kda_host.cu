@@ -62,22 +62,39 @@ kda_tensor dev_tensor(const kda_tensor* host, void* data) {
     return t;
 }
 
-// Streams and events of one call; released on every return path (a stream or event
-// destroyed with work pending is freed by the runtime once that work completes).
+// The copy streams and events of one host thread on one device, created by the thread's
+// first call there and reused by its later calls (streams and events are not allocated on
+// the hot path).  Reusing an event is safe: cudaStreamWaitEvent waits for the record that is
+// current when it is called, and every wait on an event is enqueued before the event is
+// recorded again.
 struct Resources {
     cudaStream_t s_in = nullptr, s_out = nullptr;
-    std::vector<cudaEvent_t> events;
-    ~Resources() {
-        for (cudaEvent_t e : events) cudaEventDestroy(e);
+    cudaEvent_t ev[2 + 2 * kMaxGroups] = {};
+    int used = 0;   // events handed out by the current call
+    ~Resources() {   // at thread exit; errors (a runtime already unloaded) are ignored
+        for (cudaEvent_t e : ev)
+            if (e) cudaEventDestroy(e);
         if (s_in) cudaStreamDestroy(s_in);
         if (s_out) cudaStreamDestroy(s_out);
     }
+    cudaError_t begin() {   // the streams (first call only) and a fresh run of events
+        used = 0;
+        cudaError_t r = cudaSuccess;
+        if (!s_in) r = cudaStreamCreateWithFlags(&s_in, cudaStreamNonBlocking);
+        if (r == cudaSuccess && !s_out) r = cudaStreamCreateWithFlags(&s_out, cudaStreamNonBlocking);
+        return r;
+    }
     cudaError_t event(cudaEvent_t* e) {
-        const cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
-        if (r == cudaSuccess) events.push_back(*e);
+        if (used >= (int)(sizeof(ev) / sizeof(ev[0]))) return cudaErrorInvalidValue;
+        cudaError_t r = cudaSuccess;
+        if (!ev[used]) r = cudaEventCreateWithFlags(&ev[used], cudaEventDisableTiming);
+        if (r == cudaSuccess) *e = ev[used++];
         return r;
     }
 };
+
+constexpr int kMaxDevices = 64;
+thread_local Resources t_res[kMaxDevices];
 
 }  // namespace
 
@@ -178,11 +195,16 @@ kda_status kda_fwd_host(const kda_tensor* q, const kda_tensor* k, const kda_tens
         }
     }
 
-    Resources r;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        kda::set_last_error(e != cudaSuccess ? cudaGetErrorString(e) : "device index out of range");
+        return KDA_ERR_CUDA;
+    }
+    Resources& r = t_res[dev];
     cudaStream_t s_user = reinterpret_cast<cudaStream_t>(stream);
     cudaEvent_t ev_start, ev_done;
-    cudaError_t e = cudaStreamCreateWithFlags(&r.s_in, cudaStreamNonBlocking);
-    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&r.s_out, cudaStreamNonBlocking);
+    e = r.begin();
     if (e == cudaSuccess) e = r.event(&ev_start);
     if (e == cudaSuccess) e = r.event(&ev_done);
     if (e == cudaSuccess) e = cudaEventRecord(ev_start, s_user);

@@ -296,7 +296,8 @@ size_t kda_fwd_host_device_bytes(int64_t B, int64_t T, int H, int64_t N, int ini
  * token counts fall from the first to the last (groups <= 0: 8; the last group's work is
  * the only part nothing overlaps) and pipelines them over three streams: the
  * host-to-device copies of group j + 1 run while group j computes and its results are
- * copied back.  The work is ordered after everything already on `stream` and `stream`
+ * copied back.  The two copy streams and the events are the library's: created by a host
+ * thread's first call on a device and reused by that thread's later calls there.  The work is ordered after everything already on `stream` and `stream`
  * is ordered after all of it; the call itself returns once the work is enqueued, so the
  * host buffers must stay untouched until `stream` reaches that point.  Host buffers should
  * be page-locked (cudaHostAlloc / pinned): pageable ones work but are copied synchronously.

@@ -15,6 +15,8 @@ alternatives are also measured on a long memory, where their error must exceed t
 fp32-state tolerance that the default kernel meets: the cost of that design, stated as a
 check.  They round at the same points, so they must agree with each other bit for bit.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -118,6 +120,8 @@ def test_bf16_state_loses_long_memory_precision(kernel):
     same input: tests/test_gpu_invariants.py)."""
     _, _, final, _, ref_final = _long_memory(KERNELS[kernel])
     _, rel = errors(final.double().cpu().numpy(), ref_final)
+    if os.environ.get("KDA_TEST_VERBOSE"):
+        print(f"[err] {kernel} long-memory final_state: rel_fro={rel:.3e}")
     assert rel > F32_REL_FRO, f"bf16-rounded state error {rel:.3e} unexpectedly within {F32_REL_FRO}"
     assert rel < 4 * F32_REL_FRO, f"bf16-rounded state error {rel:.3e}: more than the rounding explains"
 

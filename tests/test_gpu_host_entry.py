@@ -77,3 +77,29 @@ def test_host_entry_in_place_state():
     assert hbits == 0
     _same(out, ref_out)
     _same(final, ref_final)
+
+
+def test_host_entry_from_another_thread():
+    """The copy streams and events are kept per host thread: a call from a second thread
+    uses its own and gives the same bits."""
+    import threading
+    w = CASES[0][0]
+    inp = make_inputs(w, "cpu")
+    ref_out, ref_final, bits = run_gpu(inp)
+    assert bits == 0
+    res = {}
+
+    def work():
+        try:
+            res["r"] = _host_run(inp, 3)
+        except Exception as exc:   # surfaced below
+            res["e"] = exc
+
+    th = threading.Thread(target=work)
+    th.start()
+    th.join()
+    assert "e" not in res, res.get("e")
+    out, final, hbits = res["r"]
+    assert hbits == 0
+    _same(out, ref_out)
+    _same(final, ref_final)
