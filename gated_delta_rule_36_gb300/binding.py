@@ -52,16 +52,18 @@ _lock = threading.Lock()
 
 
 def library_path() -> str:
-    return _build.LIB_PATH
+    return os.environ.get("KDA_LIBRARY") or _build.LIB_PATH
 
 
 def load(path: Optional[str] = None):
-    """Load libkda.so (raises if it has not been built)."""
+    """Load libkda.so (raises if it has not been built).  The environment variable
+    KDA_LIBRARY names another build of the same ABI to load instead (the tests use it
+    for the range-checked build)."""
     global _lib
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or _build.LIB_PATH
+        p = path or os.environ.get("KDA_LIBRARY") or _build.LIB_PATH
         if not os.path.exists(p):
             raise ImportError(f"KDA CUDA library not found at {p}; build it with "
                               "gated_delta_rule_36_gb300.build.build()")

@@ -3,6 +3,10 @@
 Each ``csrc/*.cu`` translation unit is compiled by nvcc in parallel, then linked
 into one shared library next to this file.  The CUDA runtime is linked
 statically, so the library only needs the driver at run time.
+
+``build(checked=True)`` makes ``libkda_checked.so``, the same sources compiled with
+``-DKDA_CHECKED``: the range-checked build the tests run beside the product library
+(a bad index sets KDA_DEVERR_INTERNAL instead of faulting).
 """
 from __future__ import annotations
 
@@ -18,6 +22,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libkda.so")
+BUILD_DIR_CHECKED = os.path.join(HERE, "_build_checked")
+LIB_PATH_CHECKED = os.path.join(HERE, "libkda_checked.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -38,10 +44,11 @@ def _deps():
                                + glob.glob(os.path.join(INCLUDE, "*.h"))) + [os.path.abspath(__file__)]
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB_PATH):
+def needs_build(checked: bool = False) -> bool:
+    lib = LIB_PATH_CHECKED if checked else LIB_PATH
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(d) > t for d in _deps())
 
 
@@ -50,16 +57,19 @@ def compile_flags(extra=()):
                    "--expt-relaxed-constexpr", *extra]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every CUDA source for sm_103a and link ``libkda.so`` in-tree."""
-    if not force and not needs_build():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    """Compile every CUDA source for sm_103a and link ``libkda.so`` (``libkda_checked.so``
+    with ``checked``) in-tree."""
+    lib_path = LIB_PATH_CHECKED if checked else LIB_PATH
+    build_dir = BUILD_DIR_CHECKED if checked else BUILD_DIR
+    if not force and not needs_build(checked):
+        return lib_path
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = compile_flags(extra_flags)
+    os.makedirs(build_dir, exist_ok=True)
+    flags = compile_flags(tuple(extra_flags) + (("-DKDA_CHECKED",) if checked else ()))
 
     def cc(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *flags, "-Xptxas", "-v", "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -71,15 +81,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     srcs = _sources()
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(cc, srcs))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lrt", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

@@ -164,6 +164,38 @@ __device__ __forceinline__ uint32_t sc128(int row, int col) {
     return (uint32_t)(row * 256 + ((((col >> 3) ^ (row & 7))) << 4) + ((col & 7) << 1));
 }
 
+// Range checks of the KDA_CHECKED build (a second library for the tests; the product build
+// compiles them away).  The shared-memory and Tensor-Memory layouts are compile-time constants
+// checked by the static_asserts above; what depends on the data or the thread is checked here:
+// global state rows, beta and output rows, token coordinates of the tensor copies, and the
+// row / column arguments of the tile index functions.  A failed check sets
+// KDA_DEVERR_INTERNAL in the status word and clamps the index into range, so the access stays
+// in bounds and the kernel runs to its end: the build never faults on a bad index.
+#ifdef KDA_CHECKED
+static __shared__ uint32_t* s_chk_status;
+__device__ __forceinline__ int64_t chk_range(int64_t x, int64_t lo, int64_t hi) {
+    if (x >= lo && x < hi) return x;
+    atomicOr(s_chk_status, KDA_DEVERR_INTERNAL);
+    return lo;
+}
+#define KDA_CHK(x, lo, hi) chk_range((int64_t)(x), (int64_t)(lo), (int64_t)(hi))
+#else
+#define KDA_CHK(x, lo, hi) (x)
+#endif
+// tile index functions with their arguments checked
+__device__ __forceinline__ uint32_t sw128_at(int r, int k, int rows) {
+    return sw128_offset((int)KDA_CHK(r, 0, rows), (int)KDA_CHK(k, 0, HD), rows);
+}
+__device__ __forceinline__ uint32_t core_at(int r, int k, int kt) {
+    return core_offset((int)KDA_CHK(r, 0, CH), (int)KDA_CHK(k, 0, kt), kt);
+}
+__device__ __forceinline__ int l_at(int i, int j) {
+    i = (int)KDA_CHK(i, 0, CH);
+    j = (int)KDA_CHK(j, 0, (i < 16 ? 16 : CH));   // L keeps no upper-right block
+    return l_index(i, j);
+}
+__device__ __forceinline__ uint32_t sc_at(int row, int col) { return sc128((int)KDA_CHK(row, 0, CH), (int)KDA_CHK(col, 0, HD)); }
+
 // Bounded wait, with the verdict made uniform over the warp.  `max_sleep_ns` > 0 backs
 // off between polls (long waits off the critical path).
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t* status,
@@ -198,6 +230,7 @@ __device__ __noinline__ void prep_wind_down(int j, int k, int nloc) {
 
 // 16 state values of row `off` (element offset) as fp32 bits (zeros without an initial state).
 __device__ __forceinline__ void load_state16(const FwdParams& p, size_t off, uint32_t (&r)[16]) {
+    off = (size_t)KDA_CHK(off, 0, (int64_t)p.nseq * p.H * HD * HD - 15);
     if (!p.init_state) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) r[j] = 0u;
@@ -225,6 +258,7 @@ __device__ __forceinline__ void load_state16(const FwdParams& p, size_t off, uin
 
 __device__ __forceinline__ void store_state16(const FwdParams& p, size_t off, const uint32_t (&r)[16]) {
     if (!p.final_state) return;
+    off = (size_t)KDA_CHK(off, 0, (int64_t)p.nseq * p.H * HD * HD - 15);
     if (p.final_f32) {
         uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(p.final_state) + off);
 #pragma unroll
@@ -276,8 +310,8 @@ __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* 
 #pragma unroll
         for (int j = 0; j < 8; ++j) b[j] = pack_bf16x2(u2f(r[2 * j]), u2f(r[2 * j + 1]));
         if constexpr (kSmem) {
-            *reinterpret_cast<uint4*>(st + sw128_offset(v, 16 * piece, 128)) = make_uint4(b[0], b[1], b[2], b[3]);
-            *reinterpret_cast<uint4*>(st + sw128_offset(v, 16 * piece + 8, 128)) = make_uint4(b[4], b[5], b[6], b[7]);
+            *reinterpret_cast<uint4*>(st + sw128_at(v, 16 * piece, 128)) = make_uint4(b[0], b[1], b[2], b[3]);
+            *reinterpret_cast<uint4*>(st + sw128_at(v, 16 * piece + 8, 128)) = make_uint4(b[4], b[5], b[6], b[7]);
         } else {
             tmem_st8(lane_addr + TM_SB + piece * 8, b);
         }
@@ -349,7 +383,7 @@ __device__ __forceinline__ int chunk_valid(const Unit& u, int c) {
 
 // q, k, g boxes of chunk c into slot s (on FULLTMA, which beta completes).
 __device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int c, int s) {
-    const int t0 = (int)(u.bos + (int64_t)c * CH);
+    const int t0 = (int)KDA_CHK(u.bos + (int64_t)c * CH, u.bos, u.eos);
     const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLTMA + s);
     mbar_arrive_expect_tx(full, 3u * CH * HD * 2u);
     tma_load_3d(slot + SL_RAWQ, &maps.q, 0, u.h, t0, full);
@@ -359,7 +393,7 @@ __device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int
 
 // the v box of chunk c (two 64-channel halves, 128-byte swizzle) into slot s, on FULLV.
 __device__ __forceinline__ void load_v(const TmaMaps& maps, const Unit& u, int c, int s) {
-    const int t0 = (int)(u.bos + (int64_t)c * CH);
+    const int t0 = (int)KDA_CHK(u.bos + (int64_t)c * CH, u.bos, u.eos);
     const uint32_t slot = u.base + slot_off(s), full = bar_addr(u, B_FULLV + s);
     mbar_arrive_expect_tx(full, CH * HD * 2u);
     tma_load_3d(slot + SL_V, &maps.v, 0, u.h, t0, full);
@@ -383,7 +417,7 @@ template <bool kBetaLogit>
 __device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, int c, int lane) {
     const int64_t t0 = u.bos + (int64_t)c * CH;
     if (lane >= chunk_valid(u, c)) return 0.f;
-    const float b = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[(t0 + lane) * p.H + u.h]);
+    const float b = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[KDA_CHK((t0 + lane) * p.H + u.h, 0, p.T_total * p.H)]);
     if constexpr (kBetaLogit) return rcp_approx(1.f + ex2_approx(-b * LOG2E));
     return b;
 }
@@ -438,7 +472,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const int n = pt >> 2, kb = pt & 3;
         const uint32_t m1 = ((n >> 3) == kb) ? ((n & 1) ? 0xBF800000u : 0x0000BF80u) : 0u;   // bf16 -1 at column n
         const int wi = (n & 7) >> 1;
-        *reinterpret_cast<uint4*>(u.gbase + OFF_NEGI + core_offset(n, 8 * kb, 32)) =
+        *reinterpret_cast<uint4*>(u.gbase + OFF_NEGI + core_at(n, 8 * kb, 32)) =
             make_uint4(wi == 0 ? m1 : 0u, wi == 1 ? m1 : 0u, wi == 2 ? m1 : 0u, wi == 3 ? m1 : 0u);
         fence_proxy_async_smem();
     }
@@ -607,7 +641,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                     const uint32_t r1 = pack_bf16x2(u2f(o[8 * st + 2]), u2f(o[8 * st + 3]));
                     const uint32_t r2 = pack_bf16x2(u2f(o[8 * st + 4]), u2f(o[8 * st + 5]));
                     const uint32_t r3 = pack_bf16x2(u2f(o[8 * st + 6]), u2f(o[8 * st + 7]));
-                    stmatrix_x4_trans_s(tile + sw128_offset(tok, v0, 32), r0, r1, r2, r3);
+                    stmatrix_x4_trans_s(tile + sw128_at(tok, v0, 32), r0, r1, r2, r3);
                 }
             }
         } else {
@@ -634,11 +668,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             const int nvalid = chunk_valid(u, c);
             const uint32_t ost = slot + SL_V;
             if (nvalid == CH) {
-                tma_store_3d(&maps.out, ost, 0, u.h, (int)t0);
-                tma_store_3d(&maps.out, ost + 4096, 64, u.h, (int)t0);
+                const int tc = (int)KDA_CHK(t0, u.bos, u.eos - CH + 1);   // a full chunk inside its sequence
+                tma_store_3d(&maps.out, ost, 0, u.h, tc);
+                tma_store_3d(&maps.out, ost + 4096, 64, u.h, tc);
             } else {
                 for (int i = 0; i < nvalid; ++i)
-                    bulk_store(p.out + ((t0 + i) * p.H + u.h) * HD, ost + i * 256, 256);
+                    bulk_store(p.out + (KDA_CHK(t0 + i, u.bos, u.eos) * p.H + u.h) * HD, ost + i * 256, 256);
             }
             bulk_commit();
         }
@@ -711,9 +746,9 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
     // phase B store offsets of token 4 pw (channels c0 .. c0 + 3); token 4 pw + r differs by one XOR:
     // its row adds r to bits 8-9 (scratch tiles, 256-byte rows) or 7-8 (swizzled slot, 128-byte rows),
     // and its 16-byte chunk index is XORed with r
-    const uint32_t oB_sc = sc128(4 * pw, c0);
-    const uint32_t oB_sw = sw128_offset(4 * pw, c0, 64);
-    const uint32_t oB_kr = sw128_offset(4 * pw, c0, 32);
+    const uint32_t oB_sc = sc_at(4 * pw, c0);
+    const uint32_t oB_sw = sw128_at(4 * pw, c0, 64);
+    const uint32_t oB_kr = sw128_at(4 * pw, c0, 32);
     const float eA = expf(p.A_log[u.h]);
     const float gm = -eA * LOG2E;                       // sigmoid(x) = 1 / (1 + 2^(gm (g + dt)))
     const float4 dt = *reinterpret_cast<const float4*>(p.dt_bias + u.h * HD + c0);
@@ -920,8 +955,8 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
             if (nb <= mt) {
                 // 16-byte chunk 2 kk + h of row r sits at chunk (2 kk + h) ^ (r % 8) = (h ^ (r % 8)) ^ 2 kk:
                 // k step kk is one XOR of the k-step-0 address with kk << 5 (the tiles are 256-byte aligned)
-                const uint32_t a0 = smem_u32(Ab + sc128(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, (lane >> 4) * 8));
-                const uint32_t b0 = smem_u32(kis + sc128(nb * 16 + (lane & 7) + (lane >> 4) * 8, ((lane >> 3) & 1) * 8));
+                const uint32_t a0 = smem_u32(Ab + sc_at(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, (lane >> 4) * 8));
+                const uint32_t b0 = smem_u32(kis + sc_at(nb * 16 + (lane & 7) + (lane >> 4) * 8, ((lane >> 3) & 1) * 8));
 #pragma unroll
                 for (int kk = 0; kk < 8; kk += 2) {   // two independent chains per n-tile (even / odd k steps)
                     uint32_t a[4], b[4], a2[4], b2[4];
@@ -951,11 +986,11 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
                     // select, never multiply: the masked upper triangle may hold inf/NaN
                     if (mat == 0) {
                         if (nb <= mt) {
-                            Lb[l_index(i, j)] = (j < i) ? bs[i] * v0 : 0.f;
-                            Lb[l_index(i, j + 1)] = (j + 1 < i) ? bs[i] * v1 : 0.f;
+                            Lb[l_at(i, j)] = (j < i) ? bs[i] * v0 : 0.f;
+                            Lb[l_at(i, j + 1)] = (j + 1 < i) ? bs[i] * v1 : 0.f;
                         }
                     } else {
-                        *reinterpret_cast<uint32_t*>(gslot + SL_MQT + core_offset(i, j, 32)) =
+                        *reinterpret_cast<uint32_t*>(gslot + SL_MQT + core_at(i, j, 32)) =
                             pack_bf16x2((j <= i) ? v0 : 0.f, (j + 1 <= i) ? v1 : 0.f);   // Mqk
                     }
                 }
@@ -987,7 +1022,7 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
     float* Xb = reinterpret_cast<float*>(u.gbase + OFF_X);
 #pragma unroll
     for (int s = 0; s < NSLOT; ++s)   // -B2[i][j] = 0 for i < 16 <= j (nothing else writes there)
-        *reinterpret_cast<uint4*>(u.gbase + s * SLOT_BYTES + SL_INV + core_offset(lane >> 1, 16 + 8 * (lane & 1), 32)) =
+        *reinterpret_cast<uint4*>(u.gbase + s * SLOT_BYTES + SL_INV + core_at(lane >> 1, 16 + 8 * (lane & 1), 32)) =
             make_uint4(0, 0, 0, 0);
 
 #pragma unroll 1
@@ -1064,8 +1099,8 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
                 wv[2 * q4] = pack_bf16x2(-bv.x * xv.x, -bv.y * xv.y);
                 wv[2 * q4 + 1] = pack_bf16x2(-bv.z * xv.z, -bv.w * xv.w);
             }
-            *reinterpret_cast<uint4*>(b2s + core_offset(n, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-            *reinterpret_cast<uint4*>(b2s + core_offset(n, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
+            *reinterpret_cast<uint4*>(b2s + core_at(n, o, 32)) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            *reinterpret_cast<uint4*>(b2s + core_at(n, o + 8, 32)) = make_uint4(wv[4], wv[5], wv[6], wv[7]);
         }
 
         // ---- y = T2^T X22^T = (X22 T2)^T = -X21^T: y[nt][e] = y[gq + 8 (e >> 1)][8 nt + 2 tq + (e & 1)]
@@ -1089,7 +1124,7 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int ci = gq + 8 * (e >> 1), rr = 8 * nt + 2 * tq + (e & 1);
-                *reinterpret_cast<uint16_t*>(b2s + core_offset(16 + rr, ci, 32)) = bf16_bits((e >> 1 ? bh : bl) * y[nt][e]);
+                *reinterpret_cast<uint16_t*>(b2s + core_at(16 + rr, ci, 32)) = bf16_bits((e >> 1 ? bh : bl) * y[nt][e]);
             }
         fence_proxy_async_smem();   // -B2 is read by the tensor core
         __syncwarp();
@@ -1187,6 +1222,9 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
 
     const int tid = threadIdx.x, warp = tid >> 5;
+#ifdef KDA_CHECKED
+    if (tid == 0) s_chk_status = p.status;   // published by the __syncthreads below
+#endif
     const int rank = kCl ? (int)cluster_ctarank() : 0;   // 0: the home CTA
     const bool home = rank == 0;
     Unit u;
