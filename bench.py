@@ -235,10 +235,10 @@ def run_reference(args):
     inp = make_inputs(w, dev)
     budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(inp, budget)
+        oracle_sample(inp, budget, args.oracle_threads)
     tot_th, tot_s, threads, desc = 0, 0.0, 1, ""
     for _ in range(args.steps):
-        th, s, threads, desc = oracle_sample(inp, budget)
+        th, s, threads, desc = oracle_sample(inp, budget, args.oracle_threads)
         tot_th += th
         tot_s += s
     value = tot_th / w.H / tot_s
@@ -338,7 +338,7 @@ def run_ours(args):
     if e2e is not None:
         line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        th, s, threads, desc = oracle_sample(inp, args.cpu_budget)
+        th, s, threads, desc = oracle_sample(inp, args.cpu_budget, args.oracle_threads)
         line["cpu_baseline"] = {"value": th / w.H / s, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": desc}
     if rank == 0:
@@ -479,6 +479,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--oracle-threads", type=int, default=0,
+                    help="host threads of the oracle legs (cpu_baseline, --impl reference); 0 = all cores")
     ap.add_argument("--traffic", type=float, default=None,
                     help="ncu dram bytes (read+write) of one launch of the forward kernel; by default the "
                          "committed record in profiles/, used only while the kernel sources match it")
