@@ -232,6 +232,10 @@ kda_status kda::fwd_device(const kda_tensor* q, const kda_tensor* k, const kda_t
     p.trace = g_trace;
     p.trace_chunks = g_trace_chunks;
     p.trace_unit = g_trace_unit;
+    p.test_skip_chunk = -1;
+#ifdef KDA_WAIT_TEST
+    if (const char* sk = getenv("KDA_TEST_SKIP_FULLD")) p.test_skip_chunk = atoll(sk);
+#endif
 
     // the kernel field selects a design alternative (include/kda.h); the default is the
     // tcgen05 kernel with 32-token chunks and the fp32 state resident in TMEM

@@ -45,6 +45,9 @@ struct FwdParams {
     unsigned long long* trace;
     int64_t trace_chunks;
     int64_t trace_unit;
+    // the test-only build of the timeout path (KDA_WAIT_TEST): the local chunk whose FULLD
+    // arrival the inverse warp skips, -1 for none; ignored by every other build
+    int64_t test_skip_chunk;
 };
 
 // Token range [bos, eos) of sequence n, clamped to [0, T_total].

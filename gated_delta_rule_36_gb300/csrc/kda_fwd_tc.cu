@@ -56,7 +56,14 @@ constexpr int W_INV = W_PREP0 + PREP_WARPS;   // the inverse warp: (I + L)^-1 of
 constexpr int W_MMA = 1, T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
+#ifdef KDA_WAIT_TEST
+// The test-only build of the timeout path: waits give up after ~2 ms, and the inverse warp
+// skips its FULLD arrival for local chunk p.test_skip_chunk (chosen by the host), so that a
+// wait of the chain runs out and the kernel has to wind down and return KDA_DEVERR_TIMEOUT.
+constexpr long long WAIT_LIMIT = 4000000LL;
+#else
 constexpr long long WAIT_LIMIT = 2000000000LL;  // SM cycles (~1 s) before a wait gives up
+#endif
 
 // Slot layout (bytes).  Raw q/k/g land where derived operands are later written.
 constexpr uint32_t SL_QDKD = 0;       // [Q_d | K_d]: 64 rows x 128, K-major, 128-B swizzle (raw q at 0, k at 8192)
@@ -1128,6 +1135,9 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
             }
         fence_proxy_async_smem();   // -B2 is read by the tensor core
         __syncwarp();
+#ifdef KDA_WAIT_TEST
+        if (j == p.test_skip_chunk) continue;   // the arrival a chain warp then waits for in vain
+#endif
         if (lane == 0) mbar_arrive(bar_addr(u, B_FULLD + s));
     }
 }

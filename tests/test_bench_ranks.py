@@ -56,7 +56,7 @@ def test_reference_arm_is_silent_off_rank_zero(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
 
     class Args:
-        workload, steps, warmup = "tiny", 1, 3
+        workload, steps, warmup, oracle_threads = "tiny", 1, 3, 0
     bench.run_reference(Args())
     assert capsys.readouterr().out == ""
 
@@ -81,7 +81,7 @@ def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "0")
 
     class Args:
-        workload, steps, warmup = "tiny", 1, 3
+        workload, steps, warmup, oracle_threads = "tiny", 1, 3, 0
     bench.run_reference(Args())
     lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
     assert len(lines) == 1

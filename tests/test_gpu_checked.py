@@ -20,7 +20,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_checked_build_passes_the_parity_cases():
-    lib = kbuild.build(checked=True)
+    lib = kbuild.build(variant="checked")
     env = dict(os.environ, KDA_LIBRARY=lib)
     cases = ["tests/test_gpu_parity.py::test_small_workloads_whole_tensor",
              "tests/test_gpu_invariants.py::test_edge_cases_against_oracle",
