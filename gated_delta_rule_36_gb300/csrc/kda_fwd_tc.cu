@@ -24,7 +24,7 @@
 //               TMA loads of q, k, g and beta (warp 2), and the output store and v
 //               loads (warp 3); warp 0 owns the TMEM allocation.
 //   warps 4-11  prep group: gate, prefix, q/k norms, centered operands (section 2),
-//               K_c K_i^T and Q_c K_i^T with mma.sync.
+//               K_c K_i^T and Q_c K_i^T with mma.sync (three of its warps, one block pair each).
 //   warp 12     inverse warp: (I + L)^-1 and -B2 of chunk c while the prep group
 //               builds chunk c + 1.
 // A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
@@ -106,10 +106,11 @@ constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
 // read L.  Chain: G1, G2, G3 (MMA commits).  Cluster schedule (below): FULLOP (home slot s
 // holds a pulled chunk), HFREE (the chain is done with home slot s), READY (on the home CTA,
 // entry 2 h + b: helper h finished the chunk in its slot b), COPIED (on a helper: the home
-// CTA has pulled the chunk in its slot b).
+// CTA has pulled the chunk in its slot b).  OREADY b / OFREE b (cluster home): the chain has
+// finished O in buffer b / the epilogue warps have read it out.
 enum {
     B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 5, B_FULLP = 7, B_FULLD = 9, B_LFREE = 11, B_G1, B_G2, B_G3,
-    B_FULLOP = 15, B_HFREE = 18, B_READY = 21, B_COPIED = 27, B_COUNT = 29
+    B_FULLOP = 15, B_HFREE = 18, B_READY = 21, B_COPIED = 27, B_OREADY = 29, B_OFREE = 31, B_COUNT = 33
 };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
@@ -147,6 +148,10 @@ __host__ __device__ constexpr int l_index(int i, int j) {
 // TMEM columns: S (fp32), O, P then U (fp32), and the bf16 copy of S whose first 16
 // columns carry -R and then U between the GEMMs.
 constexpr uint32_t TM_S = 0, TM_O = 128, TM_P = 160, TM_SB = 192, TM_COLS = 256;
+// The cluster schedule's home CTA has its SM to itself and takes all 512 columns: [O | P] is
+// double-buffered by chunk parity (chunk c uses columns TM_O + 128 (c % 2)), so that the
+// epilogue warps read chunk c's O while the chain runs chunk c + 1.
+constexpr uint32_t TM_OP_STRIDE = 128, TM_COLS_CL = 512;
 
 struct TmaMaps {
     CUtensorMap q, k, v, g, out;   // v, out: boxes of 64 channels with the 128-byte swizzle
@@ -220,13 +225,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
 // Chain group: barrier k of chunk c (0: after the first decay, before chunk 0; 1: after
 // GEMM1 and -B2; 2: after U; 3: after the output staging; 4: after the next decay, for every
 // chunk but the last).
+// The cluster home's chain has no barrier 3 (its epilogue warps stage the output).
+template <bool kCl = false>
 __device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
     if (k == 0) {
         named_bar_sync(2, 128);
         k = 1;
     }
     for (; c < nchunks; ++c, k = 1)
-        for (; k <= (c + 1 < nchunks ? 4 : 3); ++k) named_bar_sync(2, 128);
+        for (; k <= (c + 1 < nchunks ? 4 : 3); ++k)
+            if (!kCl || k != 3) named_bar_sync(2, 128);
+}
+// The cluster home's epilogue warps: one barrier a chunk.
+__device__ __noinline__ void epilogue_wind_down(int c, int nchunks) {
+    for (; c < nchunks; ++c) named_bar_sync(3, 128);
 }
 // Prep group: barrier k of its local chunk j (0: after phase A, 1: after the prefix scan,
 // 2: after phase B, 3: after phase C).
@@ -284,12 +296,12 @@ __device__ __forceinline__ void store_state16(const FwdParams& p, size_t off, co
 
 // The 32 fp32 P columns of this lane (-R after GEMM1, U after GEMM2) -> bf16 -> the
 // first 16 columns of the bf16 copy of S (the A operand of the next GEMM).
-__device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr) {
+__device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr, uint32_t tm_p = TM_P) {
     uint32_t rp[16];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         uint32_t pr[16];
-        tmem_ld16(lane_addr + TM_P + hh * 16, pr);
+        tmem_ld16(lane_addr + tm_p + hh * 16, pr);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 8; ++i) rp[hh * 8 + i] = pack_bf16x2(u2f(pr[2 * i]), u2f(pr[2 * i + 1]));
@@ -492,7 +504,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         tc_fence_before();
         named_bar_sync(2, 128);
     } else {
-        chain_wind_down(0, 0, u.nchunks);
+        chain_wind_down<kCl>(0, 0, u.nchunks);
     }
 
     int sc = 0, kq = 0;   // (cluster home) slot c % NS and round c / NS
@@ -508,6 +520,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const uint32_t cpar = c & 1, kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
         const uint32_t soff = kCl ? slot_off(s) : s * SLOT_BYTES;
         const uint32_t slot = u.base + soff;
+        // [O | P] of this chunk (double-buffered by chunk parity in the cluster home)
+        const uint32_t tO = TM_O + (kCl ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
 
         // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T and P -= V^T, once the prep warps wrote the
         // chunk's operands and its v box landed
@@ -516,14 +530,19 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if constexpr (!kCl) {
             if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
             // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
-            if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) { chain_wind_down(c, 1, u.nchunks); break; }
+            if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
             // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
             beta_next = beta_ahead;
             if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
         }
         if (w == W_MMA) {
             if (kCl && pt == 32) stamp(c, 1);
-            if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) { chain_wind_down(c, 1, u.nchunks); break; }
+            if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
+            // (cluster home) the epilogue warps have read out chunk c - 2's O from this buffer
+            if (kCl && c >= 2 && !warp_wait(bar_addr(u, B_OFREE + (c & 1)), (uint32_t)(((c >> 1) + 1) & 1), p.status, 256)) {
+                chain_wind_down<kCl>(c, 1, u.nchunks);
+                break;
+            }
             tc_fence_after();
             if (kCl && pt == 32) stamp(c, 2);
             auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
@@ -539,9 +558,9 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 tc_commit_warp(bar_addr(u, B_G1));
             } else if constexpr (kWarpIssue) {
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc_mma_ts_warp(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
+                for (int kk = 0; kk < 8; ++kk) tc_mma_ts_warp(u.tmem + tO, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // P -= V^T
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + tP, av(kk), bv(kk), idescv, 1u);   // P -= V^T
                 tc_commit_warp(bar_addr(u, B_G1));
                 if (kCl && pt == 32) stamp(c, 3);
             } else if (lane == 0) {
@@ -554,13 +573,13 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
 
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
-        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) { chain_wind_down(c, 1, u.nchunks); break; }
+        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
         tc_fence_after();
         if (kCl && pt == 0) stamp(c, 4);
-        p_cols_to_bf16(lane_addr);
+        p_cols_to_bf16(lane_addr, tP);
         if (kCl && pt == 0) stamp(c, 5);
         if constexpr (!kCl) {
-            if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) { chain_wind_down(c, 1, u.nchunks); break; }
+            if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
             if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
         }
         tc_fence_before();
@@ -571,7 +590,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             auto b2 = [&](int kk) { return make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512); };
             if constexpr (kWarpIssue) {
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ts_warp(u.tmem + TM_P, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
+                for (int kk = 0; kk < 2; ++kk) tc_mma_ts_warp(u.tmem + tP, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
                 tc_commit_warp(bar_addr(u, B_G2));
                 if (kCl && pt == 32) stamp(c, 7);
             } else if (lane == 0) {
@@ -582,9 +601,9 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
 
         // U -> bf16 -> TMEM: A operand of GEMM3
-        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down(c, 2, u.nchunks); break; }
+        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down<kCl>(c, 2, u.nchunks); break; }
         tc_fence_after();
-        p_cols_to_bf16(lane_addr);
+        p_cols_to_bf16(lane_addr, tP);
         tc_fence_before();
         named_bar_sync(2, 128);
         if (w == W_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
@@ -595,7 +614,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     tc_mma_ts_warp(u.tmem + TM_S, u.tmem + TM_SB + kk * 8, br(kk), idesc3, 1u);
-                    tc_mma_ts_warp(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, bm(kk), idesc2, 1u);
+                    tc_mma_ts_warp(u.tmem + tO, u.tmem + TM_SB + kk * 8, bm(kk), idesc2, 1u);
                 }
                 tc_commit_warp(bar_addr(u, B_G3));
             } else if (lane == 0) {
@@ -607,12 +626,17 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 tc_commit(bar_addr(u, B_G3));
             }
         }
-        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down(c, 3, u.nchunks); break; }
+        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down<kCl>(c, 3, u.nchunks); break; }
         tc_fence_after();
 
         if constexpr (kCl) {
-            // the slot's pulled operands have been read for the last time
-            if (pt == 0) mbar_arrive(bar_addr(u, B_HFREE + s));
+            // the slot's pulled operands have been read for the last time, and this chunk's O is
+            // final: the epilogue warps take it from here
+            if (pt == 0) {
+                mbar_arrive(bar_addr(u, B_HFREE + s));
+                tc_fence_before();
+                mbar_arrive(bar_addr(u, B_OREADY + (c & 1)));
+            }
         } else {
             // The slot's q, k, g regions have been read for the last time: refill them with
             // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
@@ -628,6 +652,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // layout (two [32][64] blocks, 128-byte swizzle): the 16x256b TMEM load gives each
         // thread two adjacent tokens of one state row, and stmatrix.trans writes 8 tokens x
         // 8 rows per matrix as 16-byte rows, conflict-free under the swizzle.
+        if constexpr (!kCl) {   // (the cluster home's epilogue warps do this part for it)
         const bool full = chunk_valid(u, c) == CH;
         if (full) {
             const uint32_t tile = slot + SL_V;
@@ -684,14 +709,15 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             }
             bulk_commit();
         }
+        }
 
         const int s1 = kCl ? (s + 1 == NS ? 0 : s + 1) : (s ^ 1);
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
             if constexpr (kCl) {
-                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down(c, 4, u.nchunks); break; }
+                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down<kCl>(c, 4, u.nchunks); break; }
             } else {
-                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down(c, 4, u.nchunks); break; }
+                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down<kCl>(c, 4, u.nchunks); break; }
             }
             const float* a_next = reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A);
             if constexpr (kSmemState)
@@ -706,7 +732,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             named_bar_sync(2, 128);
             // the output store has had the copy-and-decay pass to read the staging tile: the
             // region takes chunk c + 2's v
-            if (pt == T_STORE && refill) {
+            if (!kCl && pt == T_STORE && refill) {
                 bulk_wait_read_all();
                 load_v(maps, u, c + NS, s);
                 vissued = c + NS + 1;
@@ -727,9 +753,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     }
     if (pt == T_STORE) bulk_wait_all();   // the output must be in global memory before the kernel ends
     if constexpr (kCl) {
-        if (pt == T_STORE)   // v boxes still in flight (only after a timeout can one be unconsumed)
-            for (int c = vissued - NS < 0 ? 0 : vissued - NS; c < vissued; ++c)
-                mbar_wait_bounded(bar_addr(u, B_FULLV + c % NS), (c / NS) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+        (void)vissued;   // the home's epilogue warps wait for the v boxes still in flight
     } else if (pt == T_TMA || pt == T_STORE) {
         // boxes still in flight must land before the CTA exits (only after a timeout can
         // one be unconsumed)
@@ -775,6 +799,9 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
     float* Lb = reinterpret_cast<float*>(u.gbase + OFF_L);
     float* tot = reinterpret_cast<float*>(u.gbase + OFF_MISC);            // [8][128]
     float* totg = tot + PREP_WARPS * HD + 64;                              // [128]
+    // partial rows 4-7 hold their channels rotated by 16, so that the scan's two half-warps
+    // (rows 0-3 and 4-7 of the same channels) use disjoint banks
+    auto trot = [](int qq, int ch) { return (ch + ((qq >> 2) << 4)) & (HD - 1); };
     float* rq = tot + PREP_WARPS * HD;
     float* rk = rq + 32;
 
@@ -841,7 +868,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
                 G01[r] = acc01;
                 G23[r] = acc23;
             }
-            *reinterpret_cast<float4*>(tot + pw * HD + c0) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
+            *reinterpret_cast<float4*>(tot + pw * HD + trot(pw, c0)) = make_float4(acc01.x, acc01.y, acc23.x, acc23.y);
 
             float2 ss0 = make_float2(0.f, 0.f), ss1 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -869,7 +896,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
         //      prefix of warp qq, and totg the chunk total
         {
             const int ch = 16 * pw + (lane & 15), h = lane >> 4;
-            float* col = tot + 4 * h * HD + ch;
+            float* col = tot + 4 * h * HD + trot(4 * h, ch);
             const float x0 = col[0], x1 = col[HD], x2 = col[2 * HD], x3 = col[3 * HD];
             const float s2 = x0 + x1, s3 = s2 + x2, s4 = s3 + x3;
             const float other = __shfl_xor_sync(0xffffffffu, s4, 16);
@@ -885,7 +912,7 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
         {
             float2 T01, T23;
             {
-                const float4 o4 = *reinterpret_cast<const float4*>(tot + pw * HD + c0);
+                const float4 o4 = *reinterpret_cast<const float4*>(tot + pw * HD + trot(pw, c0));
                 const float4 t4 = *reinterpret_cast<const float4*>(totg + c0);
                 float2 off01 = make_float2(o4.x, o4.y), off23 = make_float2(o4.z, o4.w);
                 T01 = make_float2(t4.x, t4.y);
@@ -947,59 +974,50 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
         named_bar_sync(1, PREP_THREADS);
         if (pt == 0) mbar_arrive(bar_addr(u, B_AREADY + s));   // the chain may decay S by a
 
-        // ---- C: K_c K_i^T (warps 0-3) and Q_c K_i^T (warps 4-7), one 16 x 16 block per warp.
-        //      The upper-right block of both is masked to zero, so its warps (0 and 4) skip the products
-        //      (and L keeps no such block).
-        {
-            // blocks (mt, nb) of warp pw: (0,1) [all zero], (0,0), (1,0), (1,1) for pw & 3 = 0..3
-            const int bi = pw & 3, mat = pw >> 2, mt = bi >> 1, nb = (bi & 1) ^ (1 - mt);
-            const unsigned char* Ab = mat ? qcs : kcs;
-            float acc[2][4], acc2[2][4];
+        // ---- C: K_c K_i^T and Q_c K_i^T, the three nonzero 16 x 16 blocks (mt, nb) = (1,0), (1,1),
+        //      (0,0) of each, on warps 1-3; a warp computes the same block of both products, so
+        //      the K_i fragments it loads serve both.  Warp 0 writes the zero upper-right block of
+        //      Mqk (L keeps no such block); warps 4-7 have no part in this phase.
+        if (pw == 0) {   // rows 0-15, columns 16-31: 4 core matrices of 8 rows x 16 bytes, one row a lane
+            const int cm = lane >> 3;
+            *reinterpret_cast<uint4*>(gslot + SL_MQT + core_at(8 * (cm >> 1) + (lane & 7), 16 + 8 * (cm & 1), 32)) =
+                make_uint4(0u, 0u, 0u, 0u);
+        } else if (pw < 4) {
+            const int mt = pw == 3 ? 0 : 1, nb = pw == 2 ? 1 : 0;
+            float acck[2][4], accq[2][4];
 #pragma unroll
             for (int t = 0; t < 2; ++t)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[t][e] = acc2[t][e] = 0.f;
-            if (nb <= mt) {
-                // 16-byte chunk 2 kk + h of row r sits at chunk (2 kk + h) ^ (r % 8) = (h ^ (r % 8)) ^ 2 kk:
-                // k step kk is one XOR of the k-step-0 address with kk << 5 (the tiles are 256-byte aligned)
-                const uint32_t a0 = smem_u32(Ab + sc_at(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, (lane >> 4) * 8));
-                const uint32_t b0 = smem_u32(kis + sc_at(nb * 16 + (lane & 7) + (lane >> 4) * 8, ((lane >> 3) & 1) * 8));
+                for (int e = 0; e < 4; ++e) acck[t][e] = accq[t][e] = 0.f;
+            // 16-byte chunk 2 kk + h of row r sits at chunk (2 kk + h) ^ (r % 8) = (h ^ (r % 8)) ^ 2 kk:
+            // k step kk is one XOR of the k-step-0 address with kk << 5 (the tiles are 256-byte aligned)
+            const uint32_t aoff = sc_at(mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, (lane >> 4) * 8);
+            const uint32_t ak0 = smem_u32(kcs + aoff), aq0 = smem_u32(qcs + aoff);
+            const uint32_t b0 = smem_u32(kis + sc_at(nb * 16 + (lane & 7) + (lane >> 4) * 8, ((lane >> 3) & 1) * 8));
 #pragma unroll
-                for (int kk = 0; kk < 8; kk += 2) {   // two independent chains per n-tile (even / odd k steps)
-                    uint32_t a[4], b[4], a2[4], b2[4];
-                    ldmatrix_x4_s(a, a0 ^ (kk << 5));
-                    ldmatrix_x4_s(b, b0 ^ (kk << 5));
-                    ldmatrix_x4_s(a2, a0 ^ ((kk + 1) << 5));
-                    ldmatrix_x4_s(b2, b0 ^ ((kk + 1) << 5));
-                    mma_bf16_16816(acc[0], a, b[0], b[1]);
-                    mma_bf16_16816(acc[1], a, b[2], b[3]);
-                    mma_bf16_16816(acc2[0], a2, b2[0], b2[1]);
-                    mma_bf16_16816(acc2[1], a2, b2[2], b2[3]);
-                }
-#pragma unroll
-                for (int t = 0; t < 2; ++t)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[t][e] += acc2[t][e];
-                // L is rewritten only once the inverse warp has read the previous chunk's
-                if (mat == 0 && j > 0 && !warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status)) { prep_wind_down(j, 3, nloc); return; }
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t ak[4], aq[4], b[4];
+                ldmatrix_x4_s(b, b0 ^ (kk << 5));
+                ldmatrix_x4_s(ak, ak0 ^ (kk << 5));
+                ldmatrix_x4_s(aq, aq0 ^ (kk << 5));
+                mma_bf16_16816(acck[0], ak, b[0], b[1]);
+                mma_bf16_16816(acck[1], ak, b[2], b[3]);
+                mma_bf16_16816(accq[0], aq, b[0], b[1]);
+                mma_bf16_16816(accq[1], aq, b[2], b[3]);
             }
+            // L is rewritten only once the inverse warp has read the previous chunk's
+            if (j > 0 && !warp_wait(bar_addr(u, B_LFREE), (j - 1) & 1, p.status)) { prep_wind_down(j, 3, nloc); return; }
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int i = mt * 16 + gq + hf * 8;
-                    const int j = nb * 16 + t * 8 + 2 * tq;
-                    const float v0 = acc[t][2 * hf], v1 = acc[t][2 * hf + 1];
+                    const int jj = nb * 16 + t * 8 + 2 * tq;
                     // select, never multiply: the masked upper triangle may hold inf/NaN
-                    if (mat == 0) {
-                        if (nb <= mt) {
-                            Lb[l_at(i, j)] = (j < i) ? bs[i] * v0 : 0.f;
-                            Lb[l_at(i, j + 1)] = (j + 1 < i) ? bs[i] * v1 : 0.f;
-                        }
-                    } else {
-                        *reinterpret_cast<uint32_t*>(gslot + SL_MQT + core_at(i, j, 32)) =
-                            pack_bf16x2((j <= i) ? v0 : 0.f, (j + 1 <= i) ? v1 : 0.f);   // Mqk
-                    }
+                    Lb[l_at(i, jj)] = (jj < i) ? bs[i] * acck[t][2 * hf] : 0.f;
+                    Lb[l_at(i, jj + 1)] = (jj + 1 < i) ? bs[i] * acck[t][2 * hf + 1] : 0.f;
+                    *reinterpret_cast<uint32_t*>(gslot + SL_MQT + core_at(i, jj, 32)) =
+                        pack_bf16x2((jj <= i) ? accq[t][2 * hf] : 0.f, (jj + 1 <= i) ? accq[t][2 * hf + 1] : 0.f);   // Mqk
                 }
             }
         }
@@ -1148,12 +1166,13 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
 // the other has one instance per slot, so no wait can see a phase two ahead of its own.
 // ------------------------------------------------------------------------------
 
-// Home CTA, warps 4-11: once helper h has finished chunk c (READY) and the chain is done
+// Home CTA, warps 4-7: once helper h has finished chunk c (READY) and the chain is done
 // with the chunk before it in home slot h (HFREE), copy the chunk's operands from the
-// helper's shared memory into the slot (16-byte distributed shared-memory loads, 7 or 8 a
+// helper's shared memory into the slot (16-byte distributed shared-memory loads, 15 a
 // thread, all in flight at once), then tell the chain (FULLOP) and the helper (COPIED).
+constexpr int PULL_THREADS = 128;   // home warps 4-7
 __device__ void home_puller(const FwdParams& p, const Unit& u, int pt) {
-    constexpr int PER = (PULL_VECS + PREP_THREADS - 1) / PREP_THREADS;
+    constexpr int PER = (PULL_VECS + PULL_THREADS - 1) / PULL_THREADS;
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
         const int h = c % NHELP, j = c / NHELP, b = j & 1;
@@ -1161,28 +1180,118 @@ __device__ void home_puller(const FwdParams& p, const Unit& u, int pt) {
                                               WAIT_LIMIT, 256);
         ok = ok && mbar_wait_bounded<true>(bar_addr(u, B_READY + 2 * h + b), (j >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
                                            WAIT_LIMIT, 256);
-        if (!named_bar_all(1, PREP_THREADS, ok)) return;   // one verdict for the group: no thread is left at a barrier
+        if (!named_bar_all(1, PULL_THREADS, ok)) return;   // one verdict for the group: no thread is left at a barrier
         const uint32_t src = mapa_shared(u.base + b * SLOT_BYTES, (uint32_t)(h + 1));
         unsigned char* dst = u.gbase + slot_off(h);
         uint4 x[PER];
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int e = pt + PREP_THREADS * i;
+            const int e = pt + PULL_THREADS * i;
             const uint32_t off = e < PULL_VECS_A ? 16u * e : SL_MQT + 16u * (e - PULL_VECS_A);
             if (e < PULL_VECS) x[i] = ld_dsmem_v4(src + off);
         }
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
-            const int e = pt + PREP_THREADS * i;
+            const int e = pt + PULL_THREADS * i;
             const uint32_t off = e < PULL_VECS_A ? 16u * e : SL_MQT + 16u * (e - PULL_VECS_A);
             if (e < PULL_VECS) *reinterpret_cast<uint4*>(dst + off) = x[i];
         }
         fence_proxy_async_smem();   // the operands are read by the tensor core
-        named_bar_sync(1, PREP_THREADS);
+        named_bar_sync(1, PULL_THREADS);
         if (pt == 0) {
             mbar_arrive(bar_addr(u, B_FULLOP + h));
             mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + b), (uint32_t)(h + 1)));
         }
+    }
+}
+
+// Home CTA, warps 8-11 (TMEM lanes 32 (w % 4) ..): once the chain has finished chunk c's O
+// (OREADY, buffer c % 2), read it out, stage it in the slot's v region (GEMM1 has read v) and
+// store it (tensor stores, row copies for a tail chunk), release the buffer (OFREE), then
+// refill the region with chunk c + 3's v once the stores have read it.  This takes the output
+// off the chain's critical path.
+__device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et) {
+    constexpr int NS = NHELP;
+    const int w = et >> 5, lane = et & 31, v = et;
+    const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
+    // chunks whose v boxes have been requested: the chain loads the first NS, this thread the rest
+    int vissued = u.nchunks < NS ? u.nchunks : NS;
+#pragma unroll 1
+    for (int c = 0; c < u.nchunks; ++c) {
+        const int b = c & 1, s = c % NS;
+        const uint32_t soff = slot_off(s), slot = u.base + soff;
+        const uint32_t tO = TM_O + TM_OP_STRIDE * (uint32_t)b;
+        if (!warp_wait(bar_addr(u, B_OREADY + b), (uint32_t)((c >> 1) & 1), p.status, 256)) {
+            epilogue_wind_down(c, u.nchunks);
+            break;
+        }
+        tc_fence_after();
+        const int nvalid = chunk_valid(u, c);
+        if (nvalid == CH) {   // the tile in the v boxes' layout (see the chain's staging)
+            const uint32_t tile = slot + SL_V;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                const int base = 32 * w + 16 * hf;
+                uint32_t o[16];
+                tmem_ld_16x256b_x4(u.tmem + ((uint32_t)base << 16) + tO, o);
+                tmem_wait_ld();
+                const int j = lane >> 3, k = lane & 7;
+                const int v0 = base + 8 * (j & 1);
+#pragma unroll
+                for (int st = 0; st < 2; ++st) {
+                    const int tok = 8 * (2 * st + (j >> 1)) + k;
+                    const uint32_t r0 = pack_bf16x2(u2f(o[8 * st + 0]), u2f(o[8 * st + 1]));
+                    const uint32_t r1 = pack_bf16x2(u2f(o[8 * st + 2]), u2f(o[8 * st + 3]));
+                    const uint32_t r2 = pack_bf16x2(u2f(o[8 * st + 4]), u2f(o[8 * st + 5]));
+                    const uint32_t r3 = pack_bf16x2(u2f(o[8 * st + 6]), u2f(o[8 * st + 7]));
+                    stmatrix_x4_trans_s(tile + sw128_at(tok, v0, 32), r0, r1, r2, r3);
+                }
+            }
+        } else {
+            unsigned char* ost = u.gbase + soff + SL_V + 2 * v;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                uint32_t o[16];
+                tmem_ld16(lane_addr + tO + hh * 16, o);
+                tmem_wait_ld();
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const uint32_t pr = pack_bf16x2(u2f(o[2 * m]), u2f(o[2 * m + 1]));
+                    const int i = hh * 16 + 2 * m;
+                    *reinterpret_cast<uint16_t*>(ost + i * 256) = (uint16_t)(pr & 0xffffu);
+                    *reinterpret_cast<uint16_t*>(ost + (i + 1) * 256) = (uint16_t)(pr >> 16);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        named_bar_sync(3, 128);
+        if (et == 0) {
+            mbar_arrive(bar_addr(u, B_OFREE + b));   // the buffer's columns have been read
+            const int64_t t0 = u.bos + (int64_t)c * CH;
+            const uint32_t ost = slot + SL_V;
+            if (nvalid == CH) {
+                const int tc = (int)KDA_CHK(t0, u.bos, u.eos - CH + 1);
+                tma_store_3d(&maps.out, ost, 0, u.h, tc);
+                tma_store_3d(&maps.out, ost + 4096, 64, u.h, tc);
+            } else {
+                for (int i = 0; i < nvalid; ++i)
+                    bulk_store(p.out + (KDA_CHK(t0 + i, u.bos, u.eos) * p.H + u.h) * HD, ost + i * 256, 256);
+            }
+            bulk_commit();
+            if (c + NS < u.nchunks) {
+                bulk_wait_read_all();
+                load_v(maps, u, c + NS, s);
+                vissued = c + NS + 1;
+            }
+        }
+    }
+    if (et == 0) {
+        bulk_wait_all();   // the output must be in global memory before the kernel ends
+        // the last v boxes requested, by either thread, must have landed (only after a timeout
+        // can one be unconsumed); earlier phases of the same barriers completed before these
+        for (int c = vissued - NS < 0 ? 0 : vissued - NS; c < vissued; ++c)
+            mbar_wait_bounded(bar_addr(u, B_FULLV + c % NS), (c / NS) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
 }
 
@@ -1262,7 +1371,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         tma_prefetch_desc(&maps.out);
     }
     if (warp == 0 && home) {
-        tmem_alloc(u.base + OFF_TMEMADDR, TM_COLS);
+        tmem_alloc(u.base + OFF_TMEMADDR, kCl ? TM_COLS_CL : TM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -1281,7 +1390,8 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         }
     } else if (home) {
         if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
-        else if (warp < W_INV) home_puller(p, u, tid - W_PREP0 * 32);
+        else if (warp < W_PREP0 + 4) home_puller(p, u, tid - W_PREP0 * 32);
+        else if (warp < W_INV) home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32);
     } else {
         const int h = rank - 1;
         const int nloc = u.nchunks > h ? (u.nchunks - h + NHELP - 1) / NHELP : 0;
@@ -1294,7 +1404,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     __syncthreads();
     if (warp == 0 && home) {
         tc_fence_after();
-        tmem_dealloc(u.tmem, TM_COLS);
+        tmem_dealloc(u.tmem, kCl ? TM_COLS_CL : TM_COLS);
     }
     // no CTA leaves while a peer may still read its shared memory or arrive on its barriers
     if constexpr (kCl) cluster_sync_all();
