@@ -11,22 +11,26 @@
 // Per chunk (section 3 notation; R = V^T - P, B2 = diag(beta) INV^T):
 //   GEMM1  [O_0 | P] = S_bf16 [Q_d | K_d]^T           M128 N64  K128  (A = bf16 S from TMEM)
 //          P -= V^T                                   M128 N32  K32   (A = V from SMEM, B = -I)
-//          S = S diag(a)                              CUDA cores, during GEMM1
+//          S = S diag(a)                              CUDA cores, before GEMM3 (its bf16 copy, taken
+//                                                     first, is GEMM1's A operand)
 //   GEMM2  U = (-R) (-B2)                             M128 N32  K32   (A = -R in bf16 from TMEM)
 //   GEMM3  S += U K_r,  O += U Mqk^T                  M128 N128 + N32, K32 (A = U in bf16 from TMEM)
 // The prep warps build Q_d, K_d, K_r, Mqk and L for a chunk (mma.sync for the 32 x 32
 // products) and the inverse warp turns L into -B2, while the chain runs the previous one.
 //
-// Warp roles (416 threads, up to 72 registers each):
+// Warp roles (448 threads, up to 72 registers each):
 //   warps 0-3   chain group: thread v owns state row v (TMEM lane v): initial/final
 //               state I/O, the bf16 copy of S, the decay, R' and the chunk output O.
-//               Single threads of its warps issue the tensor-core MMAs (warp 1), the
-//               TMA loads of q, k, g and beta (warp 2), and the output store and v
-//               loads (warp 3); warp 0 owns the TMEM allocation.
+//               Single threads of its warps issue the TMA loads of q, k, g and beta
+//               (warp 2) and the output store and v loads (warp 3); warp 0 owns the
+//               TMEM allocation.
 //   warps 4-11  prep group: gate, prefix, q/k norms, centered operands (section 2),
 //               K_c K_i^T and Q_c K_i^T with mma.sync (three of its warps, one block pair each).
 //   warp 12     inverse warp: (I + L)^-1 and -B2 of chunk c while the prep group
 //               builds chunk c + 1.
+//   warp 13     MMA warp: issues the chain's tensor-core MMAs as the chain hands each A
+//               operand over (named barriers, arrive / sync), GEMM1's first half of k while
+//               the chain still converts the second half of S.
 // A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
 // consumer (section 4): the chain refills a slot as soon as GEMM3 has read it, and
 // every mbarrier wait is bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
@@ -45,15 +49,15 @@
 namespace kda {
 namespace {
 
-constexpr int TC_THREADS = 416;
+constexpr int TC_THREADS = 448;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
 constexpr int W_INV = W_PREP0 + PREP_WARPS;   // the inverse warp: (I + L)^-1 of chunk c while the prep warps take c + 1
-// Duties of the chain group, spread over its warps (one per SM sub-partition): warp 1
-// issues the MMAs, warp 2 refills q, k, g and beta, warp 3 stores each output tile and
-// then refills v, whose slot region held the tile.  With two CTAs on an SM, lane 0 of
-// warp 1 issues alone (the trickle leaves the tensor pipe to the other warps' mma.sync);
-// with one CTA per SM the whole warp issues through elect.sync, which is faster.
-constexpr int W_MMA = 1, T_TMA = 64, W_BETA = 2, T_STORE = 96;
+constexpr int W_ISSUE = W_INV + 1;            // the MMA warp
+// Duties of the chain group, spread over its warps (one per SM sub-partition): warp 2
+// refills q, k, g and beta, warp 3 stores each output tile and then refills v, whose slot
+// region held the tile.  (With two CTAs on an SM lane 0 of the MMA warp issues alone; with
+// one CTA per SM the whole warp issues through elect.sync.)
+constexpr int T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
 constexpr int NSLOT = 2;
 #ifdef KDA_WAIT_TEST
@@ -222,21 +226,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_
 // normally or see a wait of their own expire (whatever the wound-down warp would have
 // produced never comes) and join it, so no warp is ever left at a barrier, and the fast path
 // keeps its code as it is.
-// Chain group: barrier k of chunk c (0: after the first decay, before chunk 0; 1: after
-// GEMM1 and -B2; 2: after U; 3: after the output staging; 4: after the next decay, for every
-// chunk but the last).
-// The cluster home's chain has no barrier 3 (its epilogue warps stage the output).
-template <bool kCl = false>
-__device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
-    if (k == 0) {
-        named_bar_sync(2, 128);
-        k = 1;
-    }
-    for (; c < nchunks; ++c, k = 1)
-        for (; k <= (c + 1 < nchunks ? 4 : 3); ++k)
-            if (!kCl || k != 3) named_bar_sync(2, 128);
-}
-// The cluster home's epilogue warps: one barrier a chunk.
 __device__ __noinline__ void epilogue_wind_down(int c, int nchunks) {
     for (; c < nchunks; ++c) named_bar_sync(3, 128);
 }
@@ -310,8 +299,26 @@ __device__ __forceinline__ void p_cols_to_bf16(uint32_t lane_addr, uint32_t tm_p
     tmem_wait_st();
 }
 
+// The chain's hand-offs to the MMA warp: named barriers that the chain warps arrive on
+// (bar.arrive, no wait) and the MMA warp syncs on, 160 threads each.  G1A / G1B: the first /
+// second half of the bf16 copy of S is in place (GEMM1's k blocks 0-3 / 4-7); G2: -R is in
+// place and -B2 has been written; G3: U is in place.  Each one is used once per chunk, and
+// the next use of an id waits for an MMA commit that follows the MMA warp's sync on it.
+constexpr int NB_G1A = 4, NB_G1B = 5, NB_G2 = 6, NB_G3 = 7, NB_HAND = 160;
+
+// A finished half of the state pass: this thread's TMEM (or shared-memory) stores are
+// complete and ordered before the MMA warp's GEMM1 issue.
+template <bool kSmem>
+__device__ __forceinline__ void hand_off_half(int id) {
+    tmem_wait_st();
+    if constexpr (kSmem) fence_proxy_async_smem();   // GEMM1 reads the tile
+    tc_fence_before();
+    named_bar_arrive(id, NB_HAND);
+}
+
 // One pass over S: its bf16 copy (the next GEMM1 operand, taken before the decay), then
 // S = S diag(a) in place with the next chunk's a (its GEMM3 adds to the decayed S).
+// Once the first half of the copy is in place it is handed to the MMA warp (G1A).
 // kBf16State (the state-precision ablation) decays the bf16 copy instead, i.e. rounds the
 // carried state to bf16 at every chunk boundary, as a bf16 state store would.
 // kSmem (the shared-memory state alternative): the bf16 copy goes to row `v` of the state tile
@@ -351,6 +358,7 @@ __device__ __forceinline__ void copy_and_decay(uint32_t lane_addr, const float* 
             r[4 * j + 2] = f2u(x1.x); r[4 * j + 3] = f2u(x1.y);
         }
         tmem_st16(lane_addr + TM_S + piece * 16, r);
+        if (piece == 3) hand_off_half<kSmem>(NB_G1A);
     }
 }
 
@@ -388,12 +396,13 @@ __device__ __forceinline__ void copy_and_decay_pipelined(uint32_t lane_addr, con
             c[4 * j + 2] = f2u(x1.x); c[4 * j + 3] = f2u(x1.y);
         }
         tmem_st16(lane_addr + TM_S + piece * 16, c);
+        if (piece == 3) hand_off_half<false>(NB_G1A);
         if (piece + 1 < 8) tmem_wait_ld_regs(r[(piece + 1) & 1]);
     }
 }
 
 // ------------------------------------------------------------------------------
-// Chain group: state row v = TMEM lane v; thread 0 issues the MMAs and the TMA copies.
+// Chain group: state row v = TMEM lane v; single threads issue the TMA copies.
 // ------------------------------------------------------------------------------
 __device__ __forceinline__ int chunk_valid(const Unit& u, int c) {
     const int64_t t0 = u.bos + (int64_t)c * CH;
@@ -446,6 +455,37 @@ __device__ __forceinline__ void put_beta(const Unit& u, int s, int lane, float b
     mbar_arrive(bar_addr(u, B_FULLTMA + s));
 }
 
+// Wind-down of the chain warps (see above).  Step k of chunk c: 0 the state pass before it
+// (hand-offs G1A, G1B), 1 the hand-off G2, 2 the hand-off G3, 3 the barrier after the output
+// staging (not in the cluster home, whose epilogue warps stage the output).  A wound-down
+// warp syncs on the hand-offs instead of arriving: with no waits in between, plain arrivals
+// could reach the next generation of a barrier before the MMA warp has met the current one.
+template <bool kCl = false>
+__device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
+    for (; c < nchunks; ++c, k = 0)
+        for (; k < 4; ++k) {
+            if (k == 0) {
+                named_bar_sync(NB_G1A, NB_HAND);
+                named_bar_sync(NB_G1B, NB_HAND);
+            } else if (k == 1) {
+                named_bar_sync(NB_G2, NB_HAND);
+            } else if (k == 2) {
+                named_bar_sync(NB_G3, NB_HAND);
+            } else if (!kCl) {
+                named_bar_sync(2, 128);
+            }
+        }
+}
+// Wind-down of the MMA warp from the start of chunk c: it meets every hand-off still ahead.
+__device__ __noinline__ void mma_wind_down(int c, int nchunks) {
+    for (; c < nchunks; ++c) {
+        named_bar_sync(NB_G1A, NB_HAND);
+        named_bar_sync(NB_G1B, NB_HAND);
+        named_bar_sync(NB_G2, NB_HAND);
+        named_bar_sync(NB_G3, NB_HAND);
+    }
+}
+
 // kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pulled chunks (FULLOP
 // stands for AREADY, FULLP and FULLD at once), it loads v alone, and it hands each slot back
 // (HFREE) once GEMM3 has read it.
@@ -455,10 +495,6 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     static_assert(!kSmemState || (kBf16State && kWarpIssue && !kCl), "the shared-memory state runs one CTA per SM");
     unsigned char* st_smem = u.gbase + OFF_STATE;
     constexpr int NS = kCl ? NHELP : NSLOT;   // slots in the ring
-    constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
-    constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
-    constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);                // GEMM2, and O += U Mqk^T
-    constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 128, true);         // S += U K_r, B MN-major
     const int w = pt >> 5, lane = pt & 31;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     const int v = pt;
@@ -486,7 +522,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     // ahead (its 2-byte loads, 2H bytes apart, miss the caches)
     float beta_ahead = (!kCl && w == W_BETA && NSLOT < u.nchunks) ? load_beta<kBetaLogit>(p, u, NSLOT, lane) : 0.f;
     int issued = first;    // chunks whose boxes were requested
-    int vissued = first;   // (cluster home) chunks whose v boxes were requested
+    int vissued = first;   // chunks whose v boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
         const int n = pt >> 2, kb = pt & 3;
         const uint32_t m1 = ((n >> 3) == kb) ? ((n & 1) ? 0xBF800000u : 0x0000BF80u) : 0u;   // bf16 -1 at column n
@@ -496,16 +532,20 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         fence_proxy_async_smem();
     }
     tmem_wait_st();
+    // the state pass before chunk c: the bf16 copy of S (GEMM1's A operand) handed to the MMA
+    // warp in two halves, and the decay by chunk c's a
+    auto state_pass = [&](const float* a_s) {
+        if constexpr (kSmemState)
+            copy_and_decay<kBf16State, true>(lane_addr, a_s, st_smem, pt);
+        else if constexpr (kWarpIssue)
+            copy_and_decay_pipelined<kBf16State>(lane_addr, a_s);
+        else
+            copy_and_decay<kBf16State>(lane_addr, a_s);
+        hand_off_half<kSmemState>(NB_G1B);
+    };
     bool ok = warp_wait(bar_addr(u, kCl ? B_FULLOP : B_AREADY), 0, p.status, 256);   // a of chunk 0
-    if (ok) {
-        copy_and_decay<kBf16State, kSmemState>(lane_addr, reinterpret_cast<const float*>(u.gbase + SL_A), st_smem, pt);
-        tmem_wait_st();
-        if constexpr (kSmemState) fence_proxy_async_smem();   // GEMM1 reads the tile
-        tc_fence_before();
-        named_bar_sync(2, 128);
-    } else {
-        chain_wind_down<kCl>(0, 0, u.nchunks);
-    }
+    if (ok) state_pass(reinterpret_cast<const float*>(u.gbase + SL_A));
+    else chain_wind_down<kCl>(0, 0, u.nchunks);
 
     int sc = 0, kq = 0;   // (cluster home) slot c % NS and round c / NS
     // chain trace (cluster schedule): SM clock at KDA_TRACE_POINTS steps of each chunk of one unit
@@ -520,60 +560,19 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const uint32_t cpar = c & 1, kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
         const uint32_t soff = kCl ? slot_off(s) : s * SLOT_BYTES;
         const uint32_t slot = u.base + soff;
-        // [O | P] of this chunk (double-buffered by chunk parity in the cluster home)
         const uint32_t tO = TM_O + (kCl ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
-
-        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T and P -= V^T, once the prep warps wrote the
-        // chunk's operands and its v box landed
         const bool refill = c + NS < u.nchunks;
         float beta_next = 0.f;
         if constexpr (!kCl) {
             if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
-            // (every chain warp waits with a back-off here: the wait spans the prep of a chunk)
-            if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
             // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
             beta_next = beta_ahead;
             if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
         }
-        if (w == W_MMA) {
-            if (kCl && pt == 32) stamp(c, 1);
-            if (!warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
-            // (cluster home) the epilogue warps have read out chunk c - 2's O from this buffer
-            if (kCl && c >= 2 && !warp_wait(bar_addr(u, B_OFREE + (c & 1)), (uint32_t)(((c >> 1) + 1) & 1), p.status, 256)) {
-                chain_wind_down<kCl>(c, 1, u.nchunks);
-                break;
-            }
-            tc_fence_after();
-            if (kCl && pt == 32) stamp(c, 2);
-            auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
-            auto av = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024); };
-            auto bv = [&](int kk) { return make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512); };
-            if constexpr (kSmemState) {   // A = the bf16 state tile in shared memory
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    tc_mma_ss_warp(u.tmem + TM_O, make_sdesc_kmajor_sw128(u.base + OFF_STATE + (kk >> 2) * STATE_BLOCK + (kk & 3) * 32),
-                                   b1(kk), idesc1, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // P -= V^T
-                tc_commit_warp(bar_addr(u, B_G1));
-            } else if constexpr (kWarpIssue) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc_mma_ts_warp(u.tmem + tO, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ss_warp(u.tmem + tP, av(kk), bv(kk), idescv, 1u);   // P -= V^T
-                tc_commit_warp(bar_addr(u, B_G1));
-                if (kCl && pt == 32) stamp(c, 3);
-            } else if (lane == 0) {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ss(u.tmem + TM_P, av(kk), bv(kk), idescv, 1u);   // tokens 16 kk ..
-                tc_commit(bar_addr(u, B_G1));
-            }
-        }
 
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
-        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
+        // (the wait spans GEMM1, and the prep of the chunk when that runs late)
+        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status, 64)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
         tc_fence_after();
         if (kCl && pt == 0) stamp(c, 4);
         p_cols_to_bf16(lane_addr, tP);
@@ -583,49 +582,15 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
         }
         tc_fence_before();
-        named_bar_sync(2, 128);
+        named_bar_arrive(NB_G2, NB_HAND);
         if (kCl && pt == 0) stamp(c, 6);
-        if (w == W_MMA) {   // GEMM2 U = (-R) (-B2), into the P columns
-            tc_fence_after();
-            auto b2 = [&](int kk) { return make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512); };
-            if constexpr (kWarpIssue) {
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ts_warp(u.tmem + tP, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
-                tc_commit_warp(bar_addr(u, B_G2));
-                if (kCl && pt == 32) stamp(c, 7);
-            } else if (lane == 0) {
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) tc_mma_ts(u.tmem + TM_P, u.tmem + TM_SB + kk * 8, b2(kk), idesc2, kk > 0);
-                tc_commit(bar_addr(u, B_G2));
-            }
-        }
 
         // U -> bf16 -> TMEM: A operand of GEMM3
         if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down<kCl>(c, 2, u.nchunks); break; }
         tc_fence_after();
         p_cols_to_bf16(lane_addr, tP);
         tc_fence_before();
-        named_bar_sync(2, 128);
-        if (w == W_MMA) {   // GEMM3: S += U K_r, O += U Mqk^T
-            tc_fence_after();
-            auto br = [&](int kk) { return make_sdesc_mnmajor_sw128(slot + SL_KR + kk * 2048, 4096, 1024); };
-            auto bm = [&](int kk) { return make_sdesc_kmajor_noswizzle(slot + SL_MQT + kk * 256, 128, 512); };
-            if constexpr (kWarpIssue) {
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    tc_mma_ts_warp(u.tmem + TM_S, u.tmem + TM_SB + kk * 8, br(kk), idesc3, 1u);
-                    tc_mma_ts_warp(u.tmem + tO, u.tmem + TM_SB + kk * 8, bm(kk), idesc2, 1u);
-                }
-                tc_commit_warp(bar_addr(u, B_G3));
-            } else if (lane == 0) {
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    tc_mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8, br(kk), idesc3, 1u);
-                    tc_mma_ts(u.tmem + TM_O, u.tmem + TM_SB + kk * 8, bm(kk), idesc2, 1u);
-                }
-                tc_commit(bar_addr(u, B_G3));
-            }
-        }
+        named_bar_arrive(NB_G3, NB_HAND);
         if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down<kCl>(c, 3, u.nchunks); break; }
         tc_fence_after();
 
@@ -645,7 +610,6 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 issued = c + NSLOT + 1;
             }
         }
-
         // O of this chunk -> staging tile [token][v] in the slot's v region (GEMM1 has read
         // v) -> tensor stores (row copies for a tail chunk); once the stores have read the
         // tile, the region takes chunk c + 2's v.  A full chunk's tile has the v boxes'
@@ -715,23 +679,13 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
             if constexpr (kCl) {
-                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down<kCl>(c, 4, u.nchunks); break; }
+                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down<kCl>(c + 1, 0, u.nchunks); break; }
             } else {
-                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down<kCl>(c, 4, u.nchunks); break; }
+                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down<kCl>(c + 1, 0, u.nchunks); break; }
             }
-            const float* a_next = reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A);
-            if constexpr (kSmemState)
-                copy_and_decay<kBf16State, true>(lane_addr, a_next, st_smem, pt);
-            else if constexpr (kWarpIssue)
-                copy_and_decay_pipelined<kBf16State>(lane_addr, a_next);
-            else
-                copy_and_decay<kBf16State>(lane_addr, a_next);
-            tmem_wait_st();
-            if constexpr (kSmemState) fence_proxy_async_smem();   // GEMM1 reads the tile
-            tc_fence_before();
-            named_bar_sync(2, 128);
-            // the output store has had the copy-and-decay pass to read the staging tile: the
-            // region takes chunk c + 2's v
+            state_pass(reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A));
+            // the output store has had the state pass to read the staging tile: the region
+            // takes chunk c + 2's v
             if (!kCl && pt == T_STORE && refill) {
                 bulk_wait_read_all();
                 load_v(maps, u, c + NS, s);
@@ -752,15 +706,122 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
     }
     if (pt == T_STORE) bulk_wait_all();   // the output must be in global memory before the kernel ends
-    if constexpr (kCl) {
-        (void)vissued;   // the home's epilogue warps wait for the v boxes still in flight
-    } else if (pt == T_TMA || pt == T_STORE) {
+    (void)vissued;
+    if (!kCl && pt == T_TMA) {
         // boxes still in flight must land before the CTA exits (only after a timeout can
         // one be unconsumed)
-        const int b0 = pt == T_TMA ? B_FULLTMA : B_FULLV;
         for (int c = issued - NSLOT < 0 ? 0 : issued - NSLOT; c < issued; ++c)
-            mbar_wait_bounded(bar_addr(u, b0 + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+            mbar_wait_bounded(bar_addr(u, B_FULLTMA + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
+    if (!kCl && pt == T_STORE) {
+        // likewise the v boxes: the last NS requested (phases before them have completed)
+        for (int c = vissued - NSLOT < 0 ? 0 : vissued - NSLOT; c < vissued; ++c)
+            mbar_wait_bounded(bar_addr(u, B_FULLV + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+    }
+}
+
+// ------------------------------------------------------------------------------
+// MMA warp: issues every tensor-core MMA of the chain (kWarpIssue: the whole warp through
+// elect.sync; else lane 0 alone), each once the chain has handed its A operand over, and
+// commits each GEMM to its mbarrier (G1, G2, G3).  GEMM1's k blocks 0-3 go out while the chain
+// still converts and decays the second half of S.
+// ------------------------------------------------------------------------------
+template <bool kWarpIssue, bool kCl, bool kSmemState>
+__device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
+    constexpr int NS = kCl ? NHELP : NSLOT;
+    constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
+    constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
+    constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);                // GEMM2, and O += U Mqk^T
+    constexpr uint32_t idesc3 = make_idesc_bf16_f32(128, 128, true);         // S += U K_r, B MN-major
+    auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kWarpIssue) tc_mma_ts_warp(d, a, b, id, acc);
+        else if (lane == 0) tc_mma_ts(d, a, b, id, acc);
+    };
+    auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+        if constexpr (kWarpIssue) tc_mma_ss_warp(d, a, b, id, acc);
+        else if (lane == 0) tc_mma_ss(d, a, b, id, acc);
+    };
+    auto commit = [&](uint32_t bar) {
+        if constexpr (kWarpIssue) tc_commit_warp(bar);
+        else if (lane == 0) tc_commit(bar);
+    };
+    int committed = 0;   // chunks whose GEMM3 was committed
+    int sc = 0, kq = 0;
+    const bool trace_me = kCl && lane == 0 && p.trace != nullptr && (int64_t)u.n * p.H + u.h == p.trace_unit;
+    auto stamp = [&](int c, int i) {
+        if (trace_me && c < p.trace_chunks) p.trace[(size_t)c * KDA_TRACE_POINTS + i] = (unsigned long long)clock64();
+    };
+#pragma unroll 1
+    for (int c = 0; c < u.nchunks; ++c) {
+        const int s = kCl ? sc : (c & 1);
+        const uint32_t kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
+        const uint32_t slot = u.base + (kCl ? slot_off(s) : s * SLOT_BYTES);
+        const uint32_t tO = TM_O + (kCl ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
+        // the chunk's operands (the cluster home's chain waited for the pulled chunk before its
+        // state pass) and its v box; (cluster home) the epilogue warps have read out chunk c - 2's
+        // O from this buffer
+        stamp(c, 1);
+        bool ok = kCl || warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256);
+        ok = ok && warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256);
+        if (kCl && c >= 2) ok = ok && warp_wait(bar_addr(u, B_OFREE + (c & 1)), (uint32_t)(((c >> 1) + 1) & 1), p.status, 256);
+        if (!ok) {
+            mma_wind_down(c, u.nchunks);
+            break;
+        }
+        stamp(c, 2);
+        auto b1 = [&](int kk) { return make_sdesc_kmajor_sw128(slot + SL_QDKD + (kk >> 2) * 8192 + (kk & 3) * 32); };
+        auto gemm1 = [&](int kk) {
+            if constexpr (kSmemState)
+                mma_ss(u.tmem + tO, make_sdesc_kmajor_sw128(u.base + OFF_STATE + (kk >> 2) * STATE_BLOCK + (kk & 3) * 32),
+                       b1(kk), idesc1, kk > 0);
+            else
+                mma_ts(u.tmem + tO, u.tmem + TM_SB + kk * 8, b1(kk), idesc1, kk > 0);
+        };
+        // GEMM1 [O_0 | P] = S_bf16 [Q_d | K_d]^T, in two halves of k, then P -= V^T
+        named_bar_sync(NB_G1A, NB_HAND);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) gemm1(kk);
+        named_bar_sync(NB_G1B, NB_HAND);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 4; kk < 8; ++kk) gemm1(kk);
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+            mma_ss(u.tmem + tP, make_sdesc_mnmajor_sw128(slot + SL_V + kk * 2048, 4096, 1024),
+                   make_sdesc_kmajor_noswizzle(u.base + OFF_NEGI + kk * 256, 128, 512), idescv, 1u);   // P -= V^T
+        commit(bar_addr(u, B_G1));
+        stamp(c, 3);
+        // GEMM2 U = (-R) (-B2), into the P columns
+        named_bar_sync(NB_G2, NB_HAND);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk)
+            mma_ts(u.tmem + tP, u.tmem + TM_SB + kk * 8, make_sdesc_kmajor_noswizzle(slot + SL_INV + kk * 256, 128, 512), idesc2,
+                   kk > 0);
+        commit(bar_addr(u, B_G2));
+        stamp(c, 7);
+        // GEMM3: S += U K_r, O += U Mqk^T
+        named_bar_sync(NB_G3, NB_HAND);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            mma_ts(u.tmem + TM_S, u.tmem + TM_SB + kk * 8, make_sdesc_mnmajor_sw128(slot + SL_KR + kk * 2048, 4096, 1024),
+                   idesc3, 1u);
+            mma_ts(u.tmem + tO, u.tmem + TM_SB + kk * 8, make_sdesc_kmajor_noswizzle(slot + SL_MQT + kk * 256, 128, 512),
+                   idesc2, 1u);
+        }
+        commit(bar_addr(u, B_G3));
+        committed = c + 1;
+        if constexpr (kCl) {
+            sc = s + 1 == NS ? 0 : s + 1;
+            if (sc == 0) ++kq;
+        }
+    }
+    // the MMAs must be complete before the CTA frees its Tensor Memory (after a wind-down the
+    // chain may not have waited for the last ones); MMAs complete in order
+    if (committed > 0)
+        mbar_wait_bounded(bar_addr(u, B_G3), (uint32_t)((committed - 1) & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
 }
 
 // ------------------------------------------------------------------------------
@@ -1385,19 +1446,22 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
             chain_group<kBf16State, kWarpIssue, kBetaLogit, false, kSmemState>(p, maps, u, tid);
         } else if (warp < W_INV) {
             prep_group<kSoftplus, 1>(p, u, tid - W_PREP0 * 32, 0, u.nchunks);
-        } else {
+        } else if (warp == W_INV) {
             inverse_warp(p, u, tid & 31, u.nchunks);
+        } else {
+            mma_warp<kWarpIssue, false, kSmemState>(p, u, tid & 31);
         }
     } else if (home) {
         if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
         else if (warp < W_PREP0 + 4) home_puller(p, u, tid - W_PREP0 * 32);
         else if (warp < W_INV) home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32);
+        else if (warp == W_ISSUE) mma_warp<true, true, false>(p, u, tid & 31);
     } else {
         const int h = rank - 1;
         const int nloc = u.nchunks > h ? (u.nchunks - h + NHELP - 1) / NHELP : 0;
         if (warp < W_PREP0) helper_io<kBetaLogit>(p, maps, u, tid, h, nloc);
         else if (warp < W_INV) prep_group<kSoftplus, NHELP>(p, u, tid - W_PREP0 * 32, h, nloc);
-        else inverse_warp(p, u, tid & 31, nloc);
+        else if (warp == W_INV) inverse_warp(p, u, tid & 31, nloc);
     }
 
     tc_fence_before();
@@ -1533,7 +1597,7 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
         e = cudaLaunchKernelEx(&cfg, ck, p, maps);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
-    // one CTA per SM: the chain issues its MMAs warp-wide (the interface variants are
+    // one CTA per SM: the MMA warp issues warp-wide (the interface variants are
     // separate instantiations, so the default one is unchanged)
     const bool lone = sched == KDA_SCHEDULE_ONE_PER_SM, sp = (p.flags & KDA_FLAG_GATE_SOFTPLUS) != 0;
     const bool lg = (p.flags & KDA_FLAG_BETA_LOGIT) != 0;

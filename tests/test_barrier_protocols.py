@@ -327,13 +327,17 @@ def test_ring_without_lfree_overwrites_l():
 # bar.sync, no waits, no work) until the sequence ends.  Its siblings either finish normally
 # or see a wait of their own expire (what the wound-down warp would have produced never
 # comes) and wind down too.  The model replays, per warp, the waits, arrivals and barriers of
-# the chain group (4 warps: warp 1 issues the MMAs, warp 2 the q/k/g box loads and beta,
-# warp 3 the stores and v loads), the prep group (8 warps; warps 1-3 wait for LFREE before
-# writing L) and the inverse warp, with the box loads and MMA commits as asynchronous
-# engines.  One producer arrival is withheld, or delayed past the waiters' limit, and waits
-# may expire at any poll past the limit.  Every warp must then reach the kernel's final
-# __syncthreads.  The same model without the wind-down (each warp leaving the loop on its own
-# verdict, the earlier form) must be able to hang.
+# the chain group (4 warps: warp 2 issues the q/k/g box loads and beta, warp 3 the stores and
+# v loads), the MMA warp (it issues each GEMM once the chain warps have handed its operand
+# over: named barriers the chain warps arrive on and the MMA warp syncs on), the prep group
+# (8 warps; warps 1-3 wait for LFREE before writing L) and the inverse warp, with the box
+# loads and MMA commits as asynchronous engines.  One producer arrival is withheld, or
+# delayed past the waiters' limit, and waits may expire at any poll past the limit.  Every
+# warp must then reach the kernel's final __syncthreads, and no warp may arrive on a hand-off
+# barrier twice within one of its generations.  The same model without the wind-down (each
+# warp leaving the loop on its own verdict, the earlier form) must be able to hang, and a
+# wind-down that arrives on the hand-offs instead of syncing on them must be able to overrun
+# one.
 # ---------------------------------------------------------------------------------------
 
 UNBOUNDED = 2   # blocked on a named barrier: only other warps' arrivals can release it
@@ -355,15 +359,52 @@ class NamedBar:
             yield (UNBOUNDED, self, g)
 
 
+class Overrun(AssertionError):
+    pass
+
+
+class HandBar:
+    """A named barrier over `count` warps that some warps arrive on (bar.arrive, no wait) and
+    one syncs on (bar.sync).  A warp arriving again before the generation it arrived in has
+    completed would count towards that generation: an overrun."""
+
+    def __init__(self, count, name):
+        self.count, self.gen, self.arrived, self.name, self.who = count, 0, 0, name, set()
+
+    def _add(self, w):
+        if w in self.who:
+            raise Overrun(f"{self.name}: warp {w} arrived twice in generation {self.gen}")
+        self.who.add(w)
+        self.arrived += 1
+        if self.arrived == self.count:
+            self.gen, self.arrived, self.who = self.gen + 1, 0, set()
+
+    def arrive(self, w):
+        self._add(w)
+
+    def sync(self, w):
+        g = self.gen
+        self._add(w)
+        while self.gen == g:
+            yield (UNBOUNDED, self, g)
+
+
+HANDOFFS = ("G1A", "G1B", "G2", "G3")   # GEMM1's two halves of k, GEMM2, GEMM3
+
+
 class RingRun:
     """One CTA of the two-slot ring over n chunks.  `perturb` = (barrier name, completion
     index, "withhold" | "late"); `limit` = polls before a wait may expire; `wind_down` = the
-    kernel's wind-down after an expired wait (False: the earlier form, which just leaves)."""
+    kernel's wind-down after an expired wait (False: the earlier form, which just leaves);
+    `sync_handoffs` = a wound-down chain warp syncs on the hand-off barriers (False: it only
+    arrives, as on the fast path)."""
 
-    def __init__(self, n, seed, perturb=None, limit=40, wind_down=True):
+    def __init__(self, n, seed, perturb=None, limit=40, wind_down=True, sync_handoffs=True):
         self.n, self.rng, self.perturb, self.limit, self.wind_down = n, random.Random(seed), perturb, limit, wind_down
+        self.sync_handoffs = sync_handoffs
         self.bars, self.engines, self.timeouts, self.consumed = {}, [], 0, []
-        self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(13)
+        self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(14)
+        self.hand = {k: HandBar(5, k) for k in HANDOFFS}   # 4 chain warps + the MMA warp
         self.fulltma_fill = {0: 0, 1: 0}
         self.exited = 0
 
@@ -421,19 +462,35 @@ class RingRun:
             self.fulltma(c)
         self.engines.append(run())
 
-    def chain_wind_down(self, c, k):
-        """Barrier k of chunk c onwards (0: before chunk 0; 1: after GEMM1 and -B2; 2: after
-        U; 3: after the output staging; 4: after the next decay, all chunks but the last)."""
+    def hand_off(self, w, *names):
+        for name in names:
+            self.hand[name].arrive(w)
+
+    def chain_wind_down(self, w, c, k):
+        """Step k of chunk c onwards (0: the state pass before it, hand-offs G1A and G1B; 1:
+        hand-off G2; 2: hand-off G3; 3: the barrier after the output staging)."""
         if not self.wind_down:
             return
-        if k == 0:
-            yield from self.chain_bar.sync()
-            k = 1
         while c < self.n:
-            while k <= (4 if c + 1 < self.n else 3):
-                yield from self.chain_bar.sync()
+            while k < 4:
+                names = (("G1A", "G1B"), ("G2",), ("G3",))[k] if k < 3 else ()
+                for name in names:
+                    if self.sync_handoffs:
+                        yield from self.hand[name].sync(w)
+                    else:
+                        self.hand[name].arrive(w)
+                if k == 3:
+                    yield from self.chain_bar.sync()
                 k += 1
-            c, k = c + 1, 1
+            c, k = c + 1, 0
+
+    def mma_wind_down(self, c):
+        """Every hand-off of chunk c onwards."""
+        if not self.wind_down:
+            return
+        for _ in range(c, self.n):
+            for name in HANDOFFS:
+                yield from self.hand[name].sync("mma")
 
     def prep_wind_down(self, j, k):
         """Barrier k (0: after phase A, 1: after the prefix scan, 2: after phase B, 3: after
@@ -457,51 +514,45 @@ class RingRun:
                 if w == 3:
                     self.engine("FULLV", c >> 1, c)
             ok = yield from self.bwait(self.bar("AREADY", 0), 0)
-            if ok:
-                yield from self.chain_bar.sync()
+            if ok:                                        # the state pass, handed over in halves
+                yield WORK
+                self.hand_off(w, "G1A")
+                yield WORK
+                self.hand_off(w, "G1B")
             else:
-                yield from self.chain_wind_down(0, 0)
+                yield from self.chain_wind_down(w, 0, 0)
             for c in range(n if ok else 0):
                 s, k, refill = c & 1, c >> 1, c + 2 < n
-                if not (yield from self.bwait(self.bar("FULLP", s), k)):
-                    yield from self.chain_wind_down(c, 1)
-                    break
-                if w == 1:
-                    if not (yield from self.bwait(self.bar("FULLV", s), k)):
-                        yield from self.chain_wind_down(c, 1)
-                        break
-                    self.engine("G1", c)
                 if not (yield from self.bwait(self.bar("G1"), c)):
-                    yield from self.chain_wind_down(c, 1)
+                    yield from self.chain_wind_down(w, c, 1)
                     break
                 if not (yield from self.bwait(self.bar("FULLD", s), k)):
-                    yield from self.chain_wind_down(c, 1)
+                    yield from self.chain_wind_down(w, c, 1)
                     break
                 if refill and w == 2:
                     self.fulltma(c + 2)                   # beta of chunk c + 2
-                yield from self.chain_bar.sync()
-                if w == 1:
-                    self.engine("G2", c)
+                self.hand_off(w, "G2")
                 if not (yield from self.bwait(self.bar("G2"), c)):
-                    yield from self.chain_wind_down(c, 2)
+                    yield from self.chain_wind_down(w, c, 2)
                     break
-                yield from self.chain_bar.sync()
-                if w == 1:
-                    self.engine("G3", c)
+                self.hand_off(w, "G3")
                 if not (yield from self.bwait(self.bar("G3"), c)):
-                    yield from self.chain_wind_down(c, 3)
+                    yield from self.chain_wind_down(w, c, 3)
                     break
                 if refill and w == 2:
                     self.load_qkg(c + 2)
                     issued_qkg = c + 3
-                yield from self.chain_bar.sync()
+                yield from self.chain_bar.sync()          # the output staging
                 if w == 0:
                     self.consumed.append(c)
                 if c + 1 < n:
                     if not (yield from self.bwait(self.bar("AREADY", s ^ 1), (c + 1) >> 1)):
-                        yield from self.chain_wind_down(c, 4)
+                        yield from self.chain_wind_down(w, c + 1, 0)
                         break
-                    yield from self.chain_bar.sync()
+                    yield WORK
+                    self.hand_off(w, "G1A")
+                    yield WORK
+                    self.hand_off(w, "G1B")
                     if w == 3 and refill:
                         self.engine("FULLV", (c + 2) >> 1, s)
                         issued_v = c + 3
@@ -512,6 +563,31 @@ class RingRun:
             if w == 3:
                 for c in range(max(0, issued_v - 2), issued_v):
                     yield from self.bwait(self.bar("FULLV", c & 1), c >> 1)
+        yield from self.cta_bar.sync()
+        self.exited += 1
+
+    def mma_warp(self):
+        committed = 0
+        for c in range(self.n):
+            s, k = c & 1, c >> 1
+            ok = yield from self.bwait(self.bar("FULLP", s), k)
+            ok = ok and (yield from self.bwait(self.bar("FULLV", s), k))
+            if not ok:
+                yield from self.mma_wind_down(c)
+                break
+            yield from self.hand["G1A"].sync("mma")
+            yield from self.hand["G1B"].sync("mma")
+            self.engine("G1", c)
+            yield from self.hand["G2"].sync("mma")
+            self.engine("G2", c)
+            yield from self.hand["G3"].sync("mma")
+            self.engine("G3", c)
+            committed = c + 1
+        if committed:   # the last commit, before the Tensor Memory is freed (in order on the hardware;
+            b, polls = self.bar("G3"), 0   # a withheld commit exists only in the model)
+            while b.done < committed and polls < 3 * self.limit:
+                polls += 1
+                yield BLOCKED
         yield from self.cta_bar.sync()
         self.exited += 1
 
@@ -546,7 +622,8 @@ class RingRun:
         self.exited += 1
 
     def run(self):
-        live = [self.chain_warp(w) for w in range(4)] + [self.prep_warp(p) for p in range(8)] + [self.inverse_warp()]
+        live = [self.chain_warp(w) for w in range(4)] + [self.prep_warp(p) for p in range(8)] + \
+            [self.inverse_warp(), self.mma_warp()]
         state = {id(a): WORK for a in live}
         while live or self.engines:
             live += self.engines
@@ -562,7 +639,8 @@ class RingRun:
                 state[id(a)] = next(a)
             except StopIteration:
                 live.remove(a)
-        assert self.exited == 13
+        assert self.exited == 14
+        assert all(h.arrived == 0 for h in self.hand.values()), "a hand-off generation left incomplete"
         return self
 
 
@@ -591,12 +669,27 @@ def test_every_warp_winds_down_after_an_expired_wait(name, index, mode):
 
 def test_leaving_without_wind_down_can_leave_a_warp_at_a_barrier():
     """The earlier form (a warp whose wait expired leaves the loop at once) hangs when a
-    phase completes just after some of the group's waits expired."""
+    phase completes just after some of the group's waits expired, or leaves a hand-off
+    barrier with arrivals that no generation completes."""
     hung = 0
     for name, index in PERTURB:
         for seed in range(30):
             try:
                 RingRun(10, seed, perturb=(name, index, "late"), wind_down=False).run()
-            except Deadlock:
+            except AssertionError:   # Deadlock, Overrun, or a hand-off left incomplete
                 hung += 1
     assert hung > 0
+
+
+def test_wind_down_that_only_arrives_on_the_hand_offs_can_overrun_one():
+    """A wound-down chain warp has no waits left between its hand-offs: arriving (instead of
+    syncing) it can reach the next generation of a hand-off barrier before the MMA warp has
+    met the current one."""
+    overrun = 0
+    for name, index in PERTURB:
+        for seed in range(30):
+            try:
+                RingRun(10, seed, perturb=(name, index, "withhold"), sync_handoffs=False).run()
+            except Overrun:
+                overrun += 1
+    assert overrun > 0
