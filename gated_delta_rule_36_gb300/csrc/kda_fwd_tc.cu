@@ -108,15 +108,16 @@ constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
 // cluster's home CTA), AREADY (the prep warps wrote a), FULLP (the prep warps finished the
 // chunk's operands and L), FULLD (the inverse warp wrote -B2).  LFREE: the inverse warp has
 // read L.  Chain: G1, G2, G3 (MMA commits).  Cluster schedule (below): FULLOP (home slot s
-// holds a pulled chunk), HFREE (the chain is done with home slot s), READY (on the home CTA,
-// entry 2 h + b: helper h finished the chunk in its slot b), COPIED (on a helper: the home
-// CTA has pulled the chunk in its slot b).  OREADY b / OFREE b (cluster home): the chain has
-// finished O in buffer b / the epilogue warps have read it out.
+// holds a pushed chunk: the courier's arrival and the copies' bytes), HFREE (the chain is done
+// with home slot s), HSLOT (on a helper: its home slot is free for its next chunk), COPIED (on
+// a helper: the push of the chunk in its slot b has landed).  OREADY b / OFREE b (cluster
+// home): the chain has finished O in buffer b / the epilogue warps have read it out.
 enum {
     B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 5, B_FULLP = 7, B_FULLD = 9, B_LFREE = 11, B_G1, B_G2, B_G3,
-    B_FULLOP = 15, B_HFREE = 18, B_READY = 21, B_COPIED = 27, B_OREADY = 29, B_OFREE = 31, B_COUNT = 33
+    B_FULLOP = 15, B_HFREE = 18, B_HSLOT = 21, B_COPIED = 27, B_OREADY = 29, B_OFREE = 31, B_COUNT = 33
 };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
+constexpr uint32_t OFF_PUSHED = OFF_TMEMADDR + 4;   // (cluster home) pushes issued by helper h, at + 4 h
 constexpr uint32_t SMEM_USED = OFF_TMEMADDR + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;      // slack to align the base to 1 KB
 static_assert(SLOT_BYTES % 1024 == 0, "slots must keep the 128-B swizzle atoms 1 KB aligned");
@@ -126,8 +127,8 @@ static_assert(OFF_L % 16 == 0 && OFF_X % 16 == 0 && OFF_NEGI % 16 == 0, "float4 
 
 // Cluster schedule, for few units: a cluster of 1 + NHELP CTAs per unit.  The home CTA (rank
 // 0) runs the chain over NHELP slots; helper h (rank h + 1) prepares the chunks c = h (mod
-// NHELP) in its own two slots with the prep and inverse warps, and the home CTA's prep warps
-// pull each finished chunk over distributed shared memory into home slot h.
+// NHELP) in its own two slots with the prep and inverse warps and pushes each finished chunk
+// into home slot h with a shared -> distributed shared memory bulk copy.
 constexpr int NHELP = 3, CL_SIZE = NHELP + 1;
 constexpr uint32_t OFF_SLOT2 = (SMEM_USED + 1023) & ~1023u;   // the home CTA's third slot
 constexpr uint32_t SMEM_BYTES_CL = OFF_SLOT2 + SLOT_BYTES + 1024;
@@ -139,10 +140,25 @@ constexpr uint32_t OFF_STATE = (SMEM_USED + 1023) & ~1023u;
 constexpr uint32_t STATE_BLOCK = 128 * 128;
 constexpr uint32_t SMEM_BYTES_SS = OFF_STATE + 2 * STATE_BLOCK + 1024;
 static_assert(SMEM_BYTES_SS <= 232448, "the shared-memory state layout must fit one CTA's shared memory");
-// The pulled part of a slot: [Q_d | K_d] and K_r (bytes [0, SL_V)), then Mqk, -B2 and a
+// The pushed part of a slot: [Q_d | K_d] and K_r (bytes [0, SL_V)), then Mqk, -B2 and a
 // (bytes [SL_MQT, SL_BETA)); v is the home CTA's own.
-constexpr int PULL_VECS_A = SL_V / 16, PULL_VECS = PULL_VECS_A + (SL_BETA - SL_MQT) / 16;
+constexpr uint32_t PUSH_A = SL_V, PUSH_B = SL_BETA - SL_MQT, PUSH_BYTES = PUSH_A + PUSH_B;
+static_assert(PUSH_A % 16 == 0 && PUSH_B % 16 == 0 && SL_MQT % 16 == 0, "bulk copies move 16-byte units");
+static_assert(OFF_PUSHED + 4 * NHELP <= SMEM_USED, "the push counts live beside the TMEM address");
 __host__ __device__ constexpr uint32_t slot_off(int s) { return s < 2 ? (uint32_t)s * SLOT_BYTES : OFF_SLOT2; }
+
+// Shared -> distributed shared memory bulk copy: `bytes` (a multiple of 16) from this CTA's
+// `src` to `dst` in a peer CTA, completing its transaction bytes on the peer's mbarrier `mbar`
+// (dst and mbar are shared::cluster addresses, 16- and 8-byte aligned).
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+                 "r"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+// A 32-bit store into a peer CTA's shared memory.
+__device__ __forceinline__ void st_dsmem_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;\n" ::"r"(cluster_addr), "r"(v) : "memory");
+}
 
 // Index of element (i, j), j < 16 or i, j >= 16, of L in its block layout.
 __host__ __device__ constexpr int l_index(int i, int j) {
@@ -486,7 +502,7 @@ __device__ __noinline__ void mma_wind_down(int c, int nchunks) {
     }
 }
 
-// kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pulled chunks (FULLOP
+// kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pushed chunks (FULLOP
 // stands for AREADY, FULLP and FULLD at once), it loads v alone, and it hands each slot back
 // (HFREE) once GEMM3 has read it.
 // kSmemState: the bf16 state resident in shared memory (with kBf16State and kWarpIssue).
@@ -595,7 +611,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         tc_fence_after();
 
         if constexpr (kCl) {
-            // the slot's pulled operands have been read for the last time, and this chunk's O is
+            // the slot's pushed operands have been read for the last time, and this chunk's O is
             // final: the epilogue warps take it from here
             if (pt == 0) {
                 mbar_arrive(bar_addr(u, B_HFREE + s));
@@ -757,7 +773,7 @@ __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
         const uint32_t kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
         const uint32_t slot = u.base + (kCl ? slot_off(s) : s * SLOT_BYTES);
         const uint32_t tO = TM_O + (kCl ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
-        // the chunk's operands (the cluster home's chain waited for the pulled chunk before its
+        // the chunk's operands (the cluster home's chain waited for the pushed chunk before its
         // state pass) and its v box; (cluster home) the epilogue warps have read out chunk c - 2's
         // O from this buffer
         stamp(c, 1);
@@ -1223,46 +1239,43 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
 
 // ------------------------------------------------------------------------------
 // Cluster schedule.  Chunk c is prepared by helper h = c % NHELP as its chunk j = c / NHELP,
-// in its slot j % 2, and pulled into home slot h.  Every barrier that one side completes for
+// in its slot j % 2, and pushed into home slot h.  Every barrier that one side completes for
 // the other has one instance per slot, so no wait can see a phase two ahead of its own.
 // ------------------------------------------------------------------------------
 
-// Home CTA, warps 4-7: once helper h has finished chunk c (READY) and the chain is done
-// with the chunk before it in home slot h (HFREE), copy the chunk's operands from the
-// helper's shared memory into the slot (16-byte distributed shared-memory loads, 15 a
-// thread, all in flight at once), then tell the chain (FULLOP) and the helper (COPIED).
-constexpr int PULL_THREADS = 128;   // home warps 4-7
-__device__ void home_puller(const FwdParams& p, const Unit& u, int pt) {
-    constexpr int PER = (PULL_VECS + PULL_THREADS - 1) / PULL_THREADS;
+// Home CTA, lane 0 of warp 4, the courier: for chunk c in home slot h = c % NHELP, once its
+// push has landed (FULLOP) it tells helper h that its slot may be refilled (COPIED); once the
+// chain is done with the chunk (HFREE) it arms the slot for chunk c + NHELP (the arrival and
+// the bytes to come) and tells helper h it may push that chunk (HSLOT).  obs[h] counts the
+// pushes into slot h it has seen land.
+__device__ void home_courier(const FwdParams& p, const Unit& u, int (&obs)[NHELP]) {
+    const int n = u.nchunks;
+    int armed = n < NHELP ? n : NHELP;   // chunks whose slot has been armed (the first NHELP at the start)
 #pragma unroll 1
-    for (int c = 0; c < u.nchunks; ++c) {
+    for (int c = 0; c < armed; ++c) {
         const int h = c % NHELP, j = c / NHELP, b = j & 1;
-        bool ok = j == 0 || mbar_wait_bounded(bar_addr(u, B_HFREE + h), (j - 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
-                                              WAIT_LIMIT, 256);
-        ok = ok && mbar_wait_bounded<true>(bar_addr(u, B_READY + 2 * h + b), (j >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT,
-                                           WAIT_LIMIT, 256);
-        if (!named_bar_all(1, PULL_THREADS, ok)) return;   // one verdict for the group: no thread is left at a barrier
-        const uint32_t src = mapa_shared(u.base + b * SLOT_BYTES, (uint32_t)(h + 1));
-        unsigned char* dst = u.gbase + slot_off(h);
-        uint4 x[PER];
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = pt + PULL_THREADS * i;
-            const uint32_t off = e < PULL_VECS_A ? 16u * e : SL_MQT + 16u * (e - PULL_VECS_A);
-            if (e < PULL_VECS) x[i] = ld_dsmem_v4(src + off);
+        if (!mbar_wait_bounded(bar_addr(u, B_FULLOP + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256))
+            continue;   // (no more arming: the drain at the end covers a push still in flight)
+        ++obs[h];
+        mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + b), (uint32_t)(h + 1)));
+        if (c + NHELP < n && armed == c + NHELP &&
+            mbar_wait_bounded(bar_addr(u, B_HFREE + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) {
+            mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
+            mbar_arrive_remote(mapa_shared(bar_addr(u, B_HSLOT), (uint32_t)(h + 1)));
+            armed = c + NHELP + 1;
         }
-#pragma unroll
-        for (int i = 0; i < PER; ++i) {
-            const int e = pt + PULL_THREADS * i;
-            const uint32_t off = e < PULL_VECS_A ? 16u * e : SL_MQT + 16u * (e - PULL_VECS_A);
-            if (e < PULL_VECS) *reinterpret_cast<uint4*>(dst + off) = x[i];
-        }
-        fence_proxy_async_smem();   // the operands are read by the tensor core
-        named_bar_sync(1, PULL_THREADS);
-        if (pt == 0) {
-            mbar_arrive(bar_addr(u, B_FULLOP + h));
-            mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + b), (uint32_t)(h + 1)));
-        }
+    }
+}
+
+// The courier again, once every CTA of the cluster has published its push count: wait until
+// every push issued has landed (a push is only issued into an armed slot, at most one of them
+// not yet seen per slot), so that no copy is in flight when a CTA of the cluster exits.
+__device__ void home_drain(const FwdParams& p, const Unit& u, const int (&obs)[NHELP]) {
+#pragma unroll 1
+    for (int h = 0; h < NHELP; ++h) {
+        const int pushed = *reinterpret_cast<volatile int*>(u.gbase + OFF_PUSHED + 4 * h);
+        for (int j = obs[h]; j < pushed; ++j)
+            mbar_wait_bounded(bar_addr(u, B_FULLOP + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
 }
 
@@ -1357,8 +1370,9 @@ __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Uni
 }
 
 // Helper CTA, warps 0-3: warp 2 loads the q, k, g boxes (lane 0) and beta of the helper's
-// chunks into its two slots, the slot of chunk j once the home CTA has pulled chunk j - 2;
-// lane 0 of warp 3 tells the home CTA when the prep and inverse warps have finished a chunk.
+// chunks into its two slots, the slot of chunk j once the push of chunk j - 2 has landed;
+// lane 0 of warp 3 pushes each chunk the prep and inverse warps have finished into the home
+// slot, once that is free, and at the end publishes how many pushes it issued.
 template <bool kBetaLogit>
 __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt, int h, int nloc) {
     const int w = pt >> 5, lane = pt & 31;
@@ -1380,15 +1394,24 @@ __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u
             for (int j = loaded - 2 < 0 ? 0 : loaded - 2; j < loaded; ++j)
                 mbar_wait_bounded(bar_addr(u, B_FULLTMA + (j & 1)), (j >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     } else if (pt == T_STORE) {
+        const uint32_t dst = mapa_shared(u.base + slot_off(h), 0u), full = mapa_shared(bar_addr(u, B_FULLOP + h), 0u);
+        int pushed = 0;
 #pragma unroll 1
         for (int j = 0; j < nloc; ++j) {
             const int b = j & 1;
             const uint32_t par = (j >> 1) & 1;
             if (!mbar_wait_bounded(bar_addr(u, B_FULLP + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
             if (!mbar_wait_bounded(bar_addr(u, B_FULLD + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
-            fence_acq_rel_cluster();   // the prep and inverse warps' writes, for the home CTA's loads
-            mbar_arrive_remote(mapa_shared(bar_addr(u, B_READY + 2 * h + b), 0u));
+            // the home slot is free (the courier armed it) from the helper's second chunk on
+            if (j > 0 && !mbar_wait_bounded<true>(bar_addr(u, B_HSLOT), (uint32_t)((j - 1) & 1), p.status,
+                                                   KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256))
+                break;
+            const uint32_t src = u.base + b * SLOT_BYTES;
+            bulk_copy_to_peer(dst, src, PUSH_A, full);
+            bulk_copy_to_peer(dst + SL_MQT, src + SL_MQT, PUSH_B, full);
+            pushed = j + 1;
         }
+        st_dsmem_u32(mapa_shared(u.base + OFF_PUSHED + 4 * h, 0u), (uint32_t)pushed);
     }
 }
 
@@ -1407,6 +1430,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
 #endif
     const int rank = kCl ? (int)cluster_ctarank() : 0;   // 0: the home CTA
     const bool home = rank == 0;
+    int obs[NHELP] = {0, 0, 0};   // (cluster home courier) pushes seen landing per home slot
     Unit u;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -1423,6 +1447,10 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         for (int s = 0; s < NSLOT; ++s) mbar_init(bar_addr(u, B_FULLTMA + s), 33);
         for (int b = B_FULLV; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
         mbar_fence_init();
+        if (kCl && home) {   // the first NHELP home slots await their pushes
+            for (int h = 0; h < NHELP && h < u.nchunks; ++h) mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
+            for (int h = 0; h < NHELP; ++h) *reinterpret_cast<int*>(u.gbase + OFF_PUSHED + 4 * h) = 0;
+        }
     }
     if (tid == 32) {
         tma_prefetch_desc(&maps.q);
@@ -1453,8 +1481,11 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         }
     } else if (home) {
         if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
-        else if (warp < W_PREP0 + 4) home_puller(p, u, tid - W_PREP0 * 32);
-        else if (warp < W_INV) home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32);
+        else if (warp < W_PREP0 + 4) {   // warps 4-7: lane 0 of warp 4 is the courier, the rest idle
+            if (warp == W_PREP0 && (tid & 31) == 0) home_courier(p, u, obs);
+        } else if (warp < W_INV) {
+            home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32);
+        }
         else if (warp == W_ISSUE) mma_warp<true, true, false>(p, u, tid & 31);
     } else {
         const int h = rank - 1;
@@ -1470,8 +1501,16 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         tc_fence_after();
         tmem_dealloc(u.tmem, kCl ? TM_COLS_CL : TM_COLS);
     }
-    // no CTA leaves while a peer may still read its shared memory or arrive on its barriers
-    if constexpr (kCl) cluster_sync_all();
+    // no CTA leaves while a peer may still read its shared memory, write it or arrive on its
+    // barriers: every CTA has published its push count; the home waits for the pushes in flight
+    if constexpr (kCl) {
+        cluster_sync_all();
+        if (home && warp == W_PREP0) {
+            if ((tid & 31) == 0) home_drain(p, u, obs);
+            __syncwarp();   // converged at the aligned cluster barrier
+        }
+        cluster_sync_all();
+    }
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).

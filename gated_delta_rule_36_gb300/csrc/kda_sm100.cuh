@@ -207,21 +207,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
-// 16 bytes of another CTA's shared memory (distributed shared memory).
-__device__ __forceinline__ uint4 ld_dsmem_v4(uint32_t cluster_addr) {
-    uint4 v;
-    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];\n"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(cluster_addr)
-                 : "memory");
-    return v;
-}
 // Arrive on an mbarrier of another CTA of the cluster, releasing this thread's prior
 // accesses at cluster scope.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;\n" ::: "memory"); }
 // Every thread of every CTA of the cluster (all must call it).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
@@ -236,17 +226,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int count) {
     asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
-}
-// Named barrier over `count` threads that also returns the AND of their `pred`: a verdict
-// every participant shares.
-__device__ __forceinline__ bool named_bar_all(int id, int count, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
 }
 // Arrive on a named barrier without waiting (the producer side of a bar.sync consumer).
 __device__ __forceinline__ void named_bar_arrive(int id, int count) {

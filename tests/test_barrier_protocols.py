@@ -3,21 +3,21 @@ cluster schedule's hand-offs between CTAs (first part), the two-slot ring inside
 (second part), and the ring warp by warp when a bounded wait expires (third part).
 
 The cluster schedule of the prefill kernel splits a unit over four CTAs: the home CTA runs
-the chain over three slots, helper h prepares chunks c = h (mod 3) in its own two slots, and
-the home CTA's pulling warps copy each finished chunk across.  Their hand-offs are mbarrier
-phases: FULLOP and HFREE per home slot, READY per (helper, helper slot), COPIED and the box
-loads (FULLTMA) per helper slot.  An mbarrier wait names only a phase's parity, so a wait
-passes as soon as the barrier's completion count has the other parity: one completion too
-few or one too many both look alike.  The kernel relies on every wait being for the
-completion right after the last one its thread saw, and on no barrier completing twice
-before its waiter looks.
+the chain over three slots, helper h prepares chunks c = h (mod 3) in its own two slots and
+pushes each finished chunk into home slot h with a bulk copy that completes on the home's
+FULLOP barrier.  A courier thread on the home CTA arms FULLOP for each push (an arrival plus
+the bytes to come), tells the helper when its home slot is free (HSLOT) and when a push has
+landed, so that the helper slot may be refilled (COPIED).  An mbarrier wait names only a
+phase's parity, so a wait passes as soon as the barrier's completion count has the other
+parity: one completion too few or one too many both look alike.  The kernel relies on every
+wait being for the completion right after the last one its thread saw, and on no barrier
+completing twice before its waiter looks.
 
 This model replays the same waits and arrivals (the same slot indices and parities) with
-that hardware rule, in random orders, and checks that nothing deadlocks, that every wait
-passes on exactly the completion it stands for, and that no slot is overwritten before it
-is read.  A variant with one READY barrier per helper instead of one per helper slot, a
-plausible simplification, must fail: its parity waits block on a completion that needs the
-waiter's own progress, or pass on the wrong one.
+that hardware rule, in random orders, with each push in flight for a while, and checks that
+nothing deadlocks, that every wait passes on exactly the completion it stands for, that no
+push lands in a slot that was not armed for it, and that no slot is overwritten before it
+is read.  A helper that pushed without waiting for HSLOT must fail.
 
 The ring model covers one CTA's slots (box loads and beta on FULLTMA, v on FULLV, the prep
 group's AREADY and FULLP, the inverse warp's LFREE and FULLD) and the slot regions each step
@@ -38,6 +38,25 @@ class Barrier:
         self.done += 1
 
 
+class TxBarrier(Barrier):
+    """An mbarrier whose phases complete on an arrival with its expected bytes (arm) and the
+    bytes themselves (land): a landing in a phase that was never armed is an error."""
+
+    def __init__(self, name):
+        super().__init__(name)
+        self.arms = self.lands = 0
+
+    def arm(self):
+        self.arms += 1
+        self.done = min(self.arms, self.lands)
+
+    def land(self):
+        self.lands += 1
+        if self.lands > self.arms:
+            raise AssertionError(f"{self.name}: bytes landed in a phase not armed")
+        self.done = min(self.arms, self.lands)
+
+
 class Aliased(AssertionError):
     pass
 
@@ -49,17 +68,18 @@ class Deadlock(AssertionError):
 BLOCKED, WORK = 0, 1
 
 
-def make_actors(n_chunks, ready_per_slot=True):
+def make_actors(n_chunks, wait_hslot=True):
     bars = {}
 
     def bar(*key):
         if key not in bars:
-            bars[key] = Barrier(key)
+            bars[key] = TxBarrier(key) if key[0] == "FULLOP" else Barrier(key)
         return bars[key]
 
     home = [None] * NSH                          # (state, chunk) of each home slot
     helper = [[None, None] for _ in range(NH)]   # (state, chunk) of each helper slot
     consumed = []
+    engines = []
 
     def wait(b, k):
         """Wait for completion k (0-based) of barrier b: parity k & 1, the hardware rule."""
@@ -68,17 +88,14 @@ def make_actors(n_chunks, ready_per_slot=True):
         if b.done != k + 1:
             raise Aliased(f"{b.name}: waited for completion {k}, passed at {b.done} completions")
 
-    def ready(h, b):
-        return bar("READY", h, b) if ready_per_slot else bar("READY", h)
-
-    def ready_index(j):
-        return j >> 1 if ready_per_slot else j
+    for h in range(min(NSH, n_chunks)):          # the first pushes are armed before anyone runs
+        bar("FULLOP", h).arm()
 
     def chain():
         yield from wait(bar("FULLOP", 0), 0)                       # a of chunk 0
         for c in range(n_chunks):
             s = c % NSH
-            assert home[s] == ("pulled", c), (c, home[s])           # GEMM1..GEMM3 read the slot
+            assert home[s] == ("pushed", c), (c, home[s])           # GEMM1..GEMM3 read the slot
             home[s] = ("consumed", c)
             consumed.append(c)
             bar("HFREE", s).arrive()
@@ -86,20 +103,29 @@ def make_actors(n_chunks, ready_per_slot=True):
                 yield from wait(bar("FULLOP", (c + 1) % NSH), (c + 1) // NSH)
             yield WORK
 
-    def puller():
-        for c in range(n_chunks):
-            h, j, hs, r = c % NH, c // NH, c % NSH, c // NSH
-            b = j & 1
-            if r > 0:
-                yield from wait(bar("HFREE", hs), r - 1)
-            yield from wait(ready(h, b), ready_index(j))
-            assert helper[h][b] == ("prepared", c), (c, helper[h][b])
-            assert home[hs] is None or home[hs] == ("consumed", c - NSH), (c, home[hs])
-            home[hs] = ("pulled", c)
-            helper[h][b] = ("copied", c)
-            bar("FULLOP", hs).arrive()
-            bar("COPIED", h, b).arrive()
+    def courier():
+        armed = min(NSH, n_chunks)
+        c = 0
+        while c < armed:
+            h, j = c % NSH, c // NSH
+            yield from wait(bar("FULLOP", h), j)                    # the push of chunk c has landed
+            bar("COPIED", h, j & 1).arrive()
+            if c + NSH < n_chunks:
+                yield from wait(bar("HFREE", h), j)                 # the chain is done with chunk c
+                bar("FULLOP", h).arm()
+                bar("HSLOT", h).arrive()
+                armed += 1
+            c += 1
+
+    def push(h, b, c):                            # the bulk copy, in flight for a while
+        for _ in range(random.randrange(1, 4)):
             yield WORK
+        hs = c % NSH
+        assert home[hs] is None or home[hs] == ("consumed", c - NSH), (c, home[hs])
+        assert helper[h][b] == ("pushing", c), (c, helper[h][b])
+        home[hs] = ("pushed", c)
+        helper[h][b] = ("pushed", c)
+        bar("FULLOP", hs).land()
 
     def loader(h):
         j = 0
@@ -107,14 +133,14 @@ def make_actors(n_chunks, ready_per_slot=True):
             c, b = h + NH * j, j & 1
             if j >= 2:
                 yield from wait(bar("COPIED", h, b), (j - 2) >> 1)
-            assert helper[h][b] is None or helper[h][b] == ("copied", c - 2 * NH), (c, helper[h][b])
+            assert helper[h][b] is None or helper[h][b] == ("pushed", c - 2 * NH), (c, helper[h][b])
             helper[h][b] = ("loading", c)
             yield WORK                                              # the boxes are in flight
             helper[h][b] = ("loaded", c)
             bar("FULLTMA", h, b).arrive()
             j += 1
 
-    def prep(h):   # prep group, inverse warp and the READY notifier of helper h
+    def prep(h):   # prep group and inverse warp of helper h
         j = 0
         while h + NH * j < n_chunks:
             c, b = h + NH * j, j & 1
@@ -122,26 +148,41 @@ def make_actors(n_chunks, ready_per_slot=True):
             assert helper[h][b] == ("loaded", c), (c, helper[h][b])
             yield WORK
             helper[h][b] = ("prepared", c)
-            ready(h, b).arrive()
+            bar("PREPARED", h, b).arrive()
             j += 1
 
-    actors = [chain(), puller()] + [loader(h) for h in range(NH)] + [prep(h) for h in range(NH)]
-    return actors, consumed
+    def pusher(h):
+        j = 0
+        while h + NH * j < n_chunks:
+            c, b = h + NH * j, j & 1
+            yield from wait(bar("PREPARED", h, b), j >> 1)
+            if j > 0 and wait_hslot:
+                yield from wait(bar("HSLOT", h), j - 1)
+            helper[h][b] = ("pushing", c)
+            engines.append(push(h, b, c))
+            j += 1
+
+    actors = [chain(), courier()] + [loader(h) for h in range(NH)] + [prep(h) for h in range(NH)] + \
+        [pusher(h) for h in range(NH)]
+    return actors, engines, consumed
 
 
-def run(n_chunks, seed, ready_per_slot=True):
+def run(n_chunks, seed, wait_hslot=True):
     rng = random.Random(seed)
-    actors, consumed = make_actors(n_chunks, ready_per_slot)
+    random.seed(seed)
+    actors, engines, consumed = make_actors(n_chunks, wait_hslot)
     live = list(actors)
     idle = 0   # consecutive steps in which the chosen actor was polling a blocked wait
-    while live:
+    while live or engines:
+        live += engines
+        engines.clear()
         a = rng.choice(live)
         try:
             idle = idle + 1 if next(a) == BLOCKED else 0
         except StopIteration:
             live.remove(a)
             idle = 0
-        if idle > 200 * len(live):
+        if idle > 200 * max(1, len(live)):
             raise Deadlock(f"{len(live)} actors all waiting")
     assert consumed == list(range(n_chunks))
 
@@ -152,14 +193,14 @@ def test_protocol_holds_under_random_interleavings(n_chunks):
         run(n_chunks, seed)
 
 
-def test_one_ready_barrier_per_helper_would_alias():
-    """With READY shared by a helper's two slots, a fast helper completes it twice before the
-    home CTA looks: the parity wait then stands for the wrong phase."""
+def test_pushing_without_waiting_for_the_home_slot_overwrites_it():
+    """A helper that pushes its next chunk as soon as it is prepared lands it in a home slot
+    the chain has not finished with (or in a phase the courier never armed)."""
     broken = 0
     for seed in range(20):
         try:
-            run(40, seed, ready_per_slot=False)
-        except (Aliased, Deadlock):
+            run(40, seed, wait_hslot=False)
+        except AssertionError:
             broken += 1
     assert broken > 0
 
