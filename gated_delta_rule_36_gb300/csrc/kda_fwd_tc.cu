@@ -108,13 +108,13 @@ constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
 // cluster's home CTA), AREADY (the prep warps wrote a), FULLP (the prep warps finished the
 // chunk's operands and L), FULLD (the inverse warp wrote -B2).  LFREE: the inverse warp has
 // read L.  Chain: G1, G2, G3 (MMA commits).  Cluster schedule (below): FULLOP (home slot s
-// holds a pushed chunk: the courier's arrival and the copies' bytes), HFREE (the chain is done
-// with home slot s), HSLOT (on a helper: its home slot is free for its next chunk), COPIED (on
-// a helper: the push of the chunk in its slot b has landed).  OREADY b / OFREE b (cluster
-// home): the chain has finished O in buffer b / the epilogue warps have read it out.
+// holds a pushed chunk: the arming arrival and the copies' bytes), HSLOT (on a helper: its home
+// slot is free for its next chunk), COPIED (on a helper: the push of the chunk in its slot b
+// has landed and been consumed).  OREADY b / OFREE b (cluster home): the chain has finished
+// chunk c (its O in buffer b = c % 2) / the epilogue warps have read the O out.
 enum {
     B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 5, B_FULLP = 7, B_FULLD = 9, B_LFREE = 11, B_G1, B_G2, B_G3,
-    B_FULLOP = 15, B_HFREE = 18, B_HSLOT = 21, B_COPIED = 27, B_OREADY = 29, B_OFREE = 31, B_COUNT = 33
+    B_FULLOP = 15, B_HSLOT = 18, B_COPIED = 19, B_OREADY = 21, B_OFREE = 23, B_COUNT = 25
 };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t OFF_PUSHED = OFF_TMEMADDR + 4;   // (cluster home) pushes issued by helper h, at + 4 h
@@ -503,8 +503,8 @@ __device__ __noinline__ void mma_wind_down(int c, int nchunks) {
 }
 
 // kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pushed chunks (FULLOP
-// stands for AREADY, FULLP and FULLD at once), it loads v alone, and it hands each slot back
-// (HFREE) once GEMM3 has read it.
+// stands for AREADY, FULLP and FULLD at once), it loads v alone, and once GEMM3 has read a slot
+// it signals OREADY, on which the epilogue warps also hand the slot back to its helper.
 // kSmemState: the bf16 state resident in shared memory (with kBf16State and kWarpIssue).
 template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSmemState = false>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
@@ -614,7 +614,6 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             // the slot's pushed operands have been read for the last time, and this chunk's O is
             // final: the epilogue warps take it from here
             if (pt == 0) {
-                mbar_arrive(bar_addr(u, B_HFREE + s));
                 tc_fence_before();
                 mbar_arrive(bar_addr(u, B_OREADY + (c & 1)));
             }
@@ -1243,48 +1242,30 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
 // the other has one instance per slot, so no wait can see a phase two ahead of its own.
 // ------------------------------------------------------------------------------
 
-// Home CTA, lane 0 of warp 4, the courier: for chunk c in home slot h = c % NHELP, once its
-// push has landed (FULLOP) it tells helper h that its slot may be refilled (COPIED); once the
-// chain is done with the chunk (HFREE) it arms the slot for chunk c + NHELP (the arrival and
-// the bytes to come) and tells helper h it may push that chunk (HSLOT).  obs[h] counts the
-// pushes into slot h it has seen land.
-__device__ void home_courier(const FwdParams& p, const Unit& u, int (&obs)[NHELP]) {
-    const int n = u.nchunks;
-    int armed = n < NHELP ? n : NHELP;   // chunks whose slot has been armed (the first NHELP at the start)
-#pragma unroll 1
-    for (int c = 0; c < armed; ++c) {
-        const int h = c % NHELP, j = c / NHELP, b = j & 1;
-        if (!mbar_wait_bounded(bar_addr(u, B_FULLOP + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256))
-            continue;   // (no more arming: the drain at the end covers a push still in flight)
-        ++obs[h];
-        mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + b), (uint32_t)(h + 1)));
-        if (c + NHELP < n && armed == c + NHELP &&
-            mbar_wait_bounded(bar_addr(u, B_HFREE + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) {
-            mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
-            mbar_arrive_remote(mapa_shared(bar_addr(u, B_HSLOT), (uint32_t)(h + 1)));
-            armed = c + NHELP + 1;
-        }
-    }
-}
-
-// The courier again, once every CTA of the cluster has published its push count: wait until
-// every push issued has landed (a push is only issued into an armed slot, at most one of them
-// not yet seen per slot), so that no copy is in flight when a CTA of the cluster exits.
-__device__ void home_drain(const FwdParams& p, const Unit& u, const int (&obs)[NHELP]) {
+// Once every CTA of the cluster has published its push count: wait until every push issued
+// has landed, so that no copy is in flight when a CTA of the cluster exits.  seen[h] chunks of
+// home slot h were finished by the chain (their pushes landed); a push is only issued into an
+// armed slot, and a slot is armed for its next chunk only once the chain has finished the
+// one before, so at most one push a slot is left to wait for.
+__device__ void home_drain(const FwdParams& p, const Unit& u, const int (&seen)[NHELP]) {
 #pragma unroll 1
     for (int h = 0; h < NHELP; ++h) {
         const int pushed = *reinterpret_cast<volatile int*>(u.gbase + OFF_PUSHED + 4 * h);
-        for (int j = obs[h]; j < pushed; ++j)
+        for (int j = seen[h]; j < pushed; ++j)
             mbar_wait_bounded(bar_addr(u, B_FULLOP + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
 }
 
-// Home CTA, warps 8-11 (TMEM lanes 32 (w % 4) ..): once the chain has finished chunk c's O
-// (OREADY, buffer c % 2), read it out, stage it in the slot's v region (GEMM1 has read v) and
-// store it (tensor stores, row copies for a tail chunk), release the buffer (OFREE), then
-// refill the region with chunk c + 3's v once the stores have read it.  This takes the output
-// off the chain's critical path.
-__device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et) {
+// Home CTA, warps 8-11 (TMEM lanes 32 (w % 4) ..): once the chain has finished chunk c
+// (OREADY, its O in buffer c % 2), read the O out, stage it in the slot's v region (GEMM1 has
+// read v) and store it (tensor stores, row copies for a tail chunk), release the buffer
+// (OFREE), then refill the region with chunk c + 3's v once the stores have read it.  This
+// takes the output off the chain's critical path.  The chunk's helper h = c % NHELP hears from
+// two single threads meanwhile: lane 0 of warp 9 arms home slot h for chunk c + NHELP (an
+// arrival and the bytes to come) and tells the helper it may push that chunk (HSLOT); lane 0
+// of warp 10 tells it that the helper slot which held chunk c may be refilled (COPIED).
+// seen[h] (lane 0 of warp 9) counts the chunks of home slot h the chain has finished.
+__device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et, int (&seen)[NHELP]) {
     constexpr int NS = NHELP;
     const int w = et >> 5, lane = et & 31, v = et;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
@@ -1300,6 +1281,18 @@ __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Uni
             break;
         }
         tc_fence_after();
+        {
+            const int h = c % NHELP;
+            if (et == 32) {
+                ++seen[h];
+                if (c + NHELP < u.nchunks) {
+                    mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
+                    mbar_arrive_remote(mapa_shared(bar_addr(u, B_HSLOT), (uint32_t)(h + 1)));
+                }
+            } else if (et == 64) {
+                mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + ((c / NHELP) & 1)), (uint32_t)(h + 1)));
+            }
+        }
         const int nvalid = chunk_valid(u, c);
         if (nvalid == CH) {   // the tile in the v boxes' layout (see the chain's staging)
             const uint32_t tile = slot + SL_V;
@@ -1402,7 +1395,7 @@ __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u
             const uint32_t par = (j >> 1) & 1;
             if (!mbar_wait_bounded(bar_addr(u, B_FULLP + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
             if (!mbar_wait_bounded(bar_addr(u, B_FULLD + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
-            // the home slot is free (the courier armed it) from the helper's second chunk on
+            // the home slot is free (and armed for this push) from the helper's second chunk on
             if (j > 0 && !mbar_wait_bounded<true>(bar_addr(u, B_HSLOT), (uint32_t)((j - 1) & 1), p.status,
                                                    KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256))
                 break;
@@ -1430,7 +1423,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
 #endif
     const int rank = kCl ? (int)cluster_ctarank() : 0;   // 0: the home CTA
     const bool home = rank == 0;
-    int obs[NHELP] = {0, 0, 0};   // (cluster home courier) pushes seen landing per home slot
+    int seen[NHELP] = {0, 0, 0};   // (cluster home, lane 0 of warp 9) chunks finished per home slot
     Unit u;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -1481,11 +1474,8 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         }
     } else if (home) {
         if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
-        else if (warp < W_PREP0 + 4) {   // warps 4-7: lane 0 of warp 4 is the courier, the rest idle
-            if (warp == W_PREP0 && (tid & 31) == 0) home_courier(p, u, obs);
-        } else if (warp < W_INV) {
-            home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32);
-        }
+        else if (warp < W_PREP0 + 4) {}   // warps 4-7 have no part in the home CTA
+        else if (warp < W_INV) home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32, seen);
         else if (warp == W_ISSUE) mma_warp<true, true, false>(p, u, tid & 31);
     } else {
         const int h = rank - 1;
@@ -1505,8 +1495,8 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     // barriers: every CTA has published its push count; the home waits for the pushes in flight
     if constexpr (kCl) {
         cluster_sync_all();
-        if (home && warp == W_PREP0) {
-            if ((tid & 31) == 0) home_drain(p, u, obs);
+        if (home && warp == W_PREP0 + 5) {
+            if ((tid & 31) == 0) home_drain(p, u, seen);
             __syncwarp();   // converged at the aligned cluster barrier
         }
         cluster_sync_all();

@@ -5,9 +5,11 @@ cluster schedule's hand-offs between CTAs (first part), the two-slot ring inside
 The cluster schedule of the prefill kernel splits a unit over four CTAs: the home CTA runs
 the chain over three slots, helper h prepares chunks c = h (mod 3) in its own two slots and
 pushes each finished chunk into home slot h with a bulk copy that completes on the home's
-FULLOP barrier.  A courier thread on the home CTA arms FULLOP for each push (an arrival plus
-the bytes to come), tells the helper when its home slot is free (HSLOT) and when a push has
-landed, so that the helper slot may be refilled (COPIED).  An mbarrier wait names only a
+FULLOP barrier.  Once the chain has finished a chunk (OREADY, one barrier per output buffer,
+chunk c in buffer c % 2; the chain reuses a buffer only after OFREE, once the epilogue has
+read it out), the home's epilogue warps arm FULLOP for the slot's next push (an arrival plus
+the bytes to come), tell the helper that its home slot is free (HSLOT) and that the helper
+slot which held the chunk may be refilled (COPIED).  An mbarrier wait names only a
 phase's parity, so a wait passes as soon as the barrier's completion count has the other
 parity: one completion too few or one too many both look alike.  The kernel relies on every
 wait being for the completion right after the last one its thread saw, and on no barrier
@@ -95,27 +97,26 @@ def make_actors(n_chunks, wait_hslot=True):
         yield from wait(bar("FULLOP", 0), 0)                       # a of chunk 0
         for c in range(n_chunks):
             s = c % NSH
+            if c >= 2:                                              # its O buffer has been read out
+                yield from wait(bar("OFREE", c & 1), (c >> 1) - 1)
             assert home[s] == ("pushed", c), (c, home[s])           # GEMM1..GEMM3 read the slot
             home[s] = ("consumed", c)
             consumed.append(c)
-            bar("HFREE", s).arrive()
+            bar("OREADY", c & 1).arrive()
             if c + 1 < n_chunks:
                 yield from wait(bar("FULLOP", (c + 1) % NSH), (c + 1) // NSH)
             yield WORK
 
-    def courier():
-        armed = min(NSH, n_chunks)
-        c = 0
-        while c < armed:
+    def epilogue():   # its two signalling threads, in chunk order
+        for c in range(n_chunks):
             h, j = c % NSH, c // NSH
-            yield from wait(bar("FULLOP", h), j)                    # the push of chunk c has landed
-            bar("COPIED", h, j & 1).arrive()
+            yield from wait(bar("OREADY", c & 1), c >> 1)          # the chain has finished chunk c
             if c + NSH < n_chunks:
-                yield from wait(bar("HFREE", h), j)                 # the chain is done with chunk c
                 bar("FULLOP", h).arm()
                 bar("HSLOT", h).arrive()
-                armed += 1
-            c += 1
+            bar("COPIED", h, j & 1).arrive()
+            yield WORK                                              # the O of chunk c is read out
+            bar("OFREE", c & 1).arrive()
 
     def push(h, b, c):                            # the bulk copy, in flight for a while
         for _ in range(random.randrange(1, 4)):
@@ -162,7 +163,7 @@ def make_actors(n_chunks, wait_hslot=True):
             engines.append(push(h, b, c))
             j += 1
 
-    actors = [chain(), courier()] + [loader(h) for h in range(NH)] + [prep(h) for h in range(NH)] + \
+    actors = [chain(), epilogue()] + [loader(h) for h in range(NH)] + [prep(h) for h in range(NH)] + \
         [pusher(h) for h in range(NH)]
     return actors, engines, consumed
 
