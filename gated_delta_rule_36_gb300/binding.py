@@ -30,7 +30,7 @@ KDA_FLAG_BETA_LOGIT, KDA_FLAG_GATE_SOFTPLUS = 0x1, 0x2
 KDA_FLAG_KERNEL_MASK = 0xF00
 KDA_KERNEL_DEFAULT, KDA_KERNEL_CHUNK16, KDA_KERNEL_REGISTER_STATE, KDA_KERNEL_BF16_STATE = 0x000, 0x100, 0x200, 0x300
 KDA_KERNEL_SMEM_STATE = 0x400
-KDA_SCHEDULE_TWO_PER_SM, KDA_SCHEDULE_ONE_PER_SM, KDA_SCHEDULE_CLUSTER = 0, 1, 2
+KDA_SCHEDULE_TWO_PER_SM, KDA_SCHEDULE_ONE_PER_SM, KDA_SCHEDULE_CLUSTER, KDA_SCHEDULE_CLUSTER2 = 0, 1, 2, 3
 KDA_TRACE_POINTS = 8
 
 _DTYPE = {torch.bfloat16: KDA_BF16, torch.float32: KDA_F32, torch.int64: KDA_I64}
@@ -282,7 +282,7 @@ def kda_fwd_set_trace(buffer=None, unit: int = 0) -> None:
 
 def kda_fwd_schedule(units: int, flags: int = 0) -> int:
     """KDA_SCHEDULE_* that kda_fwd takes on the current device for ``units`` (sequence, head)
-    units: two CTAs per SM, one CTA per SM, or a cluster of four CTAs per unit."""
+    units: two CTAs per SM, one CTA per SM, or a cluster of four or of two CTAs per unit."""
     lib = load()
     sched = ctypes.c_int32(-1)
     _check(lib, lib.kda_fwd_schedule(int(units), int(flags), ctypes.byref(sched)))

@@ -2,8 +2,8 @@
 //
 // One CTA per (sequence, head) unit, two CTAs per SM; with no more units than SMs, one CTA
 // per SM (a second instantiation); with at most a quarter as many, a cluster of four CTAs
-// per unit, three of which prepare chunks for the fourth's chain (the cluster schedule,
-// below).  The fp32 V x K state stays resident in Tensor Memory for the whole sequence
+// per unit, three of which prepare chunks for the fourth's chain, and with at most half as
+// many a cluster of two, one CTA preparing for the other (the cluster schedules, below).  The fp32 V x K state stays resident in Tensor Memory for the whole sequence
 // ("FlashInfer PR #4262" notes, section 6); the recurrent GEMMs run as tcgen05.mma with
 // fp32 TMEM accumulators, and the small intra-chunk products as warp-level mma.sync
 // (section 7).
@@ -59,7 +59,8 @@ constexpr int W_ISSUE = W_INV + 1;            // the MMA warp
 // one CTA per SM the whole warp issues through elect.sync.)
 constexpr int T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
-constexpr int NSLOT = 2;
+constexpr int NSLOT = 2;     // the ring of a CTA with its own chain
+constexpr int MAX_RING = 4;  // the ring of a cluster-of-two helper
 #ifdef KDA_WAIT_TEST
 // The test-only build of the timeout path: waits give up after ~2 ms, and the inverse warp
 // skips its FULLD arrival for local chunk p.test_skip_chunk (chosen by the host), so that a
@@ -113,8 +114,8 @@ constexpr uint32_t OFF_BAR = OFF_NEGI + 2048;
 // has landed and been consumed).  OREADY b / OFREE b (cluster home): the chain has finished
 // chunk c (its O in buffer b = c % 2) / the epilogue warps have read the O out.
 enum {
-    B_FULLTMA = 0, B_FULLV = 2, B_AREADY = 5, B_FULLP = 7, B_FULLD = 9, B_LFREE = 11, B_G1, B_G2, B_G3,
-    B_FULLOP = 15, B_HSLOT = 18, B_COPIED = 19, B_OREADY = 21, B_OFREE = 23, B_COUNT = 25
+    B_FULLTMA = 0, B_FULLV = 4, B_AREADY = 7, B_FULLP = 11, B_FULLD = 15, B_LFREE = 19, B_G1, B_G2, B_G3,
+    B_FULLOP = 23, B_HSLOT = 26, B_COPIED = 29, B_OREADY = 33, B_OFREE = 35, B_COUNT = 37
 };
 constexpr uint32_t OFF_TMEMADDR = OFF_BAR + B_COUNT * 8;
 constexpr uint32_t OFF_PUSHED = OFF_TMEMADDR + 4;   // (cluster home) pushes issued by helper h, at + 4 h
@@ -125,14 +126,16 @@ static_assert(2 * (SMEM_BYTES + 1024) <= 233472, "two CTAs must fit one SM");
 static_assert(OFF_QC % 256 == 0 && OFF_KC % 256 == 0 && OFF_KI % 256 == 0, "scratch tiles must be 256-B aligned");
 static_assert(OFF_L % 16 == 0 && OFF_X % 16 == 0 && OFF_NEGI % 16 == 0, "float4 / descriptor alignment");
 
-// Cluster schedule, for few units: a cluster of 1 + NHELP CTAs per unit.  The home CTA (rank
-// 0) runs the chain over NHELP slots; helper h (rank h + 1) prepares the chunks c = h (mod
-// NHELP) in its own two slots with the prep and inverse warps and pushes each finished chunk
-// into home slot h with a shared -> distributed shared memory bulk copy.
-constexpr int NHELP = 3, CL_SIZE = NHELP + 1;
-constexpr uint32_t OFF_SLOT2 = (SMEM_USED + 1023) & ~1023u;   // the home CTA's third slot
-constexpr uint32_t SMEM_BYTES_CL = OFF_SLOT2 + SLOT_BYTES + 1024;
-static_assert(SMEM_BYTES_CL <= 232448, "the cluster layout must fit one CTA's shared memory");
+// Cluster schedules, for few units: a cluster of 1 + kNH CTAs per unit.  The home CTA (rank
+// 0) runs the chain over NSH slots; helper h (rank h + 1) prepares the chunks c = h (mod kNH)
+// in its own ring of slots with the prep and inverse warps (two slots with three helpers,
+// four with one) and pushes each finished chunk into home slot c % NSH with a shared ->
+// distributed shared memory bulk copy.
+constexpr int NSH = 3;
+__host__ __device__ constexpr int cl_ring(int nh) { return nh == 1 ? 4 : 2; }
+constexpr uint32_t OFF_SLOT2 = (SMEM_USED + 1023) & ~1023u;   // the third and fourth slots
+__host__ __device__ constexpr uint32_t smem_bytes_cl(int nh) { return OFF_SLOT2 + (nh == 1 ? 2 : 1) * SLOT_BYTES + 1024; }
+static_assert(smem_bytes_cl(1) <= 232448 && smem_bytes_cl(3) <= 232448, "the cluster layouts must fit one CTA's shared memory");
 
 // bf16 state resident in shared memory (a design alternative, one CTA per SM): the 128 x 128
 // state as GEMM1's A operand, K-major with the 128-byte swizzle, two 64-column blocks of 16 KB.
@@ -144,8 +147,8 @@ static_assert(SMEM_BYTES_SS <= 232448, "the shared-memory state layout must fit 
 // (bytes [SL_MQT, SL_BETA)); v is the home CTA's own.
 constexpr uint32_t PUSH_A = SL_V, PUSH_B = SL_BETA - SL_MQT, PUSH_BYTES = PUSH_A + PUSH_B;
 static_assert(PUSH_A % 16 == 0 && PUSH_B % 16 == 0 && SL_MQT % 16 == 0, "bulk copies move 16-byte units");
-static_assert(OFF_PUSHED + 4 * NHELP <= SMEM_USED, "the push counts live beside the TMEM address");
-__host__ __device__ constexpr uint32_t slot_off(int s) { return s < 2 ? (uint32_t)s * SLOT_BYTES : OFF_SLOT2; }
+static_assert(OFF_PUSHED + 4 * 3 <= SMEM_USED, "the push counts live beside the TMEM address");
+__host__ __device__ constexpr uint32_t slot_off(int s) { return s < 2 ? (uint32_t)s * SLOT_BYTES : OFF_SLOT2 + (uint32_t)(s - 2) * SLOT_BYTES; }
 
 // Shared -> distributed shared memory bulk copy: `bytes` (a multiple of 16) from this CTA's
 // `src` to `dst` in a peer CTA, completing its transaction bytes on the peer's mbarrier `mbar`
@@ -428,7 +431,7 @@ __device__ __forceinline__ int chunk_valid(const Unit& u, int c) {
 // q, k, g boxes of chunk c into slot s (on FULLTMA, which beta completes).
 __device__ __forceinline__ void load_qkg(const TmaMaps& maps, const Unit& u, int c, int s) {
     const int t0 = (int)KDA_CHK(u.bos + (int64_t)c * CH, u.bos, u.eos);
-    const uint32_t slot = u.base + s * SLOT_BYTES, full = bar_addr(u, B_FULLTMA + s);
+    const uint32_t slot = u.base + slot_off(s), full = bar_addr(u, B_FULLTMA + s);
     mbar_arrive_expect_tx(full, 3u * CH * HD * 2u);
     tma_load_3d(slot + SL_RAWQ, &maps.q, 0, u.h, t0, full);
     tma_load_3d(slot + SL_RAWK, &maps.k, 0, u.h, t0, full);
@@ -467,7 +470,7 @@ __device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, in
 }
 
 __device__ __forceinline__ void put_beta(const Unit& u, int s, int lane, float b) {
-    reinterpret_cast<float*>(u.gbase + s * SLOT_BYTES + SL_BETA)[lane] = b;
+    reinterpret_cast<float*>(u.gbase + slot_off(s) + SL_BETA)[lane] = b;
     mbar_arrive(bar_addr(u, B_FULLTMA + s));
 }
 
@@ -502,7 +505,7 @@ __device__ __noinline__ void mma_wind_down(int c, int nchunks) {
     }
 }
 
-// kCl: the chain of a cluster's home CTA.  Its NHELP slots receive pushed chunks (FULLOP
+// kCl: the chain of a cluster's home CTA.  Its NSH slots receive pushed chunks (FULLOP
 // stands for AREADY, FULLP and FULLD at once), it loads v alone, and once GEMM3 has read a slot
 // it signals OREADY, on which the epilogue warps also hand the slot back to its helper.
 // kSmemState: the bf16 state resident in shared memory (with kBf16State and kWarpIssue).
@@ -510,7 +513,7 @@ template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSme
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     static_assert(!kSmemState || (kBf16State && kWarpIssue && !kCl), "the shared-memory state runs one CTA per SM");
     unsigned char* st_smem = u.gbase + OFF_STATE;
-    constexpr int NS = kCl ? NHELP : NSLOT;   // slots in the ring
+    constexpr int NS = kCl ? NSH : NSLOT;   // slots in the ring
     const int w = pt >> 5, lane = pt & 31;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     const int v = pt;
@@ -743,7 +746,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 // ------------------------------------------------------------------------------
 template <bool kWarpIssue, bool kCl, bool kSmemState>
 __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
-    constexpr int NS = kCl ? NHELP : NSLOT;
+    constexpr int NS = kCl ? NSH : NSLOT;
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
     constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);                // GEMM2, and O += U Mqk^T
@@ -846,7 +849,7 @@ __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
 // ------------------------------------------------------------------------------
 // The group prepares the chunks c = c_first + kStride j, j < nloc, in its slots j % 2 (all
 // of them, or one helper's share in the cluster schedule).
-template <bool kSoftplus, int kStride>
+template <bool kSoftplus, int kStride, int kRing = NSLOT>
 __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_first, int nloc) {
     const int lane = pt & 31, pw = pt >> 5, gq = lane >> 2, tq = lane & 3;
     const int c0 = 4 * lane;
@@ -884,9 +887,9 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
 #pragma unroll 1
     for (int j = 0; j < nloc; ++j) {
         const int c = c_first + kStride * j;
-        const int s = j & 1;
-        const uint32_t kpar = (j >> 1) & 1;
-        unsigned char* gslot = u.gbase + s * SLOT_BYTES;
+        const int s = j % kRing;
+        const uint32_t kpar = (j / kRing) & 1;
+        unsigned char* gslot = u.gbase + slot_off(s);
         if (!warp_wait(bar_addr(u, B_FULLTMA + s), kpar, p.status, 128)) { prep_wind_down(j, 0, nloc); return; }
         const int64_t t0 = u.bos + (int64_t)c * CH;
         const int nvalid = (int)((u.eos - t0) < CH ? (u.eos - t0) : CH);
@@ -1116,22 +1119,23 @@ __device__ void prep_group(const FwdParams& p, const Unit& u, int pt, int c_firs
 // ------------------------------------------------------------------------------
 __device__ __forceinline__ uint16_t bf16_bits(float x) { return (uint16_t)(pack_bf16x2(x, 0.f) & 0xffffu); }
 
+template <int kRing = NSLOT>
 __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nloc) {   // nloc: as the prep group's
     const int gq = lane >> 2, tq = lane & 3;
     const int b = lane >> 4, cc = lane & 15;   // substitution: block b, column cc
     const float* Lb = reinterpret_cast<const float*>(u.gbase + OFF_L);
     float* Xb = reinterpret_cast<float*>(u.gbase + OFF_X);
 #pragma unroll
-    for (int s = 0; s < NSLOT; ++s)   // -B2[i][j] = 0 for i < 16 <= j (nothing else writes there)
-        *reinterpret_cast<uint4*>(u.gbase + s * SLOT_BYTES + SL_INV + core_at(lane >> 1, 16 + 8 * (lane & 1), 32)) =
+    for (int s = 0; s < kRing; ++s)   // -B2[i][j] = 0 for i < 16 <= j (nothing else writes there)
+        *reinterpret_cast<uint4*>(u.gbase + slot_off(s) + SL_INV + core_at(lane >> 1, 16 + 8 * (lane & 1), 32)) =
             make_uint4(0, 0, 0, 0);
 
 #pragma unroll 1
     for (int j = 0; j < nloc; ++j) {
-        const int s = j & 1;
-        const uint32_t kpar = (j >> 1) & 1;
-        unsigned char* b2s = u.gbase + s * SLOT_BYTES + SL_INV;
-        const float* bs = reinterpret_cast<const float*>(u.gbase + s * SLOT_BYTES + SL_BETA);
+        const int s = j % kRing;
+        const uint32_t kpar = (j / kRing) & 1;
+        unsigned char* b2s = u.gbase + slot_off(s) + SL_INV;
+        const float* bs = reinterpret_cast<const float*>(u.gbase + slot_off(s) + SL_BETA);
         if (!warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 128)) return;
 
         // ---- diagonal blocks: x[r] = X_bb[r][cc]
@@ -1237,9 +1241,11 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
 }
 
 // ------------------------------------------------------------------------------
-// Cluster schedule.  Chunk c is prepared by helper h = c % NHELP as its chunk j = c / NHELP,
-// in its slot j % 2, and pushed into home slot h.  Every barrier that one side completes for
-// the other has one instance per slot, so no wait can see a phase two ahead of its own.
+// Cluster schedules.  Chunk c is prepared by helper h = c % kNH as its chunk j = c / kNH, in
+// its slot j % ring (ring = 2 slots with three helpers, 4 with one), and pushed into home slot
+// c % NSH.  Every barrier that one side completes for the other has one instance per slot
+// (HSLOT: per home slot the helper pushes into), so no wait can see a phase two ahead of its
+// own.
 // ------------------------------------------------------------------------------
 
 // Once every CTA of the cluster has published its push count: wait until every push issued
@@ -1247,12 +1253,16 @@ __device__ void inverse_warp(const FwdParams& p, const Unit& u, int lane, int nl
 // home slot h were finished by the chain (their pushes landed); a push is only issued into an
 // armed slot, and a slot is armed for its next chunk only once the chain has finished the
 // one before, so at most one push a slot is left to wait for.
-__device__ void home_drain(const FwdParams& p, const Unit& u, const int (&seen)[NHELP]) {
+template <int kNH>
+__device__ void home_drain(const FwdParams& p, const Unit& u, const int (&seen)[NSH]) {
 #pragma unroll 1
-    for (int h = 0; h < NHELP; ++h) {
-        const int pushed = *reinterpret_cast<volatile int*>(u.gbase + OFF_PUSHED + 4 * h);
-        for (int j = seen[h]; j < pushed; ++j)
-            mbar_wait_bounded(bar_addr(u, B_FULLOP + h), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+    for (int hs = 0; hs < NSH; ++hs) {
+        // pushes into home slot hs: those of helper hs (three helpers), or every third of the
+        // one helper's, from its chunk hs on
+        const int n = *reinterpret_cast<volatile int*>(u.gbase + OFF_PUSHED + 4 * (kNH == 1 ? 0 : hs));
+        const int pushed = kNH == 1 ? (n > hs ? (n - hs + NSH - 1) / NSH : 0) : n;
+        for (int j = seen[hs]; j < pushed; ++j)
+            mbar_wait_bounded(bar_addr(u, B_FULLOP + hs), (uint32_t)(j & 1), p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
 }
 
@@ -1260,13 +1270,14 @@ __device__ void home_drain(const FwdParams& p, const Unit& u, const int (&seen)[
 // (OREADY, its O in buffer c % 2), read the O out, stage it in the slot's v region (GEMM1 has
 // read v) and store it (tensor stores, row copies for a tail chunk), release the buffer
 // (OFREE), then refill the region with chunk c + 3's v once the stores have read it.  This
-// takes the output off the chain's critical path.  The chunk's helper h = c % NHELP hears from
-// two single threads meanwhile: lane 0 of warp 9 arms home slot h for chunk c + NHELP (an
-// arrival and the bytes to come) and tells the helper it may push that chunk (HSLOT); lane 0
-// of warp 10 tells it that the helper slot which held chunk c may be refilled (COPIED).
-// seen[h] (lane 0 of warp 9) counts the chunks of home slot h the chain has finished.
-__device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et, int (&seen)[NHELP]) {
-    constexpr int NS = NHELP;
+// takes the output off the chain's critical path.  The helpers hear from two single threads
+// meanwhile: lane 0 of warp 9 arms home slot hs = c % NSH for chunk c + NSH (an arrival and
+// the bytes to come) and tells that chunk's helper it may push it (HSLOT); lane 0 of warp 10
+// tells chunk c's helper that the slot which held it may be refilled (COPIED).  seen[hs]
+// (lane 0 of warp 9) counts the chunks of home slot hs the chain has finished.
+template <int kNH>
+__device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et, int (&seen)[NSH]) {
+    constexpr int NS = NSH, RING = cl_ring(kNH);
     const int w = et >> 5, lane = et & 31, v = et;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     // chunks whose v boxes have been requested: the chain loads the first NS, this thread the rest
@@ -1282,15 +1293,15 @@ __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Uni
         }
         tc_fence_after();
         {
-            const int h = c % NHELP;
-            if (et == 32) {
-                ++seen[h];
-                if (c + NHELP < u.nchunks) {
-                    mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
-                    mbar_arrive_remote(mapa_shared(bar_addr(u, B_HSLOT), (uint32_t)(h + 1)));
+            const int hs = c % NS;
+            if (et == 32) {   // home slot hs takes chunk c + NS next, from helper (c + NS) % kNH
+                ++seen[hs];
+                if (c + NS < u.nchunks) {
+                    mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + hs), PUSH_BYTES);
+                    mbar_arrive_remote(mapa_shared(bar_addr(u, B_HSLOT + hs / kNH), (uint32_t)((c + NS) % kNH + 1)));
                 }
-            } else if (et == 64) {
-                mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + ((c / NHELP) & 1)), (uint32_t)(h + 1)));
+            } else if (et == 64) {   // the helper slot that held chunk c
+                mbar_arrive_remote(mapa_shared(bar_addr(u, B_COPIED + (c / kNH) % RING), (uint32_t)(c % kNH + 1)));
             }
         }
         const int nvalid = chunk_valid(u, c);
@@ -1363,19 +1374,21 @@ __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Uni
 }
 
 // Helper CTA, warps 0-3: warp 2 loads the q, k, g boxes (lane 0) and beta of the helper's
-// chunks into its two slots, the slot of chunk j once the push of chunk j - 2 has landed;
-// lane 0 of warp 3 pushes each chunk the prep and inverse warps have finished into the home
-// slot, once that is free, and at the end publishes how many pushes it issued.
-template <bool kBetaLogit>
+// chunks into its ring of kRing slots, the slot of local chunk j once chunk j - kRing, pushed
+// from it, has been consumed; lane 0 of warp 3 pushes each chunk the prep and inverse warps
+// have finished into home slot c % NSH, once that is free, and at the end publishes how many
+// pushes it issued.
+template <bool kBetaLogit, int kNH>
 __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt, int h, int nloc) {
+    constexpr int kRing = cl_ring(kNH);
     const int w = pt >> 5, lane = pt & 31;
     if (w == W_BETA) {
         int loaded = 0;
 #pragma unroll 1
         for (int j = 0; j < nloc; ++j) {
-            const int c = h + NHELP * j, b = j & 1;
-            if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait_bounded<true>(bar_addr(u, B_COPIED + b), ((j - 2) >> 1) & 1,
-                                                                            p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)))
+            const int c = h + kNH * j, b = j % kRing;
+            if (j >= kRing && !__all_sync(0xffffffffu, mbar_wait_bounded<true>(bar_addr(u, B_COPIED + b), (uint32_t)((j / kRing - 1) & 1),
+                                                                                p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)))
                 break;
             if (lane == 0) load_qkg(maps, u, c, b);
             put_beta(u, b, lane, load_beta<kBetaLogit>(p, u, c, lane));
@@ -1384,22 +1397,24 @@ __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u
         // boxes still in flight must land before the CTA exits (only after a timeout can one
         // be unconsumed)
         if (lane == 0)
-            for (int j = loaded - 2 < 0 ? 0 : loaded - 2; j < loaded; ++j)
-                mbar_wait_bounded(bar_addr(u, B_FULLTMA + (j & 1)), (j >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+            for (int j = loaded - kRing < 0 ? 0 : loaded - kRing; j < loaded; ++j)
+                mbar_wait_bounded(bar_addr(u, B_FULLTMA + j % kRing), (uint32_t)((j / kRing) & 1), p.status, KDA_DEVERR_TIMEOUT,
+                                  WAIT_LIMIT);
     } else if (pt == T_STORE) {
-        const uint32_t dst = mapa_shared(u.base + slot_off(h), 0u), full = mapa_shared(bar_addr(u, B_FULLOP + h), 0u);
         int pushed = 0;
 #pragma unroll 1
         for (int j = 0; j < nloc; ++j) {
-            const int b = j & 1;
-            const uint32_t par = (j >> 1) & 1;
+            const int c = h + kNH * j, b = j % kRing, hs = c % NSH;
+            const uint32_t par = (j / kRing) & 1;
             if (!mbar_wait_bounded(bar_addr(u, B_FULLP + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
             if (!mbar_wait_bounded(bar_addr(u, B_FULLD + b), par, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256)) break;
-            // the home slot is free (and armed for this push) from the helper's second chunk on
-            if (j > 0 && !mbar_wait_bounded<true>(bar_addr(u, B_HSLOT), (uint32_t)((j - 1) & 1), p.status,
-                                                   KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256))
+            // home slot hs is free (and armed for this push) once the chain has finished chunk
+            // c - NSH: one barrier per home slot the helper pushes into
+            if (c >= NSH && !mbar_wait_bounded<true>(bar_addr(u, B_HSLOT + hs / kNH), (uint32_t)((c / NSH - 1) & 1), p.status,
+                                                      KDA_DEVERR_TIMEOUT, WAIT_LIMIT, 256))
                 break;
-            const uint32_t src = u.base + b * SLOT_BYTES;
+            const uint32_t dst = mapa_shared(u.base + slot_off(hs), 0u), full = mapa_shared(bar_addr(u, B_FULLOP + hs), 0u);
+            const uint32_t src = u.base + slot_off(b);
             bulk_copy_to_peer(dst, src, PUSH_A, full);
             bulk_copy_to_peer(dst + SL_MQT, src + SL_MQT, PUSH_B, full);
             pushed = j + 1;
@@ -1412,8 +1427,11 @@ __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u
 // pass, and the register file to itself: up to 128 registers a thread instead of 72).
 // kCl: the cluster schedule (one CTA per SM too).
 // kSmemState: the bf16 state resident in shared memory (one CTA per SM).
-template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit, bool kCl = false, bool kSmemState = false>
+// kNH: (cluster schedules) helpers per cluster, 3 or 1.
+template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit, bool kCl = false, bool kSmemState = false,
+          int kNH = 3>
 __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
+    constexpr int CL_SIZE = kNH + 1;
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
 
@@ -1423,7 +1441,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
 #endif
     const int rank = kCl ? (int)cluster_ctarank() : 0;   // 0: the home CTA
     const bool home = rank == 0;
-    int seen[NHELP] = {0, 0, 0};   // (cluster home, lane 0 of warp 9) chunks finished per home slot
+    int seen[NSH] = {0, 0, 0};   // (cluster home, lane 0 of warp 9) chunks finished per home slot
     Unit u;
     {
         const uint32_t raw = smem_u32(smem_raw);
@@ -1437,12 +1455,12 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         u.nchunks = (int)((u.eos - u.bos + CH - 1) / CH);
     }
     if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) mbar_init(bar_addr(u, B_FULLTMA + s), 33);
+        for (int s = 0; s < MAX_RING; ++s) mbar_init(bar_addr(u, B_FULLTMA + s), 33);
         for (int b = B_FULLV; b < B_COUNT; ++b) mbar_init(bar_addr(u, b), 1);
         mbar_fence_init();
-        if (kCl && home) {   // the first NHELP home slots await their pushes
-            for (int h = 0; h < NHELP && h < u.nchunks; ++h) mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
-            for (int h = 0; h < NHELP; ++h) *reinterpret_cast<int*>(u.gbase + OFF_PUSHED + 4 * h) = 0;
+        if (kCl && home) {   // the first NSH home slots await their pushes
+            for (int h = 0; h < NSH && h < u.nchunks; ++h) mbar_arrive_expect_tx(bar_addr(u, B_FULLOP + h), PUSH_BYTES);
+            for (int h = 0; h < 3; ++h) *reinterpret_cast<int*>(u.gbase + OFF_PUSHED + 4 * h) = 0;
         }
     }
     if (tid == 32) {
@@ -1475,14 +1493,14 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     } else if (home) {
         if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
         else if (warp < W_PREP0 + 4) {}   // warps 4-7 have no part in the home CTA
-        else if (warp < W_INV) home_epilogue(p, maps, u, tid - (W_PREP0 + 4) * 32, seen);
+        else if (warp < W_INV) home_epilogue<kNH>(p, maps, u, tid - (W_PREP0 + 4) * 32, seen);
         else if (warp == W_ISSUE) mma_warp<true, true, false>(p, u, tid & 31);
     } else {
         const int h = rank - 1;
-        const int nloc = u.nchunks > h ? (u.nchunks - h + NHELP - 1) / NHELP : 0;
-        if (warp < W_PREP0) helper_io<kBetaLogit>(p, maps, u, tid, h, nloc);
-        else if (warp < W_INV) prep_group<kSoftplus, NHELP>(p, u, tid - W_PREP0 * 32, h, nloc);
-        else if (warp == W_INV) inverse_warp(p, u, tid & 31, nloc);
+        const int nloc = u.nchunks > h ? (u.nchunks - h + kNH - 1) / kNH : 0;
+        if (warp < W_PREP0) helper_io<kBetaLogit, kNH>(p, maps, u, tid, h, nloc);
+        else if (warp < W_INV) prep_group<kSoftplus, kNH, cl_ring(kNH)>(p, u, tid - W_PREP0 * 32, h, nloc);
+        else if (warp == W_INV) inverse_warp<cl_ring(kNH)>(p, u, tid & 31, nloc);
     }
 
     tc_fence_before();
@@ -1496,7 +1514,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     if constexpr (kCl) {
         cluster_sync_all();
         if (home && warp == W_PREP0 + 5) {
-            if ((tid & 31) == 0) home_drain(p, u, seen);
+            if ((tid & 31) == 0) home_drain<kNH>(p, u, seen);
             __syncwarp();   // converged at the aligned cluster barrier
         }
         cluster_sync_all();
@@ -1536,36 +1554,65 @@ bool encode_tokens_map(CUtensorMap* m, const void* ptr, int64_t T_total, int H, 
 
 using Kernel = void (*)(const FwdParams, const TmaMaps);
 
-// The cluster instantiation for the flags, with its launch configuration (the attribute
-// array must outlive the configuration's use).
-Kernel cluster_config(uint32_t flags, long long units, cudaStream_t stream, cudaLaunchAttribute* attr,
+// The cluster instantiation for the flags and helper count (3: clusters of four CTAs, 1:
+// clusters of two), with its launch configuration (the attribute array must outlive the
+// configuration's use).
+Kernel cluster_config(uint32_t flags, int nh, long long units, cudaStream_t stream, cudaLaunchAttribute* attr,
                       cudaLaunchConfig_t* cfg) {
-    static constexpr Kernel table_cl[2][2] = {   // [softplus][beta logit]
-        {kda_fwd_tc_kernel<false, true, false, false, true>, kda_fwd_tc_kernel<false, true, false, true, true>},
-        {kda_fwd_tc_kernel<false, true, true, false, true>, kda_fwd_tc_kernel<false, true, true, true, true>}};
-    const Kernel ck = table_cl[(flags & KDA_FLAG_GATE_SOFTPLUS) != 0][(flags & KDA_FLAG_BETA_LOGIT) != 0];
+    static constexpr Kernel table_cl[2][2][2] = {   // [one helper][softplus][beta logit]
+        {{kda_fwd_tc_kernel<false, true, false, false, true>, kda_fwd_tc_kernel<false, true, false, true, true>},
+         {kda_fwd_tc_kernel<false, true, true, false, true>, kda_fwd_tc_kernel<false, true, true, true, true>}},
+        {{kda_fwd_tc_kernel<false, true, false, false, true, false, 1>, kda_fwd_tc_kernel<false, true, false, true, true, false, 1>},
+         {kda_fwd_tc_kernel<false, true, true, false, true, false, 1>, kda_fwd_tc_kernel<false, true, true, true, true, false, 1>}}};
+    const Kernel ck = table_cl[nh == 1][(flags & KDA_FLAG_GATE_SOFTPLUS) != 0][(flags & KDA_FLAG_BETA_LOGIT) != 0];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CL_SIZE;
+    attr[0].val.clusterDim.x = (unsigned)(nh + 1);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     *cfg = cudaLaunchConfig_t{};
-    cfg->gridDim = dim3((unsigned)(units * CL_SIZE));
+    cfg->gridDim = dim3((unsigned)(units * (nh + 1)));
     cfg->blockDim = dim3(TC_THREADS);
-    cfg->dynamicSmemBytes = SMEM_BYTES_CL;
+    cfg->dynamicSmemBytes = smem_bytes_cl(nh);
     cfg->stream = stream;
     cfg->attrs = attr;
     cfg->numAttrs = 1;
     return ck;
 }
 
+// Whether every cluster of (nh + 1) CTAs for `units` units can be resident at once.  The count
+// is a property of the device and the instantiation: ask the runtime once (the query costs
+// more host time than a whole launch) and keep the answer.
+cudaError_t clusters_fit(int dev, uint32_t flags, int nh, long long units, bool* fit) {
+    constexpr int kMaxDev = 64;
+    static std::atomic<int> resident_cache[kMaxDev][2][4];   // zero-initialised: 0 = not asked yet
+    const int fi = (int)(flags & 3u);
+    std::atomic<int>* slot = dev < kMaxDev ? &resident_cache[dev][nh == 1][fi] : nullptr;
+    int resident = slot ? slot->load(std::memory_order_relaxed) - 1 : -1;
+    if (resident < 0) {
+        cudaLaunchAttribute attr[1];
+        cudaLaunchConfig_t cfg;
+        const Kernel ck = cluster_config(flags, nh, units, nullptr, attr, &cfg);
+        cudaError_t e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_cl(nh));
+        if (e != cudaSuccess) return e;
+        if (cudaOccupancyMaxActiveClusters(&resident, ck, &cfg) != cudaSuccess) {
+            (void)cudaGetLastError();   // no cluster schedule on this device
+            resident = 0;
+        }
+        if (slot) slot->store(resident + 1, std::memory_order_relaxed);
+    }
+    *fit = resident >= units;
+    return cudaSuccess;
+}
+
 }  // namespace
 
 size_t fwd_tc_smem_bytes() { return SMEM_BYTES; }
 
-// One CTA per unit, two on an SM, when the units outnumber the SMs; one CTA per unit with an
-// SM to itself up to one unit per SM; with at most a quarter as many units as SMs, a cluster
-// of four CTAs per unit, if every cluster can be resident at once (clusters must fit the
-// GPCs).  The bf16-state ablation keeps its one instantiation.
+// One CTA per unit, two on an SM, when the units outnumber the SMs; with at most a quarter
+// as many units as SMs, a cluster of four CTAs per unit, and with at most half as many a
+// cluster of two, if every cluster can be resident at once (clusters must fit the GPCs);
+// else one CTA per unit with an SM to itself.  The bf16-state ablation keeps its one
+// instantiation.
 cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, int* sched) {
     *sched = KDA_SCHEDULE_TWO_PER_SM;
     if (bf16_state || units <= 0) return cudaSuccess;
@@ -1575,27 +1622,16 @@ cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, in
     if (e != cudaSuccess) return e;
     if (units > sms) return cudaSuccess;
     *sched = KDA_SCHEDULE_ONE_PER_SM;
-    if (units * CL_SIZE > sms) return cudaSuccess;
-    // the resident-cluster count is a property of the device and the instantiation: ask the
-    // runtime once (the query costs more host time than a whole launch) and keep the answer
-    constexpr int kMaxDev = 64;
-    static std::atomic<int> resident_cache[kMaxDev][4];   // zero-initialised: 0 = not asked yet
-    const int fi = (int)(flags & 3u);
-    std::atomic<int>* slot = dev < kMaxDev ? &resident_cache[dev][fi] : nullptr;
-    int resident = slot ? slot->load(std::memory_order_relaxed) - 1 : -1;
-    if (resident < 0) {
-        cudaLaunchAttribute attr[1];
-        cudaLaunchConfig_t cfg;
-        const Kernel ck = cluster_config(flags, units, nullptr, attr, &cfg);
-        e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_CL);
+    for (int nh : {3, 1}) {
+        if (units * (nh + 1) > sms) continue;
+        bool fit = false;
+        e = clusters_fit(dev, flags, nh, units, &fit);
         if (e != cudaSuccess) return e;
-        if (cudaOccupancyMaxActiveClusters(&resident, ck, &cfg) != cudaSuccess) {
-            (void)cudaGetLastError();   // no cluster schedule on this device
-            resident = 0;
+        if (fit) {
+            *sched = nh == 3 ? KDA_SCHEDULE_CLUSTER : KDA_SCHEDULE_CLUSTER2;
+            break;
         }
-        if (slot) slot->store(resident + 1, std::memory_order_relaxed);
     }
-    if (resident >= units) *sched = KDA_SCHEDULE_CLUSTER;
     return cudaSuccess;
 }
 
@@ -1617,11 +1653,12 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
     int sched = KDA_SCHEDULE_TWO_PER_SM;
     cudaError_t e = fwd_tc_schedule(units, p.flags, bf16_state, &sched);
     if (e != cudaSuccess) return e;
-    if (sched == KDA_SCHEDULE_CLUSTER) {
+    if (sched == KDA_SCHEDULE_CLUSTER || sched == KDA_SCHEDULE_CLUSTER2) {
+        const int nh = sched == KDA_SCHEDULE_CLUSTER ? 3 : 1;
         cudaLaunchAttribute attr[1];
         cudaLaunchConfig_t cfg;
-        const Kernel ck = cluster_config(p.flags, units, stream, attr, &cfg);
-        e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES_CL);
+        const Kernel ck = cluster_config(p.flags, nh, units, stream, attr, &cfg);
+        e = cudaFuncSetAttribute(ck, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes_cl(nh));
         if (e != cudaSuccess) return e;
         e = cudaLaunchKernelEx(&cfg, ck, p, maps);
         return e != cudaSuccess ? e : cudaGetLastError();

@@ -169,6 +169,10 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
  *   KDA_SCHEDULE_CLUSTER     a cluster of four CTAs per unit: one runs the recurrence, three
  *                            prepare its chunks (up to a quarter as many units as SMs, when
  *                            every cluster can be resident at once)
+ *   KDA_SCHEDULE_CLUSTER2    a cluster of two CTAs per unit: one runs the recurrence, one
+ *                            prepares its chunks (up to half as many units as SMs, when the
+ *                            clusters of four do not apply and every cluster of two can be
+ *                            resident at once)
  * A unit's arithmetic is the same in every schedule: outputs and states do not depend on it.
  * Returns KDA_ERR_INVALID_ARG for units < 0, unknown flag bits, a kernel other than the
  * default or a null `schedule`, and
@@ -178,12 +182,14 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
 #define KDA_SCHEDULE_TWO_PER_SM 0
 #define KDA_SCHEDULE_ONE_PER_SM 1
 #define KDA_SCHEDULE_CLUSTER    2
+#define KDA_SCHEDULE_CLUSTER2   3
 kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule);
 
 /*
  * Chain trace, for profiling the recurrence of one unit (a profiling aid; off by default).
  * After kda_fwd_set_trace(buf, bytes, unit) with a device buffer, the forward launches of
- * this host thread that take KDA_SCHEDULE_CLUSTER record, for (sequence, head) unit `unit`
+ * this host thread that take a cluster schedule (KDA_SCHEDULE_CLUSTER or KDA_SCHEDULE_CLUSTER2)
+ * record, for (sequence, head) unit `unit`
  * (sequence * H + head), KDA_TRACE_POINTS SM clock readings (uint64, one SM's clock) per
  * chunk c < bytes / (8 * KDA_TRACE_POINTS), at buf[c * KDA_TRACE_POINTS + i]:
  *   0 the chunk's iteration starts            4 GEMM1 has completed

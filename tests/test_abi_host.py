@@ -257,7 +257,7 @@ def test_binding_constants_match_the_header():
                 "KDA_KERNEL_DEFAULT", "KDA_KERNEL_CHUNK16", "KDA_KERNEL_REGISTER_STATE", "KDA_KERNEL_BF16_STATE",
                 "KDA_KERNEL_SMEM_STATE",
                 "KDA_SCHEDULE_TWO_PER_SM",
-                "KDA_SCHEDULE_ONE_PER_SM", "KDA_SCHEDULE_CLUSTER", "KDA_TRACE_POINTS"]
+                "KDA_SCHEDULE_ONE_PER_SM", "KDA_SCHEDULE_CLUSTER", "KDA_SCHEDULE_CLUSTER2", "KDA_TRACE_POINTS"]
     for name in mirrored:
         assert name in consts, name
         assert getattr(kb, name) == consts[name], name

@@ -29,7 +29,8 @@ import random
 
 import pytest
 
-NH, NSH = 3, 3   # helpers, home slots
+NSH = 3   # home slots
+CLUSTERS = [(3, 2), (1, 4)]   # (helpers, slots a helper) of the clusters of four and of two CTAs
 
 
 class Barrier:
@@ -70,7 +71,7 @@ class Deadlock(AssertionError):
 BLOCKED, WORK = 0, 1
 
 
-def make_actors(n_chunks, wait_hslot=True):
+def make_actors(n_chunks, wait_hslot=True, nh=3, nslh=2, one_hslot=False):
     bars = {}
 
     def bar(*key):
@@ -79,7 +80,7 @@ def make_actors(n_chunks, wait_hslot=True):
         return bars[key]
 
     home = [None] * NSH                          # (state, chunk) of each home slot
-    helper = [[None, None] for _ in range(NH)]   # (state, chunk) of each helper slot
+    helper = [[None] * nslh for _ in range(nh)]  # (state, chunk) of each helper slot
     consumed = []
     engines = []
 
@@ -109,12 +110,12 @@ def make_actors(n_chunks, wait_hslot=True):
 
     def epilogue():   # its two signalling threads, in chunk order
         for c in range(n_chunks):
-            h, j = c % NSH, c // NSH
+            hs = c % NSH
             yield from wait(bar("OREADY", c & 1), c >> 1)          # the chain has finished chunk c
-            if c + NSH < n_chunks:
-                bar("FULLOP", h).arm()
-                bar("HSLOT", h).arrive()
-            bar("COPIED", h, j & 1).arrive()
+            if c + NSH < n_chunks:                                  # home slot hs takes chunk c + 3 next
+                bar("FULLOP", hs).arm()
+                bar("HSLOT", (c + NSH) % nh, 0 if one_hslot else hs // nh).arrive()
+            bar("COPIED", c % nh, (c // nh) % nslh).arrive()       # the helper slot that held chunk c
             yield WORK                                              # the O of chunk c is read out
             bar("OFREE", c & 1).arrive()
 
@@ -130,11 +131,11 @@ def make_actors(n_chunks, wait_hslot=True):
 
     def loader(h):
         j = 0
-        while h + NH * j < n_chunks:
-            c, b = h + NH * j, j & 1
-            if j >= 2:
-                yield from wait(bar("COPIED", h, b), (j - 2) >> 1)
-            assert helper[h][b] is None or helper[h][b] == ("pushed", c - 2 * NH), (c, helper[h][b])
+        while h + nh * j < n_chunks:
+            c, b = h + nh * j, j % nslh
+            if j >= nslh:
+                yield from wait(bar("COPIED", h, b), j // nslh - 1)
+            assert helper[h][b] is None or helper[h][b] == ("pushed", c - nslh * nh), (c, helper[h][b])
             helper[h][b] = ("loading", c)
             yield WORK                                              # the boxes are in flight
             helper[h][b] = ("loaded", c)
@@ -143,9 +144,9 @@ def make_actors(n_chunks, wait_hslot=True):
 
     def prep(h):   # prep group and inverse warp of helper h
         j = 0
-        while h + NH * j < n_chunks:
-            c, b = h + NH * j, j & 1
-            yield from wait(bar("FULLTMA", h, b), j >> 1)
+        while h + nh * j < n_chunks:
+            c, b = h + nh * j, j % nslh
+            yield from wait(bar("FULLTMA", h, b), j // nslh)
             assert helper[h][b] == ("loaded", c), (c, helper[h][b])
             yield WORK
             helper[h][b] = ("prepared", c)
@@ -154,24 +155,27 @@ def make_actors(n_chunks, wait_hslot=True):
 
     def pusher(h):
         j = 0
-        while h + NH * j < n_chunks:
-            c, b = h + NH * j, j & 1
-            yield from wait(bar("PREPARED", h, b), j >> 1)
-            if j > 0 and wait_hslot:
-                yield from wait(bar("HSLOT", h), j - 1)
+        while h + nh * j < n_chunks:
+            c, b = h + nh * j, j % nslh
+            yield from wait(bar("PREPARED", h, b), j // nslh)
+            if c >= NSH and wait_hslot:                             # home slot c % 3 is free for it
+                if one_hslot:
+                    yield from wait(bar("HSLOT", h, 0), (c - NSH) // nh)
+                else:
+                    yield from wait(bar("HSLOT", h, (c % NSH) // nh), c // NSH - 1)
             helper[h][b] = ("pushing", c)
             engines.append(push(h, b, c))
             j += 1
 
-    actors = [chain(), epilogue()] + [loader(h) for h in range(NH)] + [prep(h) for h in range(NH)] + \
-        [pusher(h) for h in range(NH)]
+    actors = [chain(), epilogue()] + [loader(h) for h in range(nh)] + [prep(h) for h in range(nh)] + \
+        [pusher(h) for h in range(nh)]
     return actors, engines, consumed
 
 
-def run(n_chunks, seed, wait_hslot=True):
+def run(n_chunks, seed, wait_hslot=True, nh=3, nslh=2, one_hslot=False):
     rng = random.Random(seed)
     random.seed(seed)
-    actors, engines, consumed = make_actors(n_chunks, wait_hslot)
+    actors, engines, consumed = make_actors(n_chunks, wait_hslot, nh, nslh, one_hslot)
     live = list(actors)
     idle = 0   # consecutive steps in which the chosen actor was polling a blocked wait
     while live or engines:
@@ -188,19 +192,34 @@ def run(n_chunks, seed, wait_hslot=True):
     assert consumed == list(range(n_chunks))
 
 
+@pytest.mark.parametrize("nh,nslh", CLUSTERS)
 @pytest.mark.parametrize("n_chunks", [1, 2, 3, 4, 5, 6, 7, 12, 13, 31, 64])
-def test_protocol_holds_under_random_interleavings(n_chunks):
+def test_protocol_holds_under_random_interleavings(n_chunks, nh, nslh):
     for seed in range(25):
-        run(n_chunks, seed)
+        run(n_chunks, seed, nh=nh, nslh=nslh)
 
 
-def test_pushing_without_waiting_for_the_home_slot_overwrites_it():
+@pytest.mark.parametrize("nh,nslh", CLUSTERS)
+def test_pushing_without_waiting_for_the_home_slot_overwrites_it(nh, nslh):
     """A helper that pushes its next chunk as soon as it is prepared lands it in a home slot
-    the chain has not finished with (or in a phase the courier never armed)."""
+    the chain has not finished with (or in a phase that was never armed)."""
     broken = 0
     for seed in range(20):
         try:
-            run(40, seed, wait_hslot=False)
+            run(40, seed, wait_hslot=False, nh=nh, nslh=nslh)
+        except AssertionError:
+            broken += 1
+    assert broken > 0
+
+
+def test_one_home_slot_barrier_for_a_single_helper_would_alias():
+    """With one helper, the home-slot hand-off needs one barrier per home slot: a single
+    barrier would complete once per chunk, and the pusher's parity wait could pass on the
+    wrong completion (or see one too many)."""
+    broken = 0
+    for seed in range(20):
+        try:
+            run(40, seed, nh=1, nslh=4, one_hslot=True)
         except AssertionError:
             broken += 1
     assert broken > 0

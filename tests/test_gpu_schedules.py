@@ -1,12 +1,13 @@
 """The launch schedules of the prefill kernel, and that they do not change the numbers.
 
 More (sequence, head) units than SMs run two CTAs to an SM; up to one unit per SM, one CTA
-per SM; up to a quarter as many units as SMs, a cluster of four CTAs per unit (one CTA runs
-the recurrence over state resident in its Tensor Memory, three prepare chunks for it and
-hand them over through distributed shared memory).  A unit's arithmetic is the same in each,
-so the same sequences must give bit-identical outputs and final states whichever schedule
-their launch takes.  The cluster and one-CTA-per-SM launches are also compared with the
-oracle over whole tensors, at and around the unit counts where the schedule changes.
+per SM; up to half as many units as SMs, a cluster of two CTAs per unit, and up to a quarter
+as many a cluster of four (one CTA runs the recurrence over state resident in its Tensor
+Memory, the others prepare chunks for it and push them into its shared memory).  A unit's
+arithmetic is the same in each, so the same sequences must give bit-identical outputs and
+final states whichever schedule their launch takes.  The cluster and one-CTA-per-SM launches
+are also compared with the oracle over whole tensors, at and around the unit counts where the
+schedule changes.
 """
 import pytest
 import torch
@@ -24,12 +25,17 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-def _cluster_max():
-    """The most units that still take the cluster schedule (every cluster resident at once)."""
-    u = _sms() // 4
-    while u > 0 and kb.kda_fwd_schedule(u) != kb.KDA_SCHEDULE_CLUSTER:
+def _cluster_max(kind=None, div=4):
+    """The most units that still take a cluster schedule (every cluster resident at once)."""
+    kind = kb.KDA_SCHEDULE_CLUSTER if kind is None else kind
+    u = _sms() // div
+    while u > 0 and kb.kda_fwd_schedule(u) != kind:
         u -= 1
     return u
+
+
+def _cluster2_max():
+    return _cluster_max(kb.KDA_SCHEDULE_CLUSTER2, 2)
 
 
 def _prefix(inp, nseq):
@@ -59,53 +65,58 @@ def _lens(n, seed):
 
 
 def test_schedule_thresholds():
-    sms, cmax = _sms(), _cluster_max()
-    print(f"[schedule] SMs {sms}, cluster schedule up to {cmax} units")
-    assert 1 <= cmax <= sms // 4
-    want = lambda u: (kb.KDA_SCHEDULE_CLUSTER if u <= cmax else
+    sms, cmax, cmax2 = _sms(), _cluster_max(), _cluster2_max()
+    print(f"[schedule] SMs {sms}, clusters of four up to {cmax} units, of two up to {cmax2}")
+    assert 1 <= cmax <= sms // 4 < cmax2 <= sms // 2
+    want = lambda u: (kb.KDA_SCHEDULE_CLUSTER if u <= cmax else kb.KDA_SCHEDULE_CLUSTER2 if u <= cmax2 else
                       kb.KDA_SCHEDULE_ONE_PER_SM if u <= sms else kb.KDA_SCHEDULE_TWO_PER_SM)
-    for u in sorted({1, 2, cmax, cmax + 1, sms // 4 + 1, sms - 1, sms, sms + 1, 4 * sms}):
+    for u in sorted({1, 2, cmax, cmax + 1, sms // 4 + 1, cmax2, cmax2 + 1, sms // 2 + 1, sms - 1, sms, sms + 1,
+                     4 * sms}):
         assert kb.kda_fwd_schedule(u) == want(u), u
     assert kb.kda_fwd_schedule(0) == kb.KDA_SCHEDULE_TWO_PER_SM
     for flags in (kb.KDA_FLAG_BETA_LOGIT, kb.KDA_FLAG_GATE_SOFTPLUS):
         assert kb.kda_fwd_schedule(cmax, flags) == kb.KDA_SCHEDULE_CLUSTER
+        assert kb.kda_fwd_schedule(cmax2, flags) == kb.KDA_SCHEDULE_CLUSTER2
 
 
 def test_schedules_give_identical_numbers():
-    """The first sequences of one packed input alone (the cluster schedule), with more
-    sequences (one CTA per SM), and with more again (two CTAs per SM)."""
-    H, sms, cmax = 4, _sms(), _cluster_max()
+    """The first sequences of one packed input alone (the cluster of four), with more
+    sequences (the cluster of two), more (one CTA per SM), and more again (two CTAs per SM)."""
+    H, sms, cmax, cmax2 = 4, _sms(), _cluster_max(), _cluster2_max()
     n_cl = min(6, cmax // H)
-    n_one = cmax // H + 1                        # just past the cluster schedule
+    n_cl2 = cmax // H + 1                        # just past the clusters of four
+    n_one = cmax2 // H + 1                       # just past the clusters of two
     n_two = sms // H + 1                         # past one unit per SM
     lens = _lens(n_two, 81)
     w = Workload("sched_same", 81, H=H, B=1, T=int(sum(lens)), seq_lens=lens, init_dtype=f32, final_dtype=f32)
     inp = make_inputs(w, "cpu")
     runs = {}
-    for nseq in (n_cl, n_one, n_two):
+    for nseq in (n_cl, n_cl2, n_one, n_two):
         sub = _prefix(inp, nseq)
         runs[nseq] = (kb.kda_fwd_schedule(nseq * H),) + run_gpu(sub)
-    assert [runs[n][0] for n in (n_cl, n_one, n_two)] == [kb.KDA_SCHEDULE_CLUSTER, kb.KDA_SCHEDULE_ONE_PER_SM,
-                                                          kb.KDA_SCHEDULE_TWO_PER_SM]
+    assert [runs[n][0] for n in (n_cl, n_cl2, n_one, n_two)] == [
+        kb.KDA_SCHEDULE_CLUSTER, kb.KDA_SCHEDULE_CLUSTER2, kb.KDA_SCHEDULE_ONE_PER_SM, kb.KDA_SCHEDULE_TWO_PER_SM]
     T_cl = int(sum(lens[:n_cl]))
     _, out_cl, fin_cl, bits_cl = runs[n_cl]
     assert bits_cl == 0
-    for nseq in (n_one, n_two):
+    for nseq in (n_cl2, n_one, n_two):
         _, out, fin, bits = runs[nseq]
         assert bits == 0
         torch.testing.assert_close(out[:, :T_cl].cpu(), out_cl.cpu(), rtol=0, atol=0, equal_nan=True)
         torch.testing.assert_close(fin[:n_cl].cpu(), fin_cl.cpu(), rtol=0, atol=0)
 
 
-@pytest.mark.parametrize("units_kind", ["cluster_max", "one_per_sm_min", "one_per_sm"])
+@pytest.mark.parametrize("units_kind", ["cluster_max", "cluster2_min", "cluster2_max", "one_per_sm_min", "one_per_sm"])
 def test_schedule_against_oracle(units_kind):
-    H, cmax = 1, _cluster_max()
-    nseq = {"cluster_max": cmax, "one_per_sm_min": cmax + 1, "one_per_sm": 100}[units_kind]
+    H, cmax, cmax2 = 1, _cluster_max(), _cluster2_max()
+    nseq = {"cluster_max": cmax, "cluster2_min": cmax + 1, "cluster2_max": cmax2, "one_per_sm_min": cmax2 + 1,
+            "one_per_sm": 100}[units_kind]
     lens = _lens(nseq, 82)
     w = Workload("sched_" + units_kind, 82, H=H, B=1, T=int(sum(lens)), seq_lens=lens, init_dtype=bf16,
                  final_dtype=f32)
     inp = make_inputs(w, "cpu")
-    want = kb.KDA_SCHEDULE_CLUSTER if units_kind == "cluster_max" else kb.KDA_SCHEDULE_ONE_PER_SM
+    want = {"cluster_max": kb.KDA_SCHEDULE_CLUSTER, "cluster2_min": kb.KDA_SCHEDULE_CLUSTER2,
+            "cluster2_max": kb.KDA_SCHEDULE_CLUSTER2}.get(units_kind, kb.KDA_SCHEDULE_ONE_PER_SM)
     assert kb.kda_fwd_schedule(w.units) == want
     out, final, bits = run_gpu(inp)
     assert bits == 0
@@ -113,13 +124,16 @@ def test_schedule_against_oracle(units_kind):
     check_full(inp, out, final, ref_out, ref_final)
 
 
-def test_cluster_schedule_long_sequences_and_variants():
-    """One long sequence per head (many rounds of the three-slot ring), every flag."""
+@pytest.mark.parametrize("kind", ["four", "two"])
+def test_cluster_schedule_long_sequences_and_variants(kind):
+    """One long sequence per head (many rounds of the home's three slots and of the helpers'
+    rings), every flag, in clusters of four and of two."""
     from oracle import kda_oracle as O
     from kda_testutil import assert_close
-    w = Workload("sched_long", 83, H=3, B=1, T=1000, seq_lens=[1000], init_dtype=f32, final_dtype=f32)
+    H = 3 if kind == "four" else _cluster_max() + 2
+    w = Workload("sched_long", 83, H=H, B=1, T=1000, seq_lens=[1000], init_dtype=f32, final_dtype=f32)
     inp = make_inputs(w, "cpu")
-    assert kb.kda_fwd_schedule(w.units) == kb.KDA_SCHEDULE_CLUSTER
+    assert kb.kda_fwd_schedule(w.units) == (kb.KDA_SCHEDULE_CLUSTER if kind == "four" else kb.KDA_SCHEDULE_CLUSTER2)
     for kflag, oflag in ((0, 0), (kb.KDA_FLAG_BETA_LOGIT | kb.KDA_FLAG_GATE_SOFTPLUS, O.BETA_LOGIT | O.GATE_SOFTPLUS)):
         ref_out, ref_final = O.kda_oracle_fwd(inp.q, inp.k, inp.v, inp.g, inp.beta, inp.scale, inp.A_log,
                                               inp.dt_bias, inp.lower_bound, initial_state=inp.initial_state,
