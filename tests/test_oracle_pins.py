@@ -245,7 +245,7 @@ def test_handworked_single_token():
         gold = json.load(f)
     for c in gold["cases"]:
         u = dict(q=np.array([c["q"]]), k=np.array([c["k"]]), v=np.array([c["v"]]),
-                 g=np.array([c["g"]]), beta=np.array([c["beta"]]), A_log=0.0,
+                 g=np.array([c["g"]]), beta=np.array([c["beta"]]), A_log=c.get("A_log", 0.0),
                  dt_bias=np.array(c["dt_bias"]), lb=c["lower_bound"], S0=np.eye(2), scale=1.0)
         out, fin = oracle_unit(u)
         # eps = 1e-6 in the L2 norm perturbs the exact values by ~1e-7 relative.
