@@ -18,7 +18,7 @@
 // The prep warps build Q_d, K_d, K_r, Mqk and L for a chunk (mma.sync for the 32 x 32
 // products) and the inverse warp turns L into -B2, while the chain runs the previous one.
 //
-// Warp roles (448 threads, up to 72 registers each):
+// Warp roles (448 threads, up to 72 registers each, with two CTAs per SM):
 //   warps 0-3   chain group: thread v owns state row v (TMEM lane v): initial/final
 //               state I/O, the bf16 copy of S, the decay, R' and the chunk output O.
 //               Single threads of its warps issue the TMA loads of q, k, g and beta
@@ -31,6 +31,9 @@
 //   warp 13     MMA warp: issues the chain's tensor-core MMAs as the chain hands each A
 //               operand over (named barriers, arrive / sync), GEMM1's first half of k while
 //               the chain still converts the second half of S.
+//   warps 14-17 (one CTA per SM only, 576 threads) epilogue warps: read each chunk's O out of
+//               a double-buffered pair of TMEM column groups, stage and store it, and refill
+//               the slot's v, so that the output leaves the chain's path (as in the cluster home).
 // A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
 // consumer (section 4): the chain refills a slot as soon as GEMM3 has read it, and
 // every mbarrier wait is bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
@@ -53,6 +56,7 @@ constexpr int TC_THREADS = 448;
 constexpr int W_PREP0 = 4, PREP_WARPS = 8;
 constexpr int W_INV = W_PREP0 + PREP_WARPS;   // the inverse warp: (I + L)^-1 of chunk c while the prep warps take c + 1
 constexpr int W_ISSUE = W_INV + 1;            // the MMA warp
+constexpr int TC_THREADS_LE = 576;            // one CTA per SM: warps 14-17 read the output out
 // Duties of the chain group, spread over its warps (one per SM sub-partition): warp 2
 // refills q, k, g and beta, warp 3 stores each output tile and then refills v, whose slot
 // region held the tile.  (With two CTAs on an SM lane 0 of the MMA warp issues alone; with
@@ -479,7 +483,7 @@ __device__ __forceinline__ void put_beta(const Unit& u, int s, int lane, float b
 // staging (not in the cluster home, whose epilogue warps stage the output).  A wound-down
 // warp syncs on the hand-offs instead of arriving: with no waits in between, plain arrivals
 // could reach the next generation of a barrier before the MMA warp has met the current one.
-template <bool kCl = false>
+template <bool kEpi = false>
 __device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
     for (; c < nchunks; ++c, k = 0)
         for (; k < 4; ++k) {
@@ -490,7 +494,7 @@ __device__ __noinline__ void chain_wind_down(int c, int k, int nchunks) {
                 named_bar_sync(NB_G2, NB_HAND);
             } else if (k == 2) {
                 named_bar_sync(NB_G3, NB_HAND);
-            } else if (!kCl) {
+            } else if (!kEpi) {
                 named_bar_sync(2, 128);
             }
         }
@@ -509,7 +513,9 @@ __device__ __noinline__ void mma_wind_down(int c, int nchunks) {
 // stands for AREADY, FULLP and FULLD at once), it loads v alone, and once GEMM3 has read a slot
 // it signals OREADY, on which the epilogue warps also hand the slot back to its helper.
 // kSmemState: the bf16 state resident in shared memory (with kBf16State and kWarpIssue).
-template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSmemState = false>
+// kEpi: epilogue warps of the CTA read the output out (the cluster home, or one CTA per SM
+// with epilogue warps): O is double-buffered and the chain only signals OREADY.
+template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSmemState = false, bool kEpi = kCl>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     static_assert(!kSmemState || (kBf16State && kWarpIssue && !kCl), "the shared-memory state runs one CTA per SM");
     unsigned char* st_smem = u.gbase + OFF_STATE;
@@ -564,7 +570,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     };
     bool ok = warp_wait(bar_addr(u, kCl ? B_FULLOP : B_AREADY), 0, p.status, 256);   // a of chunk 0
     if (ok) state_pass(reinterpret_cast<const float*>(u.gbase + SL_A));
-    else chain_wind_down<kCl>(0, 0, u.nchunks);
+    else chain_wind_down<kEpi>(0, 0, u.nchunks);
 
     int sc = 0, kq = 0;   // (cluster home) slot c % NS and round c / NS
     // chain trace (cluster schedule): SM clock at KDA_TRACE_POINTS steps of each chunk of one unit
@@ -579,7 +585,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const uint32_t cpar = c & 1, kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
         const uint32_t soff = kCl ? slot_off(s) : s * SLOT_BYTES;
         const uint32_t slot = u.base + soff;
-        const uint32_t tO = TM_O + (kCl ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
+        const uint32_t tO = TM_O + (kEpi ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
         const bool refill = c + NS < u.nchunks;
         float beta_next = 0.f;
         if constexpr (!kCl) {
@@ -591,13 +597,13 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
         // (the wait spans GEMM1, and the prep of the chunk when that runs late)
-        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status, 64)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
+        if (!warp_wait(bar_addr(u, B_G1), cpar, p.status, 64)) { chain_wind_down<kEpi>(c, 1, u.nchunks); break; }
         tc_fence_after();
         if (kCl && pt == 0) stamp(c, 4);
         p_cols_to_bf16(lane_addr, tP);
         if (kCl && pt == 0) stamp(c, 5);
         if constexpr (!kCl) {
-            if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) { chain_wind_down<kCl>(c, 1, u.nchunks); break; }
+            if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) { chain_wind_down<kEpi>(c, 1, u.nchunks); break; }
             if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
         }
         tc_fence_before();
@@ -605,22 +611,23 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (kCl && pt == 0) stamp(c, 6);
 
         // U -> bf16 -> TMEM: A operand of GEMM3
-        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down<kCl>(c, 2, u.nchunks); break; }
+        if (!warp_wait(bar_addr(u, B_G2), cpar, p.status)) { chain_wind_down<kEpi>(c, 2, u.nchunks); break; }
         tc_fence_after();
         p_cols_to_bf16(lane_addr, tP);
         tc_fence_before();
         named_bar_arrive(NB_G3, NB_HAND);
-        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down<kCl>(c, 3, u.nchunks); break; }
+        if (!warp_wait(bar_addr(u, B_G3), cpar, p.status)) { chain_wind_down<kEpi>(c, 3, u.nchunks); break; }
         tc_fence_after();
 
-        if constexpr (kCl) {
-            // the slot's pushed operands have been read for the last time, and this chunk's O is
-            // final: the epilogue warps take it from here
+        if constexpr (kEpi) {
+            // this chunk's O is final (and a cluster home's pushed operands have been read for
+            // the last time): the epilogue warps take it from here
             if (pt == 0) {
                 tc_fence_before();
                 mbar_arrive(bar_addr(u, B_OREADY + (c & 1)));
             }
-        } else {
+        }
+        if constexpr (!kCl) {
             // The slot's q, k, g regions have been read for the last time: refill them with
             // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
             if (refill) {
@@ -634,7 +641,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         // layout (two [32][64] blocks, 128-byte swizzle): the 16x256b TMEM load gives each
         // thread two adjacent tokens of one state row, and stmatrix.trans writes 8 tokens x
         // 8 rows per matrix as 16-byte rows, conflict-free under the swizzle.
-        if constexpr (!kCl) {   // (the cluster home's epilogue warps do this part for it)
+        if constexpr (!kEpi) {   // (epilogue warps, where the CTA has them, do this part for it)
         const bool full = chunk_valid(u, c) == CH;
         if (full) {
             const uint32_t tile = slot + SL_V;
@@ -697,14 +704,14 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
             if constexpr (kCl) {
-                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down<kCl>(c + 1, 0, u.nchunks); break; }
+                if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down<kEpi>(c + 1, 0, u.nchunks); break; }
             } else {
-                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down<kCl>(c + 1, 0, u.nchunks); break; }
+                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down<kEpi>(c + 1, 0, u.nchunks); break; }
             }
             state_pass(reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A));
             // the output store has had the state pass to read the staging tile: the region
             // takes chunk c + 2's v
-            if (!kCl && pt == T_STORE && refill) {
+            if (!kEpi && pt == T_STORE && refill) {
                 bulk_wait_read_all();
                 load_v(maps, u, c + NS, s);
                 vissued = c + NS + 1;
@@ -731,7 +738,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         for (int c = issued - NSLOT < 0 ? 0 : issued - NSLOT; c < issued; ++c)
             mbar_wait_bounded(bar_addr(u, B_FULLTMA + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
-    if (!kCl && pt == T_STORE) {
+    if (!kEpi && pt == T_STORE) {
         // likewise the v boxes: the last NS requested (phases before them have completed)
         for (int c = vissued - NSLOT < 0 ? 0 : vissued - NSLOT; c < vissued; ++c)
             mbar_wait_bounded(bar_addr(u, B_FULLV + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
@@ -744,7 +751,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 // commits each GEMM to its mbarrier (G1, G2, G3).  GEMM1's k blocks 0-3 go out while the chain
 // still converts and decays the second half of S.
 // ------------------------------------------------------------------------------
-template <bool kWarpIssue, bool kCl, bool kSmemState>
+template <bool kWarpIssue, bool kCl, bool kSmemState, bool kEpi = kCl>
 __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
     constexpr int NS = kCl ? NSH : NSLOT;
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
@@ -774,14 +781,14 @@ __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
         const int s = kCl ? sc : (c & 1);
         const uint32_t kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
         const uint32_t slot = u.base + (kCl ? slot_off(s) : s * SLOT_BYTES);
-        const uint32_t tO = TM_O + (kCl ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
+        const uint32_t tO = TM_O + (kEpi ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
         // the chunk's operands (the cluster home's chain waited for the pushed chunk before its
         // state pass) and its v box; (cluster home) the epilogue warps have read out chunk c - 2's
         // O from this buffer
         stamp(c, 1);
         bool ok = kCl || warp_wait(bar_addr(u, B_FULLP + s), kpar, p.status, 256);
         ok = ok && warp_wait(bar_addr(u, B_FULLV + s), kpar, p.status, 256);
-        if (kCl && c >= 2) ok = ok && warp_wait(bar_addr(u, B_OFREE + (c & 1)), (uint32_t)(((c >> 1) + 1) & 1), p.status, 256);
+        if (kEpi && c >= 2) ok = ok && warp_wait(bar_addr(u, B_OFREE + (c & 1)), (uint32_t)(((c >> 1) + 1) & 1), p.status, 256);
         if (!ok) {
             mma_wind_down(c, u.nchunks);
             break;
@@ -1277,7 +1284,8 @@ __device__ void home_drain(const FwdParams& p, const Unit& u, const int (&seen)[
 // (lane 0 of warp 9) counts the chunks of home slot hs the chain has finished.
 template <int kNH>
 __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et, int (&seen)[NSH]) {
-    constexpr int NS = NSH, RING = cl_ring(kNH);
+    // kNH == 0: a CTA with its own prep (one per SM) and two slots, no helpers to signal
+    constexpr int NS = kNH ? NSH : NSLOT, RING = cl_ring(kNH);
     const int w = et >> 5, lane = et & 31, v = et;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     // chunks whose v boxes have been requested: the chain loads the first NS, this thread the rest
@@ -1292,7 +1300,7 @@ __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Uni
             break;
         }
         tc_fence_after();
-        {
+        if constexpr (kNH > 0) {
             const int hs = c % NS;
             if (et == 32) {   // home slot hs takes chunk c + NS next, from helper (c + NS) % kNH
                 ++seen[hs];
@@ -1430,8 +1438,11 @@ __device__ void helper_io(const FwdParams& p, const TmaMaps& maps, const Unit& u
 // kNH: (cluster schedules) helpers per cluster, 3 or 1.
 template <bool kBf16State, bool kWarpIssue, bool kSoftplus, bool kBetaLogit, bool kCl = false, bool kSmemState = false,
           int kNH = 3>
-__global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
+__global__ void __launch_bounds__((kWarpIssue && !kCl && !kSmemState) ? TC_THREADS_LE : TC_THREADS, kWarpIssue ? 1 : 2)
+    kda_fwd_tc_kernel(const FwdParams p, const __grid_constant__ TmaMaps maps) {
     constexpr int CL_SIZE = kNH + 1;
+    // one CTA per SM: four more warps (14-17) read the output out
+    constexpr bool kLoneEpi = kWarpIssue && !kCl && !kSmemState;
     extern __shared__ unsigned char smem_raw[];
     if (*reinterpret_cast<volatile uint32_t*>(p.status) & KDA_DEVERR_CU_SEQLENS) return;
 
@@ -1471,7 +1482,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
         tma_prefetch_desc(&maps.out);
     }
     if (warp == 0 && home) {
-        tmem_alloc(u.base + OFF_TMEMADDR, kCl ? TM_COLS_CL : TM_COLS);
+        tmem_alloc(u.base + OFF_TMEMADDR, (kCl || kLoneEpi) ? TM_COLS_CL : TM_COLS);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -1482,13 +1493,15 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
 
     if constexpr (!kCl) {
         if (warp < W_PREP0) {
-            chain_group<kBf16State, kWarpIssue, kBetaLogit, false, kSmemState>(p, maps, u, tid);
+            chain_group<kBf16State, kWarpIssue, kBetaLogit, false, kSmemState, kLoneEpi>(p, maps, u, tid);
         } else if (warp < W_INV) {
             prep_group<kSoftplus, 1>(p, u, tid - W_PREP0 * 32, 0, u.nchunks);
         } else if (warp == W_INV) {
             inverse_warp(p, u, tid & 31, u.nchunks);
-        } else {
-            mma_warp<kWarpIssue, false, kSmemState>(p, u, tid & 31);
+        } else if (warp == W_ISSUE) {
+            mma_warp<kWarpIssue, false, kSmemState, kLoneEpi>(p, u, tid & 31);
+        } else if (kLoneEpi) {
+            home_epilogue<0>(p, maps, u, tid & 127, seen);   // warps 14-17: TMEM lanes 32 (warp % 4) ..
         }
     } else if (home) {
         if (warp < W_PREP0) chain_group<false, true, kBetaLogit, true>(p, maps, u, tid);
@@ -1507,7 +1520,7 @@ __global__ void __launch_bounds__(TC_THREADS, kWarpIssue ? 1 : 2) kda_fwd_tc_ker
     __syncthreads();
     if (warp == 0 && home) {
         tc_fence_after();
-        tmem_dealloc(u.tmem, kCl ? TM_COLS_CL : TM_COLS);
+        tmem_dealloc(u.tmem, (kCl || kLoneEpi) ? TM_COLS_CL : TM_COLS);
     }
     // no CTA leaves while a peer may still read its shared memory, write it or arrive on its
     // barriers: every CTA has published its push count; the home waits for the pushes in flight
@@ -1675,7 +1688,7 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
     auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false, false, false> : table[lone][sp][lg];
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kernel<<<units, TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
+    kernel<<<units, (lone && !bf16_state) ? TC_THREADS_LE : TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
     return cudaGetLastError();
 }
 

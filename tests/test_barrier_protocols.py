@@ -458,13 +458,16 @@ class RingRun:
     index, "withhold" | "late"); `limit` = polls before a wait may expire; `wind_down` = the
     kernel's wind-down after an expired wait (False: the earlier form, which just leaves);
     `sync_handoffs` = a wound-down chain warp syncs on the hand-off barriers (False: it only
-    arrives, as on the fast path)."""
+    arrives, as on the fast path); `epi` = the one-CTA-per-SM instantiation, whose four
+    epilogue warps read each chunk's O out (OREADY from the chain, OFREE back to the MMA warp
+    for the chunk two later), stage and store it and refill the slot's v."""
 
-    def __init__(self, n, seed, perturb=None, limit=40, wind_down=True, sync_handoffs=True):
+    def __init__(self, n, seed, perturb=None, limit=40, wind_down=True, sync_handoffs=True, epi=False):
         self.n, self.rng, self.perturb, self.limit, self.wind_down = n, random.Random(seed), perturb, limit, wind_down
-        self.sync_handoffs = sync_handoffs
+        self.sync_handoffs, self.epi = sync_handoffs, epi
         self.bars, self.engines, self.timeouts, self.consumed = {}, [], 0, []
-        self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(14)
+        self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(18 if epi else 14)
+        self.epi_bar = NamedBar(4)
         self.hand = {k: HandBar(5, k) for k in HANDOFFS}   # 4 chain warps + the MMA warp
         self.fulltma_fill = {0: 0, 1: 0}
         self.exited = 0
@@ -540,7 +543,7 @@ class RingRun:
                         yield from self.hand[name].sync(w)
                     else:
                         self.hand[name].arrive(w)
-                if k == 3:
+                if k == 3 and not self.epi:
                     yield from self.chain_bar.sync()
                 k += 1
             c, k = c + 1, 0
@@ -603,7 +606,11 @@ class RingRun:
                 if refill and w == 2:
                     self.load_qkg(c + 2)
                     issued_qkg = c + 3
-                yield from self.chain_bar.sync()          # the output staging
+                if self.epi:
+                    if w == 0:                            # the epilogue warps take the output
+                        self.arrive("OREADY", c >> 1, c & 1)
+                else:
+                    yield from self.chain_bar.sync()      # the output staging
                 if w == 0:
                     self.consumed.append(c)
                 if c + 1 < n:
@@ -614,16 +621,37 @@ class RingRun:
                     self.hand_off(w, "G1A")
                     yield WORK
                     self.hand_off(w, "G1B")
-                    if w == 3 and refill:
+                    if w == 3 and refill and not self.epi:
                         self.engine("FULLV", (c + 2) >> 1, s)
                         issued_v = c + 3
             # boxes still in flight must land before the CTA exits (bounded waits)
             if w == 2:
                 for c in range(max(0, issued_qkg - 2), issued_qkg):
                     yield from self.bwait(self.bar("FULLTMA", c & 1), c >> 1)
-            if w == 3:
+            if w == 3 and not self.epi:
                 for c in range(max(0, issued_v - 2), issued_v):
                     yield from self.bwait(self.bar("FULLV", c & 1), c >> 1)
+        yield from self.cta_bar.sync()
+        self.exited += 1
+
+    def epi_warp(self, ew):
+        n, vissued = self.n, min(self.n, 2)
+        for c in range(n):
+            if not (yield from self.bwait(self.bar("OREADY", c & 1), c >> 1)):
+                if self.wind_down:                        # the epilogue group's barriers still ahead
+                    for _ in range(c, n):
+                        yield from self.epi_bar.sync()
+                break
+            yield WORK                                    # O read out and staged
+            yield from self.epi_bar.sync()
+            if ew == 0:
+                self.arrive("OFREE", c >> 1, c & 1)
+                if c + 2 < n:                             # the stores have read the tile: next v
+                    self.engine("FULLV", (c + 2) >> 1, c & 1)
+                    vissued = c + 3
+        if ew == 0:
+            for c in range(max(0, vissued - 2), vissued):
+                yield from self.bwait(self.bar("FULLV", c & 1), c >> 1)
         yield from self.cta_bar.sync()
         self.exited += 1
 
@@ -633,6 +661,8 @@ class RingRun:
             s, k = c & 1, c >> 1
             ok = yield from self.bwait(self.bar("FULLP", s), k)
             ok = ok and (yield from self.bwait(self.bar("FULLV", s), k))
+            if self.epi and c >= 2:                       # the O buffer of chunk c - 2 is read out
+                ok = ok and (yield from self.bwait(self.bar("OFREE", s), k - 1))
             if not ok:
                 yield from self.mma_wind_down(c)
                 break
@@ -684,7 +714,7 @@ class RingRun:
 
     def run(self):
         live = [self.chain_warp(w) for w in range(4)] + [self.prep_warp(p) for p in range(8)] + \
-            [self.inverse_warp(), self.mma_warp()]
+            [self.inverse_warp(), self.mma_warp()] + ([self.epi_warp(e) for e in range(4)] if self.epi else [])
         state = {id(a): WORK for a in live}
         while live or self.engines:
             live += self.engines
@@ -700,19 +730,21 @@ class RingRun:
                 state[id(a)] = next(a)
             except StopIteration:
                 live.remove(a)
-        assert self.exited == 14
+        assert self.exited == (18 if self.epi else 14)
         assert all(h.arrived == 0 for h in self.hand.values()), "a hand-off generation left incomplete"
         return self
 
 
 PERTURB = [("FULLD", 1), ("FULLP", 2), ("AREADY", 1), ("LFREE", 2), ("G1", 3), ("G2", 0), ("G3", 4),
            ("FULLV", 1), ("FULLTMA", 3), ("AREADY", 0), ("FULLTMA", 0)]
+PERTURB_EPI = PERTURB + [("OREADY", 1), ("OFREE", 0), ("OREADY", 0), ("OFREE", 1)]
 
 
+@pytest.mark.parametrize("epi", [False, True])
 @pytest.mark.parametrize("n", [1, 2, 3, 9])
-def test_ring_model_without_faults_finishes_every_chunk(n):
+def test_ring_model_without_faults_finishes_every_chunk(n, epi):
     for seed in range(10):
-        r = RingRun(n, seed, limit=10 ** 9).run()
+        r = RingRun(n, seed, limit=10 ** 9, epi=epi).run()
         assert r.timeouts == 0 and r.consumed == list(range(n))
 
 
@@ -724,6 +756,18 @@ def test_every_warp_winds_down_after_an_expired_wait(name, index, mode):
     for n in (6, 10):
         for seed in range(30):
             r = RingRun(n, seed, perturb=(name, index, mode)).run()
+            if mode == "withhold":
+                assert r.timeouts > 0
+
+
+@pytest.mark.parametrize("mode", ["withhold", "late"])
+@pytest.mark.parametrize("name,index", PERTURB_EPI)
+def test_every_warp_winds_down_with_epilogue_warps(name, index, mode):
+    """The same with the one-CTA-per-SM instantiation's epilogue warps (OREADY, OFREE, and v
+    refilled by the epilogue)."""
+    for n in (6, 10):
+        for seed in range(30):
+            r = RingRun(n, seed, perturb=(name, index, mode), epi=True).run()
             if mode == "withhold":
                 assert r.timeouts > 0
 
