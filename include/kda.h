@@ -170,7 +170,7 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
  *                            prepare its chunks (up to a quarter as many units as SMs, when
  *                            every cluster can be resident at once)
  *   KDA_SCHEDULE_CLUSTER2    a cluster of two CTAs per unit: one runs the recurrence, one
- *                            prepares its chunks (up to half as many units as SMs, when the
+ *                            prepares its chunks (up to 2/7 as many units as SMs, when the
  *                            clusters of four do not apply and every cluster of two can be
  *                            resident at once)
  * A unit's arithmetic is the same in every schedule: outputs and states do not depend on it.

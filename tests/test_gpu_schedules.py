@@ -1,7 +1,7 @@
 """The launch schedules of the prefill kernel, and that they do not change the numbers.
 
 More (sequence, head) units than SMs run two CTAs to an SM; up to one unit per SM, one CTA
-per SM; up to half as many units as SMs, a cluster of two CTAs per unit, and up to a quarter
+per SM; up to 2/7 as many units as SMs, a cluster of two CTAs per unit, and up to a quarter
 as many a cluster of four (one CTA runs the recurrence over state resident in its Tensor
 Memory, the others prepare chunks for it and push them into its shared memory).  A unit's
 arithmetic is the same in each, so the same sequences must give bit-identical outputs and
@@ -35,7 +35,7 @@ def _cluster_max(kind=None, div=4):
 
 
 def _cluster2_max():
-    return _cluster_max(kb.KDA_SCHEDULE_CLUSTER2, 2)
+    return _cluster_max(kb.KDA_SCHEDULE_CLUSTER2, 3)
 
 
 def _prefix(inp, nseq):
@@ -67,11 +67,11 @@ def _lens(n, seed):
 def test_schedule_thresholds():
     sms, cmax, cmax2 = _sms(), _cluster_max(), _cluster2_max()
     print(f"[schedule] SMs {sms}, clusters of four up to {cmax} units, of two up to {cmax2}")
-    assert 1 <= cmax <= sms // 4 < cmax2 <= sms // 2
+    assert 1 <= cmax <= sms // 4 < cmax2 <= 2 * sms // 7
     want = lambda u: (kb.KDA_SCHEDULE_CLUSTER if u <= cmax else kb.KDA_SCHEDULE_CLUSTER2 if u <= cmax2 else
                       kb.KDA_SCHEDULE_ONE_PER_SM if u <= sms else kb.KDA_SCHEDULE_TWO_PER_SM)
-    for u in sorted({1, 2, cmax, cmax + 1, sms // 4 + 1, cmax2, cmax2 + 1, sms // 2 + 1, sms - 1, sms, sms + 1,
-                     4 * sms}):
+    for u in sorted({1, 2, cmax, cmax + 1, sms // 4 + 1, cmax2, cmax2 + 1, sms // 2, sms // 2 + 1, sms - 1, sms,
+                     sms + 1, 4 * sms}):
         assert kb.kda_fwd_schedule(u) == want(u), u
     assert kb.kda_fwd_schedule(0) == kb.KDA_SCHEDULE_TWO_PER_SM
     for flags in (kb.KDA_FLAG_BETA_LOGIT, kb.KDA_FLAG_GATE_SOFTPLUS):
