@@ -34,8 +34,9 @@
 //   warps 14-17 (one CTA per SM only, 576 threads) epilogue warps: read each chunk's O out of
 //               a double-buffered pair of TMEM column groups, stage and store it, and refill
 //               the slot's v, so that the output leaves the chain's path (as in the cluster home).
-// A two-slot SMEM ring carries prepared chunks to the strictly ordered recurrent
-// consumer (section 4): the chain refills a slot as soon as GEMM3 has read it, and
+// A two-slot SMEM ring (three slots with one CTA per SM, whose shared memory has room)
+// carries prepared chunks to the strictly ordered recurrent consumer (section 4): the
+// chain refills a slot as soon as GEMM3 has read it, and
 // every mbarrier wait is bounded (on expiry: KDA_DEVERR_TIMEOUT and the CTA winds down).
 //
 // TMEM columns (256 per CTA): [0,128) fp32 S; [128,160) O; [160,192) P;
@@ -63,7 +64,8 @@ constexpr int TC_THREADS_LE = 576;            // one CTA per SM: warps 14-17 rea
 // one CTA per SM the whole warp issues through elect.sync.)
 constexpr int T_TMA = 64, W_BETA = 2, T_STORE = 96;
 constexpr int PREP_THREADS = PREP_WARPS * 32;
-constexpr int NSLOT = 2;     // the ring of a CTA with its own chain
+constexpr int NSLOT = 2;     // the ring of a CTA with its own chain (two CTAs per SM)
+constexpr int NSL1 = 3;      // the ring of one CTA per SM: chunk c in slot c % 3
 constexpr int MAX_RING = 4;  // the ring of a cluster-of-two helper
 #ifdef KDA_WAIT_TEST
 // The test-only build of the timeout path: waits give up after ~2 ms, and the inverse warp
@@ -140,6 +142,8 @@ __host__ __device__ constexpr int cl_ring(int nh) { return nh == 1 ? 4 : 2; }
 constexpr uint32_t OFF_SLOT2 = (SMEM_USED + 1023) & ~1023u;   // the third and fourth slots
 __host__ __device__ constexpr uint32_t smem_bytes_cl(int nh) { return OFF_SLOT2 + (nh == 1 ? 2 : 1) * SLOT_BYTES + 1024; }
 static_assert(smem_bytes_cl(1) <= 232448 && smem_bytes_cl(3) <= 232448, "the cluster layouts must fit one CTA's shared memory");
+// One CTA per SM with its own prep: the same three slots (slot 2 past the scratch).
+constexpr uint32_t SMEM_BYTES_LE = smem_bytes_cl(3);
 
 // bf16 state resident in shared memory (a design alternative, one CTA per SM): the 128 x 128
 // state as GEMM1's A operand, K-major with the 128-byte swizzle, two 64-column blocks of 16 KB.
@@ -515,11 +519,15 @@ __device__ __noinline__ void mma_wind_down(int c, int nchunks) {
 // kSmemState: the bf16 state resident in shared memory (with kBf16State and kWarpIssue).
 // kEpi: epilogue warps of the CTA read the output out (the cluster home, or one CTA per SM
 // with epilogue warps): O is double-buffered and the chain only signals OREADY.
-template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSmemState = false, bool kEpi = kCl>
+// kR3: one CTA per SM with its own prep: a ring of three slots, chunk c in slot c % 3.
+template <bool kBf16State, bool kWarpIssue, bool kBetaLogit, bool kCl, bool kSmemState = false, bool kEpi = kCl,
+          bool kR3 = false>
 __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit& u, int pt) {
     static_assert(!kSmemState || (kBf16State && kWarpIssue && !kCl), "the shared-memory state runs one CTA per SM");
+    static_assert(!kR3 || (kEpi && !kCl), "the three-slot ring has epilogue warps");
     unsigned char* st_smem = u.gbase + OFF_STATE;
-    constexpr int NS = kCl ? NSH : NSLOT;   // slots in the ring
+    constexpr int NS = kCl ? NSH : (kR3 ? NSL1 : NSLOT);   // slots in the ring
+    constexpr bool kCtr = kCl || kR3;                        // slot and round kept as counters
     const int w = pt >> 5, lane = pt & 31;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     const int v = pt;
@@ -545,7 +553,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         for (int c = 0; c < first; ++c) load_v(maps, u, c, c);
     // beta of chunk c + 2 goes into the slot during iteration c; it is loaded an iteration
     // ahead (its 2-byte loads, 2H bytes apart, miss the caches)
-    float beta_ahead = (!kCl && w == W_BETA && NSLOT < u.nchunks) ? load_beta<kBetaLogit>(p, u, NSLOT, lane) : 0.f;
+    float beta_ahead = (!kCl && w == W_BETA && NS < u.nchunks) ? load_beta<kBetaLogit>(p, u, NS, lane) : 0.f;
     int issued = first;    // chunks whose boxes were requested
     int vissued = first;   // chunks whose v boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
@@ -580,19 +588,19 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     };
 #pragma unroll 1
     for (int c = 0; ok && c < u.nchunks; ++c) {
-        const int s = kCl ? sc : (c & 1);
+        const int s = kCtr ? sc : (c & 1);
         if (kCl && pt == 0) stamp(c, 0);
-        const uint32_t cpar = c & 1, kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
-        const uint32_t soff = kCl ? slot_off(s) : s * SLOT_BYTES;
+        const uint32_t cpar = c & 1, kpar = kCtr ? (kq & 1) : ((c >> 1) & 1);
+        const uint32_t soff = kCtr ? slot_off(s) : s * SLOT_BYTES;
         const uint32_t slot = u.base + soff;
         const uint32_t tO = TM_O + (kEpi ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
         const bool refill = c + NS < u.nchunks;
         float beta_next = 0.f;
         if constexpr (!kCl) {
-            if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NSLOT);
+            if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NS);
             // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
             beta_next = beta_ahead;
-            if (w == W_BETA && c + NSLOT + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NSLOT + 1, lane);
+            if (w == W_BETA && c + NS + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NS + 1, lane);
         }
 
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
@@ -631,8 +639,8 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
             // The slot's q, k, g regions have been read for the last time: refill them with
             // chunk c + 2 (its boxes were prefetched into L2 at the top of the iteration)
             if (refill) {
-                if (pt == T_TMA) load_qkg(maps, u, c + NSLOT, s);
-                issued = c + NSLOT + 1;
+                if (pt == T_TMA) load_qkg(maps, u, c + NS, s);
+                issued = c + NS + 1;
             }
         }
         // O of this chunk -> staging tile [token][v] in the slot's v region (GEMM1 has read
@@ -700,15 +708,16 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         }
         }
 
-        const int s1 = kCl ? (s + 1 == NS ? 0 : s + 1) : (s ^ 1);
+        const int s1 = kCtr ? (s + 1 == NS ? 0 : s + 1) : (s ^ 1);
         if (c + 1 < u.nchunks) {
             // the bf16 copy of S for the next GEMM1 and the decay by the next chunk's a
             if constexpr (kCl) {
                 if (!warp_wait(bar_addr(u, B_FULLOP + s1), (s1 == 0 ? kq + 1 : kq) & 1, p.status, 256)) { chain_wind_down<kEpi>(c + 1, 0, u.nchunks); break; }
             } else {
-                if (!warp_wait(bar_addr(u, B_AREADY + s1), ((c + 1) >> 1) & 1, p.status, 256)) { chain_wind_down<kEpi>(c + 1, 0, u.nchunks); break; }
+                const uint32_t apar = kCtr ? ((s1 == 0 ? kq + 1 : kq) & 1) : (((c + 1) >> 1) & 1);
+                if (!warp_wait(bar_addr(u, B_AREADY + s1), apar, p.status, 256)) { chain_wind_down<kEpi>(c + 1, 0, u.nchunks); break; }
             }
-            state_pass(reinterpret_cast<const float*>(u.gbase + (kCl ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A));
+            state_pass(reinterpret_cast<const float*>(u.gbase + (kCtr ? slot_off(s1) : s1 * SLOT_BYTES) + SL_A));
             // the output store has had the state pass to read the staging tile: the region
             // takes chunk c + 2's v
             if (!kEpi && pt == T_STORE && refill) {
@@ -725,7 +734,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
                 store_state16(p, srow + piece * 16, r);
             }
         }
-        if constexpr (kCl) {
+        if constexpr (kCtr) {
             sc = s1;
             if (s1 == 0) ++kq;
         }
@@ -735,13 +744,13 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
     if (!kCl && pt == T_TMA) {
         // boxes still in flight must land before the CTA exits (only after a timeout can
         // one be unconsumed)
-        for (int c = issued - NSLOT < 0 ? 0 : issued - NSLOT; c < issued; ++c)
-            mbar_wait_bounded(bar_addr(u, B_FULLTMA + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+        for (int c = issued - NS < 0 ? 0 : issued - NS; c < issued; ++c)
+            mbar_wait_bounded(bar_addr(u, B_FULLTMA + c % NS), (c / NS) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
     if (!kEpi && pt == T_STORE) {
         // likewise the v boxes: the last NS requested (phases before them have completed)
-        for (int c = vissued - NSLOT < 0 ? 0 : vissued - NSLOT; c < vissued; ++c)
-            mbar_wait_bounded(bar_addr(u, B_FULLV + (c & 1)), (c >> 1) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
+        for (int c = vissued - NS < 0 ? 0 : vissued - NS; c < vissued; ++c)
+            mbar_wait_bounded(bar_addr(u, B_FULLV + c % NS), (c / NS) & 1, p.status, KDA_DEVERR_TIMEOUT, WAIT_LIMIT);
     }
 }
 
@@ -751,9 +760,10 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
 // commits each GEMM to its mbarrier (G1, G2, G3).  GEMM1's k blocks 0-3 go out while the chain
 // still converts and decays the second half of S.
 // ------------------------------------------------------------------------------
-template <bool kWarpIssue, bool kCl, bool kSmemState, bool kEpi = kCl>
+template <bool kWarpIssue, bool kCl, bool kSmemState, bool kEpi = kCl, bool kR3 = false>
 __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
-    constexpr int NS = kCl ? NSH : NSLOT;
+    constexpr int NS = kCl ? NSH : (kR3 ? NSL1 : NSLOT);
+    constexpr bool kCtr = kCl || kR3;
     constexpr uint32_t idesc1 = make_idesc_bf16_f32(128, 64);
     constexpr uint32_t idescv = make_idesc_bf16_f32(128, 32, false, true);   // A = V^T, MN-major
     constexpr uint32_t idesc2 = make_idesc_bf16_f32(128, 32);                // GEMM2, and O += U Mqk^T
@@ -778,9 +788,9 @@ __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
     };
 #pragma unroll 1
     for (int c = 0; c < u.nchunks; ++c) {
-        const int s = kCl ? sc : (c & 1);
-        const uint32_t kpar = kCl ? (kq & 1) : ((c >> 1) & 1);
-        const uint32_t slot = u.base + (kCl ? slot_off(s) : s * SLOT_BYTES);
+        const int s = kCtr ? sc : (c & 1);
+        const uint32_t kpar = kCtr ? (kq & 1) : ((c >> 1) & 1);
+        const uint32_t slot = u.base + (kCtr ? slot_off(s) : s * SLOT_BYTES);
         const uint32_t tO = TM_O + (kEpi ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
         // the chunk's operands (the cluster home's chain waited for the pushed chunk before its
         // state pass) and its v box; (cluster home) the epilogue warps have read out chunk c - 2's
@@ -838,7 +848,7 @@ __device__ void mma_warp(const FwdParams& p, const Unit& u, int lane) {
         }
         commit(bar_addr(u, B_G3));
         committed = c + 1;
-        if constexpr (kCl) {
+        if constexpr (kCtr) {
             sc = s + 1 == NS ? 0 : s + 1;
             if (sc == 0) ++kq;
         }
@@ -1284,8 +1294,8 @@ __device__ void home_drain(const FwdParams& p, const Unit& u, const int (&seen)[
 // (lane 0 of warp 9) counts the chunks of home slot hs the chain has finished.
 template <int kNH>
 __device__ void home_epilogue(const FwdParams& p, const TmaMaps& maps, const Unit& u, int et, int (&seen)[NSH]) {
-    // kNH == 0: a CTA with its own prep (one per SM) and two slots, no helpers to signal
-    constexpr int NS = kNH ? NSH : NSLOT, RING = cl_ring(kNH);
+    // kNH == 0: a CTA with its own prep (one per SM) and a ring of three slots, no helpers to signal
+    constexpr int NS = kNH ? NSH : NSL1, RING = cl_ring(kNH);
     const int w = et >> 5, lane = et & 31, v = et;
     const uint32_t lane_addr = u.tmem + ((uint32_t)(w * 32) << 16);
     // chunks whose v boxes have been requested: the chain loads the first NS, this thread the rest
@@ -1492,14 +1502,16 @@ __global__ void __launch_bounds__((kWarpIssue && !kCl && !kSmemState) ? TC_THREA
     u.tmem = home ? *reinterpret_cast<volatile uint32_t*>(u.gbase + OFF_TMEMADDR) : 0u;
 
     if constexpr (!kCl) {
+        // one CTA per SM (kLoneEpi): a ring of three slots
+        constexpr int kRing = kLoneEpi ? NSL1 : NSLOT;
         if (warp < W_PREP0) {
-            chain_group<kBf16State, kWarpIssue, kBetaLogit, false, kSmemState, kLoneEpi>(p, maps, u, tid);
+            chain_group<kBf16State, kWarpIssue, kBetaLogit, false, kSmemState, kLoneEpi, kLoneEpi>(p, maps, u, tid);
         } else if (warp < W_INV) {
-            prep_group<kSoftplus, 1>(p, u, tid - W_PREP0 * 32, 0, u.nchunks);
+            prep_group<kSoftplus, 1, kRing>(p, u, tid - W_PREP0 * 32, 0, u.nchunks);
         } else if (warp == W_INV) {
-            inverse_warp(p, u, tid & 31, u.nchunks);
+            inverse_warp<kRing>(p, u, tid & 31, u.nchunks);
         } else if (warp == W_ISSUE) {
-            mma_warp<kWarpIssue, false, kSmemState, kLoneEpi>(p, u, tid & 31);
+            mma_warp<kWarpIssue, false, kSmemState, kLoneEpi, kLoneEpi>(p, u, tid & 31);
         } else if (kLoneEpi) {
             home_epilogue<0>(p, maps, u, tid & 127, seen);   // warps 14-17: TMEM lanes 32 (warp % 4) ..
         }
@@ -1688,9 +1700,11 @@ cudaError_t launch_fwd_tc(const FwdParams& p, cudaStream_t stream, bool bf16_sta
         {{kda_fwd_tc_kernel<false, true, false, false>, kda_fwd_tc_kernel<false, true, false, true>},
          {kda_fwd_tc_kernel<false, true, true, false>, kda_fwd_tc_kernel<false, true, true, true>}}};
     auto kernel = bf16_state ? kda_fwd_tc_kernel<true, false, false, false> : table[lone][sp][lg];
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    const bool le = lone && !bf16_state;   // one CTA per SM: epilogue warps and a ring of three slots
+    const uint32_t smem = le ? SMEM_BYTES_LE : SMEM_BYTES;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kernel<<<units, (lone && !bf16_state) ? TC_THREADS_LE : TC_THREADS, SMEM_BYTES, stream>>>(p, maps);
+    kernel<<<units, le ? TC_THREADS_LE : TC_THREADS, smem, stream>>>(p, maps);
     return cudaGetLastError();
 }
 

@@ -460,16 +460,18 @@ class RingRun:
     `sync_handoffs` = a wound-down chain warp syncs on the hand-off barriers (False: it only
     arrives, as on the fast path); `epi` = the one-CTA-per-SM instantiation, whose four
     epilogue warps read each chunk's O out (OREADY from the chain, OFREE back to the MMA warp
-    for the chunk two later), stage and store it and refill the slot's v."""
+    for the chunk two later), stage and store it and refill the slot's v, over a ring of
+    three slots (chunk c in slot c % 3) instead of two."""
 
     def __init__(self, n, seed, perturb=None, limit=40, wind_down=True, sync_handoffs=True, epi=False):
         self.n, self.rng, self.perturb, self.limit, self.wind_down = n, random.Random(seed), perturb, limit, wind_down
         self.sync_handoffs, self.epi = sync_handoffs, epi
+        self.ns = 3 if epi else 2
         self.bars, self.engines, self.timeouts, self.consumed = {}, [], 0, []
         self.chain_bar, self.prep_bar, self.cta_bar = NamedBar(4), NamedBar(8), NamedBar(18 if epi else 14)
         self.epi_bar = NamedBar(4)
         self.hand = {k: HandBar(5, k) for k in HANDOFFS}   # 4 chain warps + the MMA warp
-        self.fulltma_fill = {0: 0, 1: 0}
+        self.fulltma_fill = {s: 0 for s in range(self.ns)}
         self.exited = 0
 
     def bar(self, *key):
@@ -513,7 +515,7 @@ class RingRun:
         self.engines.append(run())
 
     def fulltma(self, c):
-        s = c & 1
+        s = c % self.ns
         self.fulltma_fill[s] += 1
         if self.fulltma_fill[s] == 2:   # the box bytes and the 32 beta lanes, as two events
             self.fulltma_fill[s] = 0
@@ -568,15 +570,15 @@ class RingRun:
             j, k = j + 1, 0
 
     def chain_warp(self, w):
-        n = self.n
-        issued_qkg = issued_v = min(n, 2)
+        n, ns = self.n, self.ns
+        issued_qkg = issued_v = min(n, ns)
         if n > 0:
-            for c in range(min(n, 2)):
+            for c in range(min(n, ns)):
                 if w == 2:
                     self.load_qkg(c)
                     self.fulltma(c)                       # beta
                 if w == 3:
-                    self.engine("FULLV", c >> 1, c)
+                    self.engine("FULLV", 0, c)
             ok = yield from self.bwait(self.bar("AREADY", 0), 0)
             if ok:                                        # the state pass, handed over in halves
                 yield WORK
@@ -586,7 +588,7 @@ class RingRun:
             else:
                 yield from self.chain_wind_down(w, 0, 0)
             for c in range(n if ok else 0):
-                s, k, refill = c & 1, c >> 1, c + 2 < n
+                s, k, refill = c % ns, c // ns, c + ns < n
                 if not (yield from self.bwait(self.bar("G1"), c)):
                     yield from self.chain_wind_down(w, c, 1)
                     break
@@ -594,7 +596,7 @@ class RingRun:
                     yield from self.chain_wind_down(w, c, 1)
                     break
                 if refill and w == 2:
-                    self.fulltma(c + 2)                   # beta of chunk c + 2
+                    self.fulltma(c + ns)                  # beta of chunk c + ns
                 self.hand_off(w, "G2")
                 if not (yield from self.bwait(self.bar("G2"), c)):
                     yield from self.chain_wind_down(w, c, 2)
@@ -604,8 +606,8 @@ class RingRun:
                     yield from self.chain_wind_down(w, c, 3)
                     break
                 if refill and w == 2:
-                    self.load_qkg(c + 2)
-                    issued_qkg = c + 3
+                    self.load_qkg(c + ns)
+                    issued_qkg = c + ns + 1
                 if self.epi:
                     if w == 0:                            # the epilogue warps take the output
                         self.arrive("OREADY", c >> 1, c & 1)
@@ -614,7 +616,7 @@ class RingRun:
                 if w == 0:
                     self.consumed.append(c)
                 if c + 1 < n:
-                    if not (yield from self.bwait(self.bar("AREADY", s ^ 1), (c + 1) >> 1)):
+                    if not (yield from self.bwait(self.bar("AREADY", (c + 1) % ns), (c + 1) // ns)):
                         yield from self.chain_wind_down(w, c + 1, 0)
                         break
                     yield WORK
@@ -622,20 +624,21 @@ class RingRun:
                     yield WORK
                     self.hand_off(w, "G1B")
                     if w == 3 and refill and not self.epi:
-                        self.engine("FULLV", (c + 2) >> 1, s)
-                        issued_v = c + 3
+                        self.engine("FULLV", (c + ns) // ns, s)
+                        issued_v = c + ns + 1
             # boxes still in flight must land before the CTA exits (bounded waits)
             if w == 2:
-                for c in range(max(0, issued_qkg - 2), issued_qkg):
-                    yield from self.bwait(self.bar("FULLTMA", c & 1), c >> 1)
+                for c in range(max(0, issued_qkg - ns), issued_qkg):
+                    yield from self.bwait(self.bar("FULLTMA", c % ns), c // ns)
             if w == 3 and not self.epi:
-                for c in range(max(0, issued_v - 2), issued_v):
-                    yield from self.bwait(self.bar("FULLV", c & 1), c >> 1)
+                for c in range(max(0, issued_v - ns), issued_v):
+                    yield from self.bwait(self.bar("FULLV", c % ns), c // ns)
         yield from self.cta_bar.sync()
         self.exited += 1
 
     def epi_warp(self, ew):
-        n, vissued = self.n, min(self.n, 2)
+        n, ns = self.n, self.ns
+        vissued = min(n, ns)
         for c in range(n):
             if not (yield from self.bwait(self.bar("OREADY", c & 1), c >> 1)):
                 if self.wind_down:                        # the epilogue group's barriers still ahead
@@ -646,23 +649,23 @@ class RingRun:
             yield from self.epi_bar.sync()
             if ew == 0:
                 self.arrive("OFREE", c >> 1, c & 1)
-                if c + 2 < n:                             # the stores have read the tile: next v
-                    self.engine("FULLV", (c + 2) >> 1, c & 1)
-                    vissued = c + 3
+                if c + ns < n:                            # the stores have read the tile: next v
+                    self.engine("FULLV", (c + ns) // ns, c % ns)
+                    vissued = c + ns + 1
         if ew == 0:
-            for c in range(max(0, vissued - 2), vissued):
-                yield from self.bwait(self.bar("FULLV", c & 1), c >> 1)
+            for c in range(max(0, vissued - ns), vissued):
+                yield from self.bwait(self.bar("FULLV", c % ns), c // ns)
         yield from self.cta_bar.sync()
         self.exited += 1
 
     def mma_warp(self):
         committed = 0
         for c in range(self.n):
-            s, k = c & 1, c >> 1
+            s, k = c % self.ns, c // self.ns
             ok = yield from self.bwait(self.bar("FULLP", s), k)
             ok = ok and (yield from self.bwait(self.bar("FULLV", s), k))
             if self.epi and c >= 2:                       # the O buffer of chunk c - 2 is read out
-                ok = ok and (yield from self.bwait(self.bar("OFREE", s), k - 1))
+                ok = ok and (yield from self.bwait(self.bar("OFREE", c & 1), (c >> 1) - 1))
             if not ok:
                 yield from self.mma_wind_down(c)
                 break
@@ -684,7 +687,7 @@ class RingRun:
 
     def prep_warp(self, pw):
         for j in range(self.n):
-            s, k = j & 1, j >> 1
+            s, k = j % self.ns, j // self.ns
             if not (yield from self.bwait(self.bar("FULLTMA", s), k)):
                 yield from self.prep_wind_down(j, 0)
                 break
@@ -692,23 +695,23 @@ class RingRun:
             yield from self.prep_bar.sync()               # end of the prefix scan
             yield from self.prep_bar.sync()               # end of phase B
             if pw == 0:
-                self.arrive("AREADY", j >> 1, s)
+                self.arrive("AREADY", k, s)
             if pw in (1, 2, 3) and j > 0 and not (yield from self.bwait(self.bar("LFREE"), j - 1)):
                 yield from self.prep_wind_down(j, 3)
                 break
             yield from self.prep_bar.sync()               # end of phase C
             if pw == 0:
-                self.arrive("FULLP", j >> 1, s)
+                self.arrive("FULLP", k, s)
         yield from self.cta_bar.sync()
         self.exited += 1
 
     def inverse_warp(self):
         for j in range(self.n):
-            s, k = j & 1, j >> 1
+            s, k = j % self.ns, j // self.ns
             if not (yield from self.bwait(self.bar("FULLP", s), k)):
                 break
             self.arrive("LFREE", j)
-            self.arrive("FULLD", j >> 1, s)
+            self.arrive("FULLD", k, s)
         yield from self.cta_bar.sync()
         self.exited += 1
 
@@ -737,7 +740,8 @@ class RingRun:
 
 PERTURB = [("FULLD", 1), ("FULLP", 2), ("AREADY", 1), ("LFREE", 2), ("G1", 3), ("G2", 0), ("G3", 4),
            ("FULLV", 1), ("FULLTMA", 3), ("AREADY", 0), ("FULLTMA", 0)]
-PERTURB_EPI = PERTURB + [("OREADY", 1), ("OFREE", 0), ("OREADY", 0), ("OFREE", 1)]
+PERTURB_EPI = PERTURB + [("OREADY", 1), ("OFREE", 0), ("OREADY", 0), ("OFREE", 1), ("FULLTMA", 4), ("AREADY", 2),
+                         ("FULLV", 0)]
 
 
 @pytest.mark.parametrize("epi", [False, True])
@@ -764,8 +768,8 @@ def test_every_warp_winds_down_after_an_expired_wait(name, index, mode):
 @pytest.mark.parametrize("name,index", PERTURB_EPI)
 def test_every_warp_winds_down_with_epilogue_warps(name, index, mode):
     """The same with the one-CTA-per-SM instantiation's epilogue warps (OREADY, OFREE, and v
-    refilled by the epilogue)."""
-    for n in (6, 10):
+    refilled by the epilogue, over three slots)."""
+    for n in (8, 11):
         for seed in range(30):
             r = RingRun(n, seed, perturb=(name, index, mode), epi=True).run()
             if mode == "withhold":
