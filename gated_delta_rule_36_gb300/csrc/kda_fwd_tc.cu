@@ -1634,12 +1634,12 @@ cudaError_t clusters_fit(int dev, uint32_t flags, int nh, long long units, bool*
 size_t fwd_tc_smem_bytes() { return SMEM_BYTES; }
 
 // One CTA per unit, two on an SM, when the units outnumber the SMs; with at most a quarter
-// as many units as SMs, a cluster of four CTAs per unit, and with at most 2/7 as many a
+// as many units as SMs, a cluster of four CTAs per unit, and with at most 7/25 as many a
 // cluster of two, if every cluster can be resident at once (clusters must fit the GPCs);
 // else one CTA per unit with an SM to itself.  (Clusters of two are paced by their one
-// helper's prep: on GB300 they beat one CTA per SM at 40 units, 0.48 against 0.53 ms for
-// 8,192 tokens, and lose from about 48 units on, by 18 % at 76.)  The bf16-state ablation keeps its one
-// instantiation.
+// helper: on GB300, at 8,192 tokens a unit, they take 0.478 ms up to 42 units against 0.520
+// for one CTA per SM, and 0.534 from 43 units on, a step measured at every count from 37 to
+// 46; 7/25 of the 152 SMs is 42.6.)  The bf16-state ablation keeps its one instantiation.
 cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, int* sched) {
     *sched = KDA_SCHEDULE_TWO_PER_SM;
     if (bf16_state || units <= 0) return cudaSuccess;
@@ -1650,7 +1650,7 @@ cudaError_t fwd_tc_schedule(long long units, uint32_t flags, bool bf16_state, in
     if (units > sms) return cudaSuccess;
     *sched = KDA_SCHEDULE_ONE_PER_SM;
     for (int nh : {3, 1}) {
-        if (units * (nh + 1) > sms || (nh == 1 && units * 7 > 2LL * sms)) continue;
+        if (units * (nh + 1) > sms || (nh == 1 && units * 25 > 7LL * sms)) continue;
         bool fit = false;
         e = clusters_fit(dev, flags, nh, units, &fit);
         if (e != cudaSuccess) return e;

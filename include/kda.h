@@ -170,7 +170,7 @@ kda_status kda_fwd_ex(const kda_tensor* q, const kda_tensor* k, const kda_tensor
  *                            prepare its chunks (up to a quarter as many units as SMs, when
  *                            every cluster can be resident at once)
  *   KDA_SCHEDULE_CLUSTER2    a cluster of two CTAs per unit: one runs the recurrence, one
- *                            prepares its chunks (up to 2/7 as many units as SMs, when the
+ *                            prepares its chunks (up to 7/25 as many units as SMs, when the
  *                            clusters of four do not apply and every cluster of two can be
  *                            resident at once)
  * A unit's arithmetic is the same in every schedule: outputs and states do not depend on it.
@@ -196,6 +196,8 @@ kda_status kda_fwd_schedule(int64_t units, uint32_t flags, int32_t* schedule);
  *   1 the MMA warp waits for the chunk's v    5 -R is in bf16 in Tensor Memory
  *   2 v has landed                            6 GEMM2's operands are ready
  *   3 GEMM1 is issued                         7 GEMM2 is issued
+ * (points 0 and 4-6 are read by thread 0 of the chain, 1-3 and 7 by the MMA warp; point 6
+ * is read after thread 0's non-blocking hand-off, so it can come a few cycles after 7.)
  * Other launches and entries leave the buffer untouched; outputs do not depend on tracing.
  * The caller owns the buffer, which the traced launches write on their streams: it must
  * stay allocated until they complete.  kda_fwd_set_trace(NULL, 0, 0) turns it off.  A

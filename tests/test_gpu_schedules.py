@@ -1,7 +1,7 @@
 """The launch schedules of the prefill kernel, and that they do not change the numbers.
 
 More (sequence, head) units than SMs run two CTAs to an SM; up to one unit per SM, one CTA
-per SM; up to 2/7 as many units as SMs, a cluster of two CTAs per unit, and up to a quarter
+per SM; up to 7/25 as many units as SMs, a cluster of two CTAs per unit, and up to a quarter
 as many a cluster of four (one CTA runs the recurrence over state resident in its Tensor
 Memory, the others prepare chunks for it and push them into its shared memory).  A unit's
 arithmetic is the same in each, so the same sequences must give bit-identical outputs and
@@ -67,7 +67,7 @@ def _lens(n, seed):
 def test_schedule_thresholds():
     sms, cmax, cmax2 = _sms(), _cluster_max(), _cluster2_max()
     print(f"[schedule] SMs {sms}, clusters of four up to {cmax} units, of two up to {cmax2}")
-    assert 1 <= cmax <= sms // 4 < cmax2 <= 2 * sms // 7
+    assert 1 <= cmax <= sms // 4 < cmax2 <= 7 * sms // 25
     want = lambda u: (kb.KDA_SCHEDULE_CLUSTER if u <= cmax else kb.KDA_SCHEDULE_CLUSTER2 if u <= cmax2 else
                       kb.KDA_SCHEDULE_ONE_PER_SM if u <= sms else kb.KDA_SCHEDULE_TWO_PER_SM)
     for u in sorted({1, 2, cmax, cmax + 1, sms // 4 + 1, cmax2, cmax2 + 1, sms // 2, sms // 2 + 1, sms - 1, sms,
@@ -178,5 +178,8 @@ def test_chain_trace_records_one_unit_without_changing_the_numbers():
         r = t[c].tolist()
         assert r[0] <= r[4] <= r[5] <= r[6], r      # thread 0, in program order
         assert r[1] <= r[2] <= r[3] <= r[7], r      # the MMA warp, in program order
-        assert r[3] < r[4] and r[6] <= r[7], r      # GEMM1 completes after its issue; GEMM2 issues after its operands
+        # GEMM1 completes after its issue; GEMM2 issues after -R is in place.  (Point 6 is read
+        # after thread 0's non-blocking arrival on the hand-off, so the MMA warp may pass the
+        # barrier and stamp GEMM2's issue before thread 0 reads its clock: no order there.)
+        assert r[3] < r[4] and r[5] <= r[7], r
     assert (t[1:nch, 0] > t[: nch - 1, 7]).all()    # chunks run in order
