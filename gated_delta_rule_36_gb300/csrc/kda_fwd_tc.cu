@@ -465,16 +465,29 @@ __device__ __forceinline__ void prefetch_chunk(const TmaMaps& maps, const Unit& 
     tma_prefetch_l2_3d(&maps.v, 64, u.h, t0);
 }
 
-// beta of token `lane` of chunk c (0 past the end), by a plain load: its token stride
-// is 2H bytes, too narrow for a tensor box when H is small.  kBetaLogit (KDA_FLAG_BETA_LOGIT):
-// the stored value is a logit and beta = sigmoid(logit).
-template <bool kBetaLogit>
-__device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, int c, int lane) {
+// beta of token `lane` of chunk c, by a plain load: its token stride is 2H bytes, too narrow
+// for a tensor box when H is small.  The load is predicated and its bits are kept as they are
+// (BETA_NONE past the end), so a warp that loads beta ahead does not wait for the load until
+// it uses the value (beta_of).  kBetaLogit (KDA_FLAG_BETA_LOGIT): the stored value is a logit
+// and beta = sigmoid(logit).
+constexpr uint32_t BETA_NONE = 0x10000u;   // no token: beta = 0 (not a 16-bit pattern)
+__device__ __forceinline__ uint32_t load_beta_bits(const FwdParams& p, const Unit& u, int c, int lane) {
     const int64_t t0 = u.bos + (int64_t)c * CH;
-    if (lane >= chunk_valid(u, c)) return 0.f;
-    const float b = bf16_bits_to_f32(reinterpret_cast<const uint16_t*>(p.beta)[KDA_CHK((t0 + lane) * p.H + u.h, 0, p.T_total * p.H)]);
+    uint32_t raw = BETA_NONE;
+    if (lane < chunk_valid(u, c))
+        raw = reinterpret_cast<const uint16_t*>(p.beta)[KDA_CHK((t0 + lane) * p.H + u.h, 0, p.T_total * p.H)];
+    return raw;
+}
+template <bool kBetaLogit>
+__device__ __forceinline__ float beta_of(uint32_t raw) {
+    if (raw == BETA_NONE) return 0.f;
+    const float b = bf16_bits_to_f32((uint16_t)raw);
     if constexpr (kBetaLogit) return rcp_approx(1.f + ex2_approx(-b * LOG2E));
     return b;
+}
+template <bool kBetaLogit>
+__device__ __forceinline__ float load_beta(const FwdParams& p, const Unit& u, int c, int lane) {
+    return beta_of<kBetaLogit>(load_beta_bits(p, u, c, lane));
 }
 
 __device__ __forceinline__ void put_beta(const Unit& u, int s, int lane, float b) {
@@ -553,7 +566,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         for (int c = 0; c < first; ++c) load_v(maps, u, c, c);
     // beta of chunk c + 2 goes into the slot during iteration c; it is loaded an iteration
     // ahead (its 2-byte loads, 2H bytes apart, miss the caches)
-    float beta_ahead = (!kCl && w == W_BETA && NS < u.nchunks) ? load_beta<kBetaLogit>(p, u, NS, lane) : 0.f;
+    uint32_t beta_ahead = (!kCl && w == W_BETA && NS < u.nchunks) ? load_beta_bits(p, u, NS, lane) : BETA_NONE;
     int issued = first;    // chunks whose boxes were requested
     int vissued = first;   // chunks whose v boxes were requested
     {   // -I: B operand of P -= V^T; thread = (row n, 8-column block)
@@ -595,12 +608,12 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         const uint32_t slot = u.base + soff;
         const uint32_t tO = TM_O + (kEpi ? TM_OP_STRIDE * (uint32_t)(c & 1) : 0u), tP = tO + 32;
         const bool refill = c + NS < u.nchunks;
-        float beta_next = 0.f;
+        uint32_t beta_next = BETA_NONE;
         if constexpr (!kCl) {
             if (pt == T_TMA && refill) prefetch_chunk(maps, u, c + NS);
             // chunk c + 2's beta goes into the slot once the inverse warp is done with this one's
             beta_next = beta_ahead;
-            if (w == W_BETA && c + NS + 1 < u.nchunks) beta_ahead = load_beta<kBetaLogit>(p, u, c + NS + 1, lane);
+            if (w == W_BETA && c + NS + 1 < u.nchunks) beta_ahead = load_beta_bits(p, u, c + NS + 1, lane);
         }
 
         // -R = P - V^T -> bf16 -> TMEM: A operand of GEMM2, which also waits for -B2
@@ -612,7 +625,7 @@ __device__ void chain_group(const FwdParams& p, const TmaMaps& maps, const Unit&
         if (kCl && pt == 0) stamp(c, 5);
         if constexpr (!kCl) {
             if (!warp_wait(bar_addr(u, B_FULLD + s), kpar, p.status, 64)) { chain_wind_down<kEpi>(c, 1, u.nchunks); break; }
-            if (refill && w == W_BETA) put_beta(u, s, lane, beta_next);
+            if (refill && w == W_BETA) put_beta(u, s, lane, beta_of<kBetaLogit>(beta_next));
         }
         tc_fence_before();
         named_bar_arrive(NB_G2, NB_HAND);
